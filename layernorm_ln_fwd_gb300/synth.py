@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs for the fused residual-add + LayerNorm workloads.
+
+This module holds random draws only -- none of the method's arithmetic -- so that the CUDA
+path and the float64 oracle can be fed identical inputs without sharing any code.
+
+Recipe (every workload): a CPU ``torch.Generator`` seeded with ``seed`` draws, in this order,
+x, res, dy (each [rows, cols]), gamma and beta ([cols]) as float32 from the stated
+distributions; each tensor is then cast to the I/O dtype (bf16 casts round to nearest even).
+gamma ~ N(1, 0.1), beta ~ N(0, 0.1) and eps = 1e-5 in every workload.
+
+The shapes follow the Transformer shapes on the pages: 8 sequences x 1024 tokens with
+hidden size 768 (GPT-2 small, the width llm.c uses) and 1280 (GPT-2 large, the shape the
+whole-step accounting in "Accelerating Transformer on GPU (II): Training with LightSeq2",
+section 1.2, uses), plus a wide-row case with a large mean (the cancellation experiment of
+"Accelerating Transformer on GPU (I)", section 4.2) and a large fp32 case whose width is
+not a multiple of the 128-column warp stride.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+EPS = 1e-5
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    dtype: str  # "f32" or "bf16": the I/O (storage) dtype; arithmetic is fp32
+    rows: int
+    cols: int
+    x: tuple = ("normal", 0.0, 1.0)
+    res: tuple = ("normal", 0.0, 1.0)
+    dy: tuple = ("normal", 0.0, 1.0)
+    gamma: tuple = ("normal", 1.0, 0.1)
+    beta: tuple = ("normal", 0.0, 0.1)
+    eps: float = EPS
+    note: str = field(default="", compare=False)
+
+
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("f32_64x768", "f32", 64, 768,
+                 note="small fp32 case the oracle finishes in well under a second"),
+        Workload("bf16_8192x768", "bf16", 8192, 768,
+                 note="GPT-2 small shape: 8 x 1024 tokens, hidden 768"),
+        Workload("bf16_8192x1280", "bf16", 8192, 1280,
+                 note="GPT-2 large shape: 8 x 1024 tokens, hidden 1280"),
+        Workload("bf16_4096x8192_mean100", "bf16", 4096, 8192, x=("normal", 100.0, 1.0),
+                 note="wide rows; x has mean 100 (stresses E[x^2]-E[x]^2 cancellation)"),
+        Workload("f32_262144x1000", "f32", 262144, 1000, x=("uniform", -3.0, 3.0),
+                 res=("normal", 0.0, 0.5),
+                 note="large fp32 case, 1000 columns: ragged against the warp stride"),
+    ]
+}
+
+# The workload the benchmark times (the GPT-2 small shape).
+BENCH_WORKLOAD = "bf16_8192x768"
+
+
+def torch_dtype(dtype: str):
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
+
+
+def _draw(gen: torch.Generator, shape, dist) -> torch.Tensor:
+    kind, a, b = dist
+    if kind == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32) * b + a
+    if kind == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * (b - a) + a
+    if kind == "int":  # integers drawn uniformly from [a, b]
+        return torch.randint(int(a), int(b) + 1, shape, generator=gen).to(torch.float32)
+    if kind == "const":
+        return torch.full(shape, float(a), dtype=torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def make_inputs(rows: int, cols: int, dtype: str, seed: int = 0, x=("normal", 0.0, 1.0),
+                res=("normal", 0.0, 1.0), dy=("normal", 0.0, 1.0), gamma=("normal", 1.0, 0.1),
+                beta=("normal", 0.0, 0.1)) -> dict:
+    """CPU tensors in the I/O dtype: x, res, dy [rows, cols]; gamma, beta [cols]."""
+    gen = torch.Generator().manual_seed(int(seed))
+    td = torch_dtype(dtype)
+    out = {}
+    for name, shape, dist in (("x", (rows, cols), x), ("res", (rows, cols), res),
+                              ("dy", (rows, cols), dy), ("gamma", (cols,), gamma),
+                              ("beta", (cols,), beta)):
+        out[name] = _draw(gen, shape, dist).to(td).contiguous()
+    return out
+
+
+def workload_inputs(name: str, seed: int = 0) -> dict:
+    w = WORKLOADS[name]
+    return make_inputs(w.rows, w.cols, w.dtype, seed=seed, x=w.x, res=w.res, dy=w.dy,
+                       gamma=w.gamma, beta=w.beta)

@@ -1,0 +1,170 @@
+"""Float64 CPU oracle for fused residual-add + LayerNorm -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl reference``
+legs of ``bench.py`` may import this package.  The CUDA library never calls it and shares no
+code with it.
+
+Two independent implementations of the same definitions live here:
+
+* ``ln_oracle.c`` (float64 C, OpenMP over rows; built into ``libln_oracle.so`` by
+  :func:`build`) -- the oracle proper, fast enough for the full-size configurations;
+* ``numpy_ref.py`` (float64 NumPy, vectorised) -- a twin for small shapes, used to
+  cross-check the C code.
+
+Definitions followed (page titles and sections):
+
+* forward: "Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1
+  (xhat = (x - mu)/sigma, sigma = sqrt(var + eps), y = gamma*xhat + beta; mu and 1/sigma
+  saved per row); biased variance as in "AI infra learning log (2): LayerNorm operator
+  optimisation", section 2.1; residual sum written out first and normalised, as in
+  "llm.c: the llmc/ CUDA kernel layer", section 3.2;
+* backward: HW4 form and slides form of dx, dgamma = sum_rows dy*xhat, dbeta = sum_rows dy
+  ("Training with LightSeq2", sections 2.1 and 2.4).
+
+Every function here is pinned by tests marked ``not gpu`` (finite differences, torch float64
+autograd, invariants, the pages' worked example, agreement of the two backward forms).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from . import numpy_ref  # noqa: F401  (re-exported for tests)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ln_oracle.c")
+_LIB = os.path.join(_HERE, "libln_oracle.so")
+
+IO_CODES = {"f64": 0, "f32": 1, "bf16": 2}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``ln_oracle.c`` with gcc (no fast-math, no FMA contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            d = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.c_int64
+            lib.oracle_ln_fwd.argtypes = [d, d, d, d, ctypes.c_double, i64, i64, ctypes.c_int,
+                                          d, d, d, d, ctypes.c_int]
+            lib.oracle_ln_fwd.restype = None
+            lib.oracle_ln_bwd.argtypes = [d, d, d, d, d, i64, i64, ctypes.c_int, d, d, d,
+                                          ctypes.c_int]
+            lib.oracle_ln_bwd.restype = None
+            lib.oracle_ln_bwd_dx_slides.argtypes = [d, d, d, d, d, i64, i64, d, ctypes.c_int]
+            lib.oracle_ln_bwd_dx_slides.restype = None
+            lib.oracle_round_io.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.oracle_round_io.restype = ctypes.c_double
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def round_io(v, io: str):
+    """Round float64 values to the I/O precision (round to nearest even)."""
+    lib = _load()
+    arr = _f64(v)
+    flat = arr.reshape(-1)
+    out = np.empty_like(flat)
+    code = IO_CODES[io]
+    for i in range(flat.size):
+        out[i] = lib.oracle_round_io(float(flat[i]), code)
+    return out.reshape(arr.shape)
+
+
+def ln_fwd(x, res, gamma, beta, eps: float, io: str = "f64", threads: int = 0,
+           want_out: bool = True, want_res_out: bool = True):
+    """Forward of the fused residual-add + LayerNorm.
+
+    ``x``, ``res``: [rows, cols] (``res`` may be None); ``gamma``, ``beta``: [cols].
+    Returns a dict with ``out``, ``res_out`` (rounded to ``io``), ``mean`` and ``rstd``
+    (float64, unrounded).
+    """
+    x = _f64(x)
+    rows, cols = x.shape
+    res = _f64(res)
+    gamma = _f64(gamma)
+    beta = _f64(beta)
+    assert gamma.shape == (cols,) and beta.shape == (cols,)
+    if res is not None:
+        assert res.shape == x.shape
+    out = np.empty((rows, cols)) if want_out else None
+    res_out = np.empty((rows, cols)) if want_res_out else None
+    mean = np.empty(rows)
+    rstd = np.empty(rows)
+    _load().oracle_ln_fwd(_ptr(x), _ptr(res), _ptr(gamma), _ptr(beta), float(eps), rows, cols,
+                          IO_CODES[io], _ptr(out), _ptr(res_out), _ptr(mean), _ptr(rstd),
+                          int(threads))
+    return {"out": out, "res_out": res_out, "mean": mean, "rstd": rstd}
+
+
+def ln_bwd(dy, xr, gamma, mean, rstd, io: str = "f64", threads: int = 0, want_dx: bool = True,
+           want_dparams: bool = True):
+    """Backward (HW4 form).  ``xr`` is the tensor the forward normalised (the stored residual
+    sum when the forward had a residual, else x).  Returns ``dx`` [rows, cols] and
+    ``dgamma``, ``dbeta`` [cols], rounded to ``io``."""
+    dy = _f64(dy)
+    rows, cols = dy.shape
+    xr = _f64(xr)
+    gamma = _f64(gamma)
+    mean = _f64(mean)
+    rstd = _f64(rstd)
+    assert xr.shape == dy.shape and gamma.shape == (cols,)
+    assert mean.shape == (rows,) and rstd.shape == (rows,)
+    dx = np.empty((rows, cols)) if want_dx else None
+    dgamma = np.empty(cols) if want_dparams else None
+    dbeta = np.empty(cols) if want_dparams else None
+    _load().oracle_ln_bwd(_ptr(dy), _ptr(xr), _ptr(gamma), _ptr(mean), _ptr(rstd), rows, cols,
+                          IO_CODES[io], _ptr(dx), _ptr(dgamma), _ptr(dbeta), int(threads))
+    return {"dx": dx, "dgamma": dgamma, "dbeta": dbeta}
+
+
+def ln_bwd_dx_slides(dy, xr, gamma, mean, rstd, threads: int = 0):
+    """dx by the slides form (raw x in the second sum), float64, unrounded."""
+    dy = _f64(dy)
+    rows, cols = dy.shape
+    xr = _f64(xr)
+    gamma = _f64(gamma)
+    mean = _f64(mean)
+    rstd = _f64(rstd)
+    dx = np.empty((rows, cols))
+    _load().oracle_ln_bwd_dx_slides(_ptr(dy), _ptr(xr), _ptr(gamma), _ptr(mean), _ptr(rstd),
+                                    rows, cols, _ptr(dx), int(threads))
+    return dx

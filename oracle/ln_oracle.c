@@ -1,0 +1,242 @@
+/*
+ * ln_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, float64 CPU oracle for the fused residual-add + LayerNorm forward and
+ * backward.  Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load it; the CUDA library never links or calls it, and it shares no code with it.
+ *
+ * Sources (page titles and sections; the pages are course notes and blog posts):
+ *  - Forward definition, per row of length m:
+ *      xhat_i = (x_i - mu) / sigma,  sigma = sqrt(var + eps),  y_i = gamma_i * xhat_i + beta_i,
+ *    with mu and r = 1/sigma saved per row.
+ *    ("Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1.)
+ *    The variance is the biased one (divide by m), the way the one-thread-per-row kernel of
+ *    "AI infra learning log (2): LayerNorm operator optimisation", section 2.1 (v1), computes it.
+ *  - Fused residual: the residual sum s = inp1 + inp2 is written out first and then
+ *    normalised ("llm.c: the llmc/ CUDA kernel layer", section 3.2, fused_residual_forward5).
+ *    Reading taken here: the STORED residual (s rounded to the I/O precision) is what gets
+ *    normalised, so that the backward, which only sees that stored tensor, differentiates
+ *    exactly the function the forward evaluated.
+ *  - Backward, "HW4 form" ("Training with LightSeq2", section 2.1): with g_i = gamma_i * dy_i,
+ *      dx_i = r * [ g_i - (sum_j g_j + xhat_i * sum_j g_j xhat_j) / m ].
+ *  - Backward, "slides form" (same section), used only as an independent cross-check:
+ *      dx_i = g_i / sigma + alpha_i sum_j g_j + beta_i sum_j g_j x_j,
+ *      alpha_i = ((x_i - mu) mu - sigma^2) / (m sigma^3),  beta_i = (mu - x_i) / (m sigma^3).
+ *  - Column gradients ("Training with LightSeq2", sections 2.1 and 2.4):
+ *      dgamma_j = sum over rows of dy * xhat,   dbeta_j = sum over rows of dy.
+ *
+ * Precision: every stored input is an exact float64 upcast of an fp32 or bf16 value.  All
+ * arithmetic is float64.  Results that the GPU stores in the I/O precision are rounded here
+ * to that precision with round-to-nearest-even ("io" = 0: no rounding, 1: fp32, 2: bf16).
+ * Mean and rstd are returned unrounded (float64).
+ *
+ * Threads: rows are independent, so the row loops run in parallel over rows.  The column
+ * sums run in parallel over columns, each column summed over rows in row order, which is
+ * the definition's order.  Nothing is blocked, fused or reordered beyond that.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define IO_F64 0
+#define IO_F32 1
+#define IO_BF16 2
+
+/* Largest finite bf16: (2 - 2^-7) * 2^127. */
+static const double kBf16Max = 3.3895313892515355e38;
+
+/* Round a float64 value to the nearest bf16 value, ties to even.  bf16 keeps 8 significant
+ * bits and the fp32 exponent range; below 2^-126 the spacing is fixed at 2^-133. */
+static double round_to_bf16(double v) {
+    if (v == 0.0 || isnan(v) || isinf(v)) return v;
+    int e;
+    (void)frexp(v, &e); /* |v| = f * 2^e with f in [0.5, 1) */
+    int qexp = e - 8;   /* spacing of 8-significant-bit numbers in [2^(e-1), 2^e) */
+    if (qexp < -133) qexp = -133;
+    double q = ldexp(1.0, qexp);
+    double r = nearbyint(v / q) * q; /* v/q is exact; nearbyint rounds ties to even */
+    if (fabs(r) > kBf16Max) r = copysign(INFINITY, v);
+    return r;
+}
+
+static double round_io(double v, int io) {
+    if (io == IO_F32) return (double)(float)v; /* C conversion: round to nearest even */
+    if (io == IO_BF16) return round_to_bf16(v);
+    return v;
+}
+
+double oracle_round_io(double v, int io) { return round_io(v, io); }
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Forward.  x, res: [rows, cols] (res may be NULL: no residual).  gamma, beta: [cols].
+ * Outputs: out, res_out [rows, cols] (either may be NULL), mean, rstd [rows].
+ */
+void oracle_ln_fwd(const double* x, const double* res, const double* gamma, const double* beta,
+                   double eps, int64_t rows, int64_t cols, int io, double* out, double* res_out,
+                   double* mean, double* rstd, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * cols;
+        const double* rr = res ? res + r * cols : NULL;
+        /* The residual sum, rounded to the stored precision (it is what gets normalised). */
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double s = rr ? xr[j] + rr[j] : xr[j];
+            s = round_io(s, io);
+            if (res_out) res_out[r * cols + j] = s;
+            sum += s;
+        }
+        double mu = sum / (double)cols;
+        /* Second, dependent pass: the centred sum of squares (two-pass variance). */
+        double sq = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double s = rr ? xr[j] + rr[j] : xr[j];
+            s = round_io(s, io);
+            double d = s - mu;
+            sq += d * d;
+        }
+        double var = sq / (double)cols;
+        double rs = 1.0 / sqrt(var + eps);
+        mean[r] = mu;
+        rstd[r] = rs;
+        if (out) {
+            for (int64_t j = 0; j < cols; ++j) {
+                double s = rr ? xr[j] + rr[j] : xr[j];
+                s = round_io(s, io);
+                double xhat = (s - mu) * rs;
+                out[r * cols + j] = round_io(gamma[j] * xhat + beta[j], io);
+            }
+        }
+    }
+}
+
+/*
+ * Backward, HW4 form.  dy, xr: [rows, cols] (xr is the tensor the forward normalised);
+ * gamma: [cols]; mean, rstd: [rows].  Outputs: dx [rows, cols] (may be NULL),
+ * dgamma, dbeta [cols] (either may be NULL).
+ */
+void oracle_ln_bwd(const double* dy, const double* xr, const double* gamma, const double* mean,
+                   const double* rstd, int64_t rows, int64_t cols, int io, double* dx,
+                   double* dgamma, double* dbeta, int nthreads) {
+    set_threads(nthreads);
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            const double* d = dy + r * cols;
+            const double* x = xr + r * cols;
+            double mu = mean[r], rs = rstd[r];
+            double sum_g = 0.0, sum_gx = 0.0;
+            for (int64_t j = 0; j < cols; ++j) {
+                double xhat = (x[j] - mu) * rs;
+                double g = gamma[j] * d[j];
+                sum_g += g;
+                sum_gx += g * xhat;
+            }
+            for (int64_t j = 0; j < cols; ++j) {
+                double xhat = (x[j] - mu) * rs;
+                double g = gamma[j] * d[j];
+                double v = rs * (g - (sum_g + xhat * sum_gx) / (double)cols);
+                dx[r * cols + j] = round_io(v, io);
+            }
+        }
+    }
+    if (dgamma || dbeta) {
+        /* Each thread owns a contiguous slice of columns and walks the rows in order, so
+         * every column is summed over rows 0, 1, ..., rows-1 exactly as written above. */
+#pragma omp parallel
+        {
+            int t = 0, nt = 1;
+#ifdef _OPENMP
+            t = omp_get_thread_num();
+            nt = omp_get_num_threads();
+#endif
+            int64_t j0 = cols * t / nt, j1 = cols * (t + 1) / nt;
+            int64_t w = j1 - j0;
+            double* acc = w > 0 ? (double*)calloc((size_t)(2 * w), sizeof(double)) : NULL;
+            if (w > 0 && acc) {
+                double* acc_g = acc;
+                double* acc_b = acc + w;
+                for (int64_t r = 0; r < rows; ++r) {
+                    const double* d = dy + r * cols;
+                    const double* x = xr + r * cols;
+                    double mu = mean[r], rs = rstd[r];
+                    for (int64_t j = j0; j < j1; ++j) {
+                        double xhat = (x[j] - mu) * rs;
+                        acc_g[j - j0] += d[j] * xhat;
+                        acc_b[j - j0] += d[j];
+                    }
+                }
+                for (int64_t j = j0; j < j1; ++j) {
+                    if (dgamma) dgamma[j] = round_io(acc_g[j - j0], io);
+                    if (dbeta) dbeta[j] = round_io(acc_b[j - j0], io);
+                }
+            } else if (w > 0) {
+                /* Out of memory for the slice: fall back to one column at a time. */
+                for (int64_t j = j0; j < j1; ++j) {
+                    double ag = 0.0, ab = 0.0;
+                    for (int64_t r = 0; r < rows; ++r) {
+                        double xhat = (xr[r * cols + j] - mean[r]) * rstd[r];
+                        ag += dy[r * cols + j] * xhat;
+                        ab += dy[r * cols + j];
+                    }
+                    if (dgamma) dgamma[j] = round_io(ag, io);
+                    if (dbeta) dbeta[j] = round_io(ab, io);
+                }
+            }
+            free(acc);
+        }
+    }
+}
+
+/*
+ * Backward dx only, slides form (raw x instead of xhat in the second sum).  Unrounded
+ * float64 output; used to cross-check the HW4 form, never as the expected GPU value.
+ */
+void oracle_ln_bwd_dx_slides(const double* dy, const double* xr, const double* gamma,
+                             const double* mean, const double* rstd, int64_t rows, int64_t cols,
+                             double* dx, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* d = dy + r * cols;
+        const double* x = xr + r * cols;
+        double mu = mean[r];
+        double sigma = 1.0 / rstd[r];
+        double m = (double)cols;
+        double sum_g = 0.0, sum_gx = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double g = gamma[j] * d[j];
+            sum_g += g;
+            sum_gx += g * x[j];
+        }
+        double s3 = m * sigma * sigma * sigma;
+        for (int64_t j = 0; j < cols; ++j) {
+            double g = gamma[j] * d[j];
+            double alpha = ((x[j] - mu) * mu - sigma * sigma) / s3;
+            double beta = (mu - x[j]) / s3;
+            dx[r * cols + j] = g / sigma + alpha * sum_g + beta * sum_gx;
+        }
+    }
+}

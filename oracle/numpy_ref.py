@@ -1,0 +1,66 @@
+"""Float64 NumPy twin of the C oracle -- TEST INFRASTRUCTURE ONLY.
+
+Vectorised, for small shapes.  It restates the same definitions as ``ln_oracle.c`` in
+independent code so that the two can be compared:
+
+* forward ("Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1;
+  residual sum stored then normalised, "llm.c: the llmc/ CUDA kernel layer", section 3.2);
+* backward, HW4 form, and dgamma/dbeta as column sums (same lecture, sections 2.1, 2.4).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
+
+
+def round_bf16(v):
+    """Round float64 values to bf16 (8 significant bits, fp32 exponent range), ties to even."""
+    v = np.asarray(v, dtype=np.float64)
+    _, e = np.frexp(v)
+    qexp = np.maximum(e - 8, -133)
+    q = np.ldexp(np.ones_like(v), qexp)
+    with np.errstate(invalid="ignore", over="ignore"):
+        r = np.rint(v / q) * q
+    r = np.where(np.abs(r) > _BF16_MAX, np.copysign(np.inf, v), r)
+    r = np.where((v == 0) | ~np.isfinite(v), v, r)
+    return r
+
+
+def round_io(v, io: str):
+    v = np.asarray(v, dtype=np.float64)
+    if io == "f32":
+        return v.astype(np.float32).astype(np.float64)
+    if io == "bf16":
+        return round_bf16(v)
+    return v
+
+
+def ln_fwd(x, res, gamma, beta, eps: float, io: str = "f64"):
+    x = np.asarray(x, dtype=np.float64)
+    s = x if res is None else x + np.asarray(res, dtype=np.float64)
+    s = round_io(s, io)
+    mean = s.mean(axis=1)
+    var = ((s - mean[:, None]) ** 2).mean(axis=1)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (s - mean[:, None]) * rstd[:, None]
+    out = round_io(np.asarray(gamma, np.float64)[None, :] * xhat
+                   + np.asarray(beta, np.float64)[None, :], io)
+    return {"out": out, "res_out": s, "mean": mean, "rstd": rstd}
+
+
+def ln_bwd(dy, xr, gamma, mean, rstd, io: str = "f64"):
+    dy = np.asarray(dy, dtype=np.float64)
+    xr = np.asarray(xr, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    mean = np.asarray(mean, dtype=np.float64)
+    rstd = np.asarray(rstd, dtype=np.float64)
+    m = dy.shape[1]
+    xhat = (xr - mean[:, None]) * rstd[:, None]
+    g = gamma[None, :] * dy
+    sum_g = g.sum(axis=1, keepdims=True)
+    sum_gx = (g * xhat).sum(axis=1, keepdims=True)
+    dx = rstd[:, None] * (g - (sum_g + xhat * sum_gx) / m)
+    dgamma = (dy * xhat).sum(axis=0)
+    dbeta = dy.sum(axis=0)
+    return {"dx": round_io(dx, io), "dgamma": round_io(dgamma, io), "dbeta": round_io(dbeta, io)}
