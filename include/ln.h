@@ -1,0 +1,203 @@
+/*
+ * ln.h -- C ABI of the GB300 (sm_103a) fused residual-add + LayerNorm library (libln.so).
+ *
+ * The library computes, for a row-major [rows, cols] problem:
+ *
+ *   forward   s = x + res                      (stored as res_out, rounded to the I/O type)
+ *             mu = mean(s), var = mean((s - mu)^2), rstd = 1 / sqrt(var + eps)
+ *             out = gamma * (s - mu) * rstd + beta
+ *   backward  xhat = (s - mu) * rstd, g = gamma * dy
+ *             dx = rstd * (g - (sum_j g_j + xhat * sum_j g_j xhat_j) / cols)
+ *             dgamma = sum over rows of dy * xhat,  dbeta = sum over rows of dy
+ *
+ * Definitions: "Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1
+ * (forward; the HW4 form of the backward; dgamma and dbeta) and section 2.4 (column sums);
+ * the residual sum is written out and then normalised as in "llm.c: the llmc/ CUDA kernel
+ * layer", section 3.2 (fused_residual_forward5).  The variance is the biased one (divide by
+ * cols) and eps sits inside the square root ("AI infra learning log (2): LayerNorm operator
+ * optimisation", section 2.1).  The normalised tensor is the STORED res_out (rounded to the
+ * I/O type), so the backward, which sees only res_out, mu and rstd, differentiates exactly
+ * the function the forward evaluated.
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers owned by the caller, on the current CUDA
+ *    device; row-major and contiguous ([rows, cols] with row stride cols, [cols], [rows]).
+ *  - Element types: ``float`` is fp32; ``ln_bf16`` is the raw 16-bit pattern of a bfloat16
+ *    (the same bits as CUDA's __nv_bfloat16).  Arithmetic is always fp32; results stored in
+ *    bf16 are rounded to nearest even.  mean and rstd are always fp32.
+ *  - Calls are asynchronous on ``stream`` (NULL = the legacy default stream) and return as
+ *    soon as the work is enqueued.  Argument errors are detected on the host before anything
+ *    is launched; nothing is launched when a call returns an error.
+ *  - Pointers need no particular alignment.  When every pointer is 16-byte aligned and a row
+ *    is a multiple of 16 bytes (cols % 4 == 0 for fp32, cols % 8 == 0 for bf16) the 128-bit
+ *    vector kernels run; otherwise a scalar kernel computes the same result.
+ *  - Limits: 1 <= cols <= LN_MAX_COLS; 0 <= rows < 2^31.  rows == 0 is a no-op for the
+ *    forward; for the backward it writes dgamma = dbeta = 0.  With rows == 0 the pointers
+ *    to [rows, cols] and [rows] arrays may be NULL (empty tensors often have no storage).
+ *    eps must be finite and >= 0.
+ *  - Thread safety: entry points may be called from several host threads.  Two backward
+ *    calls that share a workspace (the same stream, or the same caller-owned workspace) must
+ *    not overlap on the GPU; stream order takes care of that for one stream.
+ */
+#ifndef LN_H_
+#define LN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LN_MAX_COLS 16384
+
+/* The raw bits of one bfloat16 value. */
+typedef uint16_t ln_bf16;
+
+/* The same type as cudaStream_t; NULL selects the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* ln_stream_t;
+
+typedef enum ln_status {
+    LN_OK = 0,
+    LN_EINVAL = 1,        /* a NULL required pointer, rows < 0, cols <= 0, eps < 0 or not finite */
+    LN_EALIGN = 2,        /* a workspace pointer that is not 256-byte aligned */
+    LN_EUNSUPPORTED = 3,  /* cols > LN_MAX_COLS, rows >= 2^31, or not an sm_103 device */
+    LN_ECUDA = 4,         /* a CUDA runtime call failed; see ln_last_cuda_error() */
+    LN_ETIMEOUT = 5,      /* a bounded device-side wait ran out (reported by ln_device_check) */
+    LN_ENOSPACE = 6       /* a caller-owned workspace smaller than ln_bwd_workspace_bytes() */
+} ln_status;
+
+/*
+ * Forward of the fused residual-add + LayerNorm.
+ *
+ *   x        [rows, cols]  input
+ *   res      [rows, cols]  residual added to x; may be NULL (plain LayerNorm of x)
+ *   gamma    [cols]        scale
+ *   beta     [cols]        shift
+ *   eps                    added to the variance inside the square root
+ *   out      [rows, cols]  gamma * xhat + beta                      (written)
+ *   res_out  [rows, cols]  the residual sum x + res, rounded to the I/O type (written);
+ *                          may be NULL.  When res is NULL it receives a copy of x.
+ *   mean     [rows] fp32   per-row mean of res_out                  (written)
+ *   rstd     [rows] fp32   per-row 1 / sqrt(var + eps)              (written)
+ *
+ * out, res_out, mean and rstd must not overlap any input.  Nothing is allocated.
+ * Errors: LN_EINVAL, LN_EUNSUPPORTED, LN_ECUDA (launch failure).
+ */
+ln_status ln_fwd_f32(const float* x, const float* res, const float* gamma, const float* beta,
+                     float eps, int64_t rows, int64_t cols, float* out, float* res_out,
+                     float* mean, float* rstd, ln_stream_t stream);
+
+ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma,
+                      const ln_bf16* beta, float eps, int64_t rows, int64_t cols, ln_bf16* out,
+                      ln_bf16* res_out, float* mean, float* rstd, ln_stream_t stream);
+
+/*
+ * Backward of the fused residual-add + LayerNorm.
+ *
+ *   dy            [rows, cols]  gradient of the loss with respect to out
+ *   x_or_res_out  [rows, cols]  the tensor the forward normalised: its res_out when it had a
+ *                               residual, else its x
+ *   gamma         [cols]
+ *   mean, rstd    [rows] fp32   as written by the forward
+ *   dx            [rows, cols]  gradient with respect to s = x + res, and therefore with
+ *                               respect to both x and res (OVERWRITTEN, not accumulated)
+ *   dgamma        [cols]        sum over rows of dy * xhat                (overwritten)
+ *   dbeta         [cols]        sum over rows of dy                       (overwritten)
+ *
+ * The two row sums are taken in one reduction (HW4 form, "Training with LightSeq2",
+ * section 2.2).  dgamma and dbeta are reduced in two deterministic stages without float
+ * atomics (section 2.4; the last-block-finishes scheme of "llm.c: the llmc/ CUDA kernel
+ * layer", section 3.3): each thread block writes compensated fp32 partial column sums over
+ * a fixed range of rows to a workspace, an integer counter elects the blocks that arrive
+ * last, and they add the partials of every block in block order.  The result is bitwise
+ * identical from run to run on the same device and build.
+ *
+ * This variant uses a workspace owned by the library, one per (device, stream), allocated
+ * with cudaMalloc on first use and grown when a larger problem arrives; ln_release() frees
+ * them.  The first call on a stream (and a call that grows its workspace) must therefore
+ * not happen during CUDA graph capture; use the _ws variant there.
+ * Errors: LN_EINVAL, LN_EUNSUPPORTED, LN_ECUDA.
+ */
+ln_status ln_bwd_f32(const float* dy, const float* x_or_res_out, const float* gamma,
+                     const float* mean, const float* rstd, float* dx, float* dgamma,
+                     float* dbeta, int64_t rows, int64_t cols, ln_stream_t stream);
+
+ln_status ln_bwd_bf16(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                      const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
+                      ln_bf16* dbeta, int64_t rows, int64_t cols, ln_stream_t stream);
+
+/*
+ * Size in bytes of the caller-owned workspace the _ws backward variants need for a
+ * [rows, cols] problem on the current device (an upper bound over element types and
+ * alignments).  Returns 0 for invalid sizes or when no device is available.
+ */
+size_t ln_bwd_workspace_bytes(int64_t rows, int64_t cols);
+
+/*
+ * Backward with a caller-owned device workspace (256-byte aligned, at least
+ * ln_bwd_workspace_bytes(rows, cols) bytes).  The caller must zero the whole workspace once
+ * before its first use; every call leaves its counters at zero again, so it can be reused
+ * by later calls in stream order without clearing.  After LN_ETIMEOUT it must be zeroed
+ * again.  Nothing is allocated.
+ * Errors: as ln_bwd_*, plus LN_EALIGN and LN_ENOSPACE.
+ */
+ln_status ln_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
+                        const float* mean, const float* rstd, float* dx, float* dgamma,
+                        float* dbeta, int64_t rows, int64_t cols, void* workspace,
+                        size_t workspace_bytes, ln_stream_t stream);
+
+ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                         const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
+                         ln_bf16* dbeta, int64_t rows, int64_t cols, void* workspace,
+                         size_t workspace_bytes, ln_stream_t stream);
+
+/*
+ * Device-side status.  Every wait inside a kernel (the bulk-copy barrier of the wide-row
+ * kernels, the backward's wait for the last blocks) is bounded; when one runs out the
+ * kernel records LN_ETIMEOUT in a per-device status word and returns early without
+ * faulting.  ln_device_check synchronizes ``stream``, reads and clears that word on the
+ * current device, re-zeroes the library-owned workspace of ``stream``, and returns LN_OK or
+ * LN_ETIMEOUT (LN_ECUDA if the synchronization itself fails).  Setting the environment
+ * variable LN_CHECK=1 makes every entry point do this before returning.
+ */
+ln_status ln_device_check(ln_stream_t stream);
+
+/* Frees every library-owned workspace on every device (synchronizes those devices). */
+ln_status ln_release(void);
+
+/* A static, human-readable name for a status code. */
+const char* ln_status_str(ln_status status);
+
+/* The cudaError_t value behind the most recent LN_ECUDA returned on this host thread. */
+int ln_last_cuda_error(void);
+
+/* The library's version as major * 10000 + minor * 100 + patch. */
+int ln_version(void);
+
+/*
+ * Tuning and test hooks.  They change no result beyond what the tests check: every path
+ * computes the same function.
+ *
+ * ln_debug_force_path selects the kernel family for later calls on all threads:
+ * 0 = automatic (default), 1 = warp per row (128-bit vectors; falls back to automatic when
+ * the row does not fit), 2 = block per row with bulk-copy (TMA) staging, 3 = scalar
+ * kernels.  Returns the previous setting.
+ *
+ * ln_debug_wait_test makes the next backward launches wait for one block more than exists,
+ * with a wait limit of ``limit_us`` microseconds, so that the bounded wait runs out and
+ * LN_ETIMEOUT is reported by ln_device_check; 0 turns it off.  Used by the test of the
+ * timeout path; it never faults the device.
+ */
+int ln_debug_force_path(int path);
+void ln_debug_wait_test(unsigned limit_us);
+
+/* Number of kernels the most recent ln_fwd_* / ln_bwd_* call on this host thread launched. */
+int ln_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LN_H_ */

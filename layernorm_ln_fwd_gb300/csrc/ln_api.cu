@@ -1,0 +1,391 @@
+// ln_api.cu -- the C ABI declared in include/ln.h: argument checks, kernel selection,
+// backward workspaces and the per-device status word.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <utility>
+
+#include "ln.h"
+#include "ln_device.cuh"
+#include "ln_internal.h"
+
+// One status word per device.  Kernels OR kStatusTimeout into it when a bounded wait runs
+// out; ln_device_check reads and clears it.
+__device__ unsigned ln_status_word_dev;
+
+namespace lnk {
+namespace {
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<int, unsigned*> g_status_ptrs;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occupancy;
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, cudaStream_t>, Workspace> g_workspaces;
+
+std::atomic<int> g_force_path{kPathAuto};
+std::atomic<unsigned> g_wait_test_us{0};
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_launches = 0;
+
+bool check_mode() {
+    static const bool on = [] {
+        const char* v = std::getenv("LN_CHECK");
+        return v && v[0] && v[0] != '0';
+    }();
+    return on;
+}
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+}  // namespace
+
+const DeviceInfo& device_info(int dev) {
+    if (dev < 0) dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_devices.find(dev);
+    if (it != g_devices.end()) return it->second;
+    DeviceInfo d;
+    d.device = dev;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev);
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    return g_devices.emplace(dev, d).first->second;
+}
+
+unsigned* status_word() {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_status_ptrs.find(dev);
+    if (it != g_status_ptrs.end()) return it->second;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, ln_status_word_dev) != cudaSuccess) return nullptr;
+    g_status_ptrs[dev] = static_cast<unsigned*>(p);
+    return static_cast<unsigned*>(p);
+}
+
+int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+    const int dev = current_device();
+    auto key = std::make_tuple(dev, kernel, threads, smem);
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
+        n = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occupancy[key] = n;
+    return n;
+}
+
+bool vector_ok(Dtype dt, int cols, const void* const* ptrs, int nptrs) {
+    const int esize = dt == Dtype::F32 ? 4 : 2;
+    if (((size_t)cols * esize) % 16 != 0) return false;
+    for (int i = 0; i < nptrs; ++i)
+        if (ptrs[i] && (reinterpret_cast<uintptr_t>(ptrs[i]) & 15u) != 0) return false;
+    return true;
+}
+
+namespace {
+
+// Validation shared by all entry points; touches no CUDA state.
+ln_status check_sizes(int64_t rows, int64_t cols) {
+    if (rows < 0 || cols <= 0) return LN_EINVAL;
+    if (cols > LN_MAX_COLS || rows >= (int64_t(1) << 31)) return LN_EUNSUPPORTED;
+    return LN_OK;
+}
+
+ln_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return LN_ECUDA;
+}
+
+ln_status check_device() {
+    const int dev = current_device();
+    if (dev < 0) return cuda_fail(cudaGetLastError());
+    const DeviceInfo& di = device_info(dev);
+    if (di.cc_major != 10 || di.cc_minor != 3) return LN_EUNSUPPORTED;
+    return LN_OK;
+}
+
+uint64_t wait_limit_ns() {
+    const unsigned us = g_wait_test_us.load();
+    return us ? (uint64_t)us * 1000ull : kWaitLimitNs;
+}
+
+ln_status finish_call(cudaError_t e, int launches, cudaStream_t stream) {
+    t_last_launches = launches;
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (check_mode()) return ln_device_check(reinterpret_cast<ln_stream_t>(stream));
+    return LN_OK;
+}
+
+template <typename T>
+ln_status fwd_impl(Dtype dt, const T* x, const T* res, const T* gamma, const T* beta, float eps,
+                   int64_t rows, int64_t cols, T* out, T* res_out, float* mean, float* rstd,
+                   ln_stream_t stream_) {
+    t_last_launches = 0;
+    if (!std::isfinite(eps) || eps < 0.f) return LN_EINVAL;
+    ln_status st = check_sizes(rows, cols);
+    if (st != LN_OK) return st;
+    if (rows == 0) return LN_OK;  // nothing is read or written
+    if (!x || !gamma || !beta || !out || !mean || !rstd) return LN_EINVAL;
+    st = check_device();
+    if (st != LN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const void* ptrs[] = {x, res, gamma, beta, out, res_out};
+    const bool aligned = vector_ok(dt, (int)cols, ptrs, 6);
+    FwdArgs a;
+    a.x = x;
+    a.res = res;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.eps = eps;
+    a.rows = (int)rows;
+    a.cols = (int)cols;
+    a.out = out;
+    a.res_out = res_out;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.status = status_word();
+    a.wait_limit_ns = wait_limit_ns();
+    int launches = 0;
+    cudaError_t e = launch_fwd(dt, a, aligned, g_force_path.load(), stream, &launches);
+    return finish_call(e, launches, stream);
+}
+
+template <typename T>
+ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const float* mean,
+                   const float* rstd, T* dx, T* dgamma, T* dbeta, int64_t rows, int64_t cols,
+                   void* ws, size_t ws_bytes, bool own_ws, ln_stream_t stream_) {
+    t_last_launches = 0;
+    ln_status st = check_sizes(rows, cols);
+    if (st != LN_OK) return st;
+    if (!dgamma || !dbeta) return LN_EINVAL;
+    if (rows > 0 && (!dy || !xr || !gamma || !mean || !rstd || !dx)) return LN_EINVAL;
+    if (!own_ws && !ws) return LN_EINVAL;
+    if (!own_ws && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LN_EALIGN;
+    st = check_device();
+    if (st != LN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const size_t esize = sizeof(T);
+    if (rows == 0) {  // sums over no rows
+        cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)cols * esize, stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, (size_t)cols * esize, stream);
+        return finish_call(e, 0, stream);
+    }
+    const void* ptrs[] = {dy, xr, gamma, dx};
+    const bool aligned = vector_ok(dt, (int)cols, ptrs, 4);
+    BwdPlan plan;
+    cudaError_t e = plan_bwd(dt, (int)rows, (int)cols, aligned, g_force_path.load(), &plan);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const size_t need = bwd_workspace_bytes(plan.grid, (int)cols);
+    if (own_ws) {
+        const int dev = current_device();
+        std::lock_guard<std::mutex> lk(g_mu);
+        Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+        if (w.bytes < need) {
+            if (w.ptr) {
+                e = cudaStreamSynchronize(stream);  // the old workspace may still be in use
+                if (e == cudaSuccess) e = cudaFree(w.ptr);
+                w.ptr = nullptr;
+                w.bytes = 0;
+                if (e != cudaSuccess) return cuda_fail(e);
+            }
+            e = cudaMalloc(&w.ptr, need);
+            if (e != cudaSuccess) {
+                w.ptr = nullptr;
+                return cuda_fail(e);
+            }
+            w.bytes = need;
+            e = cudaMemsetAsync(w.ptr, 0, kWorkspaceHeader, stream);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        ws = w.ptr;
+    } else if (ws_bytes < need) {
+        return LN_ENOSPACE;
+    }
+    BwdArgs a;
+    a.dy = dy;
+    a.xr = xr;
+    a.gamma = gamma;
+    a.mean = mean;
+    a.rstd = rstd;
+    a.dx = dx;
+    a.dgamma = dgamma;
+    a.dbeta = dbeta;
+    a.rows = (int)rows;
+    a.cols = (int)cols;
+    a.counters = static_cast<unsigned*>(ws);
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kWorkspaceHeader);
+    a.status = status_word();
+    a.wait_limit_ns = wait_limit_ns();
+    a.wait_extra = g_wait_test_us.load() ? 1u : 0u;
+    int launches = 0;
+    e = launch_bwd(dt, a, plan, stream, &launches);
+    return finish_call(e, launches, stream);
+}
+
+}  // namespace
+}  // namespace lnk
+
+using lnk::Dtype;
+
+extern "C" {
+
+ln_status ln_fwd_f32(const float* x, const float* res, const float* gamma, const float* beta,
+                     float eps, int64_t rows, int64_t cols, float* out, float* res_out,
+                     float* mean, float* rstd, ln_stream_t stream) {
+    return lnk::fwd_impl<float>(Dtype::F32, x, res, gamma, beta, eps, rows, cols, out, res_out,
+                                mean, rstd, stream);
+}
+
+ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma,
+                      const ln_bf16* beta, float eps, int64_t rows, int64_t cols, ln_bf16* out,
+                      ln_bf16* res_out, float* mean, float* rstd, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::fwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(x),
+                            reinterpret_cast<const B*>(res), reinterpret_cast<const B*>(gamma),
+                            reinterpret_cast<const B*>(beta), eps, rows, cols,
+                            reinterpret_cast<B*>(out), reinterpret_cast<B*>(res_out), mean, rstd,
+                            stream);
+}
+
+ln_status ln_bwd_f32(const float* dy, const float* x_or_res_out, const float* gamma,
+                     const float* mean, const float* rstd, float* dx, float* dgamma,
+                     float* dbeta, int64_t rows, int64_t cols, ln_stream_t stream) {
+    return lnk::bwd_impl<float>(Dtype::F32, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
+                                dbeta, rows, cols, nullptr, 0, true, stream);
+}
+
+ln_status ln_bwd_bf16(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                      const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
+                      ln_bf16* dbeta, int64_t rows, int64_t cols, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(dy),
+                            reinterpret_cast<const B*>(x_or_res_out),
+                            reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
+                            reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols,
+                            nullptr, 0, true, stream);
+}
+
+size_t ln_bwd_workspace_bytes(int64_t rows, int64_t cols) {
+    if (lnk::check_sizes(rows, cols) != LN_OK) return 0;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const lnk::DeviceInfo& di = lnk::device_info(dev);
+    if (di.sms <= 0) return 0;
+    return lnk::bwd_workspace_bytes(lnk::bwd_max_grid((int)std::max<int64_t>(rows, 1), di.sms),
+                                    (int)cols);
+}
+
+ln_status ln_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
+                        const float* mean, const float* rstd, float* dx, float* dgamma,
+                        float* dbeta, int64_t rows, int64_t cols, void* workspace,
+                        size_t workspace_bytes, ln_stream_t stream) {
+    return lnk::bwd_impl<float>(Dtype::F32, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
+                                dbeta, rows, cols, workspace, workspace_bytes, false, stream);
+}
+
+ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                         const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
+                         ln_bf16* dbeta, int64_t rows, int64_t cols, void* workspace,
+                         size_t workspace_bytes, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(dy),
+                            reinterpret_cast<const B*>(x_or_res_out),
+                            reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
+                            reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols,
+                            workspace, workspace_bytes, false, stream);
+}
+
+ln_status ln_device_check(ln_stream_t stream_) {
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return lnk::cuda_fail(e);
+    unsigned* sw = lnk::status_word();
+    if (!sw) return lnk::cuda_fail(cudaGetLastError());
+    unsigned word = 0;
+    e = cudaMemcpy(&word, sw, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return lnk::cuda_fail(e);
+    if (word == 0) return LN_OK;
+    const unsigned zero = 0;
+    e = cudaMemcpy(sw, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return lnk::cuda_fail(e);
+    // A backward that gave up may have left its counters non-zero: clear this stream's one.
+    {
+        const int dev = lnk::current_device();
+        std::lock_guard<std::mutex> lk(lnk::g_mu);
+        auto it = lnk::g_workspaces.find(std::make_pair(dev, stream));
+        if (it != lnk::g_workspaces.end() && it->second.ptr) {
+            e = cudaMemset(it->second.ptr, 0, lnk::kWorkspaceHeader);
+            if (e != cudaSuccess) return lnk::cuda_fail(e);
+        }
+    }
+    return (word & lnk::kStatusTimeout) ? LN_ETIMEOUT : LN_OK;
+}
+
+ln_status ln_release(void) {
+    std::lock_guard<std::mutex> lk(lnk::g_mu);
+    int cur = -1;
+    cudaGetDevice(&cur);
+    ln_status st = LN_OK;
+    for (auto& kv : lnk::g_workspaces) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaError_t e = cudaDeviceSynchronize();
+        if (e == cudaSuccess) e = cudaFree(kv.second.ptr);
+        if (e != cudaSuccess) st = lnk::cuda_fail(e);
+    }
+    lnk::g_workspaces.clear();
+    if (cur >= 0) cudaSetDevice(cur);
+    return st;
+}
+
+const char* ln_status_str(ln_status status) {
+    switch (status) {
+        case LN_OK: return "LN_OK";
+        case LN_EINVAL: return "LN_EINVAL: invalid argument";
+        case LN_EALIGN: return "LN_EALIGN: workspace not 256-byte aligned";
+        case LN_EUNSUPPORTED: return "LN_EUNSUPPORTED: size or device not supported";
+        case LN_ECUDA: return "LN_ECUDA: CUDA runtime error";
+        case LN_ETIMEOUT: return "LN_ETIMEOUT: a bounded device wait ran out";
+        case LN_ENOSPACE: return "LN_ENOSPACE: workspace too small";
+    }
+    return "unknown ln_status";
+}
+
+int ln_last_cuda_error(void) { return lnk::t_last_cuda_error; }
+
+int ln_version(void) { return 10000; }
+
+int ln_debug_force_path(int path) {
+    if (path < lnk::kPathAuto || path > lnk::kPathScalar) path = lnk::kPathAuto;
+    return lnk::g_force_path.exchange(path);
+}
+
+void ln_debug_wait_test(unsigned limit_us) { lnk::g_wait_test_us.store(limit_us); }
+
+int ln_last_launch_count(void) { return lnk::t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+// ln_device.cuh -- device-side building blocks shared by the forward and backward kernels.
+//
+// 128-bit vectors of the I/O type, warp reductions, mergeable row statistics, bulk-copy
+// (TMA) staging with mbarriers, bounded waits and the per-device status word.  Everything
+// here is sm_100-family code (built for sm_103a); nothing here allocates.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lnk {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Bit set in the status word when a bounded wait ran out.
+constexpr unsigned kStatusTimeout = 1u;
+
+// ---------------------------------------------------------------------------------------
+// I/O element types.  A "vector" is 16 bytes: 4 fp32 or 8 bf16 values.
+// ---------------------------------------------------------------------------------------
+template <typename T>
+struct Io;
+
+template <>
+struct Io<float> {
+    static constexpr int kVec = 4;
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+    // Round an fp32 value to the I/O type and back (identity for fp32).
+    static __device__ __forceinline__ float round(float v) { return v; }
+    static __device__ __forceinline__ void unpack(const uint4& u, float (&f)[4]) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+};
+
+template <>
+struct Io<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+    static __device__ __forceinline__ float round(float v) {
+        return __bfloat162float(__float2bfloat16_rn(v));
+    }
+    static __device__ __forceinline__ float2 pair(uint32_t w) {
+        __nv_bfloat162 h;
+        memcpy(&h, &w, 4);
+        return __bfloat1622float2(h);
+    }
+    static __device__ __forceinline__ uint32_t pair_bits(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    static __device__ __forceinline__ void unpack(const uint4& u, float (&f)[8]) {
+        float2 p0 = pair(u.x), p1 = pair(u.y), p2 = pair(u.z), p3 = pair(u.w);
+        f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
+        f[4] = p2.x; f[5] = p2.y; f[6] = p3.x; f[7] = p3.y;
+    }
+    static __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
+        return make_uint4(pair_bits(f[0], f[1]), pair_bits(f[2], f[3]), pair_bits(f[4], f[5]),
+                          pair_bits(f[6], f[7]));
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// Global memory access with cache hints.  Streamed tensors are read and written once per
+// kernel: they use the evict-first ("cs") policy so they do not push gamma/beta or the
+// backward's partial sums out of L2.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint4 ld_keep(const void* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(void* p, const uint4& v) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// ---------------------------------------------------------------------------------------
+// Reductions.  The xor butterfly leaves the same bits in every lane: at each step the two
+// lanes of a pair add the same two operands, and fp32 addition is commutative.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void warp_sum2(float& a, float& b) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(kFullMask, a, o);
+        b += __shfl_xor_sync(kFullMask, b, o);
+    }
+}
+
+// Row statistics as a mergeable summary: count n, the sum S + c of the shifted values (S and
+// its compensation c, kept error-free with TwoSum) and M2, the sum of squared deviations from
+// the group's own mean.  Two summaries merge with the pairwise update of Welford/Chan
+// ("Accelerating Transformer on GPU (I)", section 4.2):
+//   n = na + nb,  S = Sa + Sb,  M2 = M2a + M2b + delta^2 na nb / n,  delta = Sb/nb - Sa/na,
+// where delta^2 na nb / n is computed as (na Sb - nb Sa)^2 / (na nb n).  Every operation is
+// rounded separately (never fused) and is symmetric in (a, b), so both lanes of an xor-
+// butterfly pair end with the same bits.  M2 is a sum of non-negative terms: no cancellation.
+struct RowStats {
+    float n, s, c, q;
+};
+
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void stats_merge(RowStats& a, const RowStats& b) {
+    const float nn = __fadd_rn(a.n, b.n);  // exact: small integers
+    if (a.n > 0.f && b.n > 0.f) {
+        const float sa = __fadd_rn(a.s, a.c), sb = __fadd_rn(b.s, b.c);
+        const float t = __fsub_rn(__fmul_rn(a.n, sb), __fmul_rn(b.n, sa));
+        const float den = __fmul_rn(__fmul_rn(a.n, b.n), nn);
+        a.q = __fadd_rn(__fadd_rn(a.q, b.q), __fdiv_rn(__fmul_rn(t, t), den));
+    } else {
+        a.q = __fadd_rn(a.q, b.q);
+    }
+    float s, e;
+    two_sum_f(a.s, b.s, s, e);
+    a.c = __fadd_rn(__fadd_rn(a.c, b.c), e);
+    a.s = s;
+    a.n = nn;
+}
+
+__device__ __forceinline__ void warp_stats(RowStats& r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        RowStats b;
+        b.n = __shfl_xor_sync(kFullMask, r.n, o);
+        b.s = __shfl_xor_sync(kFullMask, r.s, o);
+        b.c = __shfl_xor_sync(kFullMask, r.c, o);
+        b.q = __shfl_xor_sync(kFullMask, r.q, o);
+        stats_merge(r, b);
+    }
+}
+
+// A thread's own summary of the values v[0..count) (already shifted): compensated sum, then
+// M2 about the thread's mean in a second pass over its registers.
+template <int N>
+__device__ __forceinline__ RowStats thread_stats(const float (&v)[N], int count) {
+    RowStats r{0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        if (i < count) {
+            float s, e;
+            two_sum_f(r.s, v[i], s, e);
+            r.s = s;
+            r.c = __fadd_rn(r.c, e);
+        }
+    }
+    r.n = (float)count;
+    if (count > 0) {
+        const float m = __fdiv_rn(__fadd_rn(r.s, r.c), r.n);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            if (i < count) {
+                const float e = v[i] - m;
+                r.q += e * e;
+            }
+        }
+    }
+    return r;
+}
+
+// ---------------------------------------------------------------------------------------
+// Status word and time.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void raise_status(unsigned* status, unsigned bit) {
+    if (status) atomicOr(status, bit);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *ctr >= target or `limit_ns` has passed.  Returns whether the target was seen.
+__device__ __forceinline__ bool wait_counter_geq(const unsigned* ctr, unsigned target,
+                                                 uint64_t limit_ns) {
+    if (ld_acquire_u32(ctr) >= target) return true;
+    const uint64_t t0 = global_ns();
+    unsigned sleep_ns = 32;
+    while (true) {
+        __nanosleep(sleep_ns);
+        if (ld_acquire_u32(ctr) >= target) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+        if (sleep_ns < 512) sleep_ns <<= 1;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Bulk copies (TMA, non-tensor form) global -> shared, completed on an mbarrier.
+// Source and destination must be 16-byte aligned and the size a multiple of 16.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Default limit of every device-side wait: 2 seconds.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+}  // namespace lnk

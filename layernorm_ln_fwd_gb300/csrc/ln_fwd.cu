@@ -1,0 +1,503 @@
+// ln_fwd.cu -- forward kernels of the fused residual-add + LayerNorm.
+//
+// For each row: s = x + res (fp32), stored as res_out after rounding to the I/O type; the
+// row statistics of the stored values; out = gamma * (s - mu) * rstd + beta.
+// ("Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1; residual
+// fusion as in "llm.c: the llmc/ CUDA kernel layer", section 3.2.)
+//
+// Statistics in one reduction, without the cancellation of E[s^2] - E[s]^2 that breaks rows
+// whose mean dwarfs their spread ("Accelerating Transformer on GPU (I)", section 4.2):
+//  * every row is shifted by K = its first stored element, d = s - K (exact for bf16 rows),
+//    so the centre is carried as K + mean(d) and never as one large rounded number;
+//  * each thread summarises its own values of d as (count, compensated sum, M2 about its
+//    own mean) and the summaries are combined with the Welford/Chan pairwise merge (same
+//    section) in one xor butterfly -- one reduction; M2 is a sum of non-negative terms, so
+//    nothing cancels, and the compensated sum keeps mean(d) accurate to about one rounding;
+//  * xhat = (d - mean(d)) * rstd, which never subtracts two large numbers either.
+// mean = K + mean(d) and rstd = 1 / sqrt(M2 / n + eps) are stored in fp32.
+//
+// Three kernel families compute the same function:
+//  * warp per row (rows of at most 256 vectors of 16 bytes): each lane holds its part of
+//    the row in registers, 128-bit loads and stores, one xor butterfly, no block barrier;
+//  * block per row (wider rows): a persistent block streams rows into shared memory with
+//    bulk copies (cp.async.bulk, completed on an mbarrier) several rows ahead, so each row
+//    is read from HBM once; one warp butterfly plus one cross-warp exchange per row;
+//  * scalar block per row, for rows that are not 16-byte multiples or unaligned pointers.
+#include <algorithm>
+
+#include "ln_device.cuh"
+#include "ln_internal.h"
+
+namespace lnk {
+namespace {
+
+constexpr int kFwdWarpThreads = 256;  // 8 warps, one row per warp at a time
+constexpr int kFwdBlockMaxThreads = 512;
+constexpr int kFwdScalarThreads = 256;
+constexpr int kMaxStages = 4;
+
+// ---------------------------------------------------------------------------------------
+// Warp per row.
+// ---------------------------------------------------------------------------------------
+template <typename T, int VPL, bool HAS_RES>
+__global__ void __launch_bounds__(kFwdWarpThreads)
+    fwd_warp_kernel(const T* __restrict__ x, const T* __restrict__ res,
+                    const T* __restrict__ gamma, const T* __restrict__ beta, float eps, int rows,
+                    int cols, T* __restrict__ out, T* __restrict__ res_out,
+                    float* __restrict__ mean, float* __restrict__ rstd) {
+    using IO = Io<T>;
+    constexpr int V = IO::kVec;
+    const int lane = threadIdx.x & 31;
+    const int warps_per_block = kFwdWarpThreads / 32;
+    const int nvec = cols / V;
+    const float fcols = (float)cols;
+
+    // gamma and beta stay in registers (packed) for all rows this warp normalises.
+    uint4 gv[VPL], bv[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        const int vi = v * 32 + lane;
+        gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+        bv[v] = vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+    }
+
+    const bool write_res = res_out != nullptr;
+    for (int row = blockIdx.x * warps_per_block + (threadIdx.x >> 5); row < rows;
+         row += gridDim.x * warps_per_block) {
+        const size_t base = (size_t)row * cols;
+        uint4 xv[VPL], rv[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            const int vi = v * 32 + lane;
+            if (vi < nvec) {
+                xv[v] = ld_stream(x + base + (size_t)vi * V);
+                if (HAS_RES) rv[v] = ld_stream(res + base + (size_t)vi * V);
+            }
+        }
+        // s = x + res, rounded to the stored type; it is what gets normalised.
+        float s[VPL][V];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            const int vi = v * 32 + lane;
+            if (vi < nvec) {
+                IO::unpack(xv[v], s[v]);
+                if (HAS_RES) {
+                    float r[V];
+                    IO::unpack(rv[v], r);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) s[v][k] = IO::round(s[v][k] + r[k]);
+                }
+                if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
+            } else {
+#pragma unroll
+                for (int k = 0; k < V; ++k) s[v][k] = 0.f;
+            }
+        }
+        // Shift: the row's first stored element (lane 0 always holds it).
+        const float K = __shfl_sync(kFullMask, s[0][0], 0);
+        float dv[VPL * V];
+        int cnt = 0;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+#pragma unroll
+            for (int k = 0; k < V; ++k) dv[v * V + k] = s[v][k] - K;
+            if (v * 32 + lane < nvec) cnt += V;
+        }
+        RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
+        warp_stats(st);                        // the one reduction of the row
+        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
+        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+        if (lane == 0) {
+            mean[row] = K + md;
+            rstd[row] = rs;
+        }
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            const int vi = v * 32 + lane;
+            if (vi < nvec) {
+                float g[V], b[V], o[V];
+                IO::unpack(gv[v], g);
+                IO::unpack(bv[v], b);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = g[k] * ((s[v][k] - K - md) * rs) + b[k];
+                st_stream(out + base + (size_t)vi * V, IO::pack(o));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Block per row with bulk-copy staging.
+//
+// Shared memory: `stages` slots, each holding the row of x and (if present) the row of res;
+// one mbarrier per slot.  Thread 0 keeps `stages` rows in flight: after a row is consumed
+// (end-of-row barrier) it refills that slot with the row `stages` iterations ahead.
+// Thread t of the block owns vectors t, t + blockDim.x, ... of every row.
+// ---------------------------------------------------------------------------------------
+template <typename T, int VPT, bool HAS_RES>
+__global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
+    fwd_block_kernel(const T* __restrict__ x, const T* __restrict__ res,
+                     const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
+                     int rows, int cols, T* __restrict__ out, T* __restrict__ res_out,
+                     float* __restrict__ mean, float* __restrict__ rstd, int stages,
+                     unsigned* status, uint64_t wait_limit_ns) {
+    using IO = Io<T>;
+    constexpr int V = IO::kVec;
+    constexpr int MAXW = kFwdBlockMaxThreads / 32;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ uint64_t full_bar[kMaxStages];
+    __shared__ float red[4][MAXW];
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthreads = blockDim.x, nw = nthreads >> 5;
+    const int nvec = cols / V;
+    const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
+    const unsigned nin = HAS_RES ? 2u : 1u;
+    const unsigned slot_bytes = nin * row_bytes;
+    const float fcols = (float)cols;
+
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) mbar_init(&full_bar[i], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int k) {  // thread 0 only: fetch the k-th row of this block
+        const int row = blockIdx.x + k * gridDim.x;
+        if (row >= rows) return;
+        const int slot = k % stages;
+        unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
+        mbar_arrive_expect_tx(&full_bar[slot], slot_bytes);
+        bulk_g2s(dst, x + (size_t)row * cols, row_bytes, &full_bar[slot]);
+        if (HAS_RES) bulk_g2s(dst + row_bytes, res + (size_t)row * cols, row_bytes, &full_bar[slot]);
+    };
+    if (tid == 0)
+        for (int k = 0; k < stages; ++k) issue(k);
+
+    // gamma, beta for this thread's vectors (the same columns in every row).
+    uint4 gv[VPT], bv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int vi = v * nthreads + tid;
+        if (vi < nvec) {
+            gv[v] = ld_keep(gamma + (size_t)vi * V);
+            bv[v] = ld_keep(beta + (size_t)vi * V);
+        }
+    }
+
+    const bool write_res = res_out != nullptr;
+    int k = 0;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x, ++k) {
+        const int slot = k % stages;
+        const unsigned parity = (unsigned)(k / stages) & 1u;
+        if (!mbar_wait(&full_bar[slot], parity, wait_limit_ns)) abort_flag = 1;
+        const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
+        const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
+        const size_t base = (size_t)row * cols;
+
+        float s[VPT][V];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int vi = v * nthreads + tid;
+            if (vi < nvec) {
+                IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), s[v]);
+                if (HAS_RES) {
+                    float r[V];
+                    IO::unpack(*reinterpret_cast<const uint4*>(rsm + (size_t)vi * V), r);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) s[v][q] = IO::round(s[v][q] + r[q]);
+                }
+                if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
+            } else {
+#pragma unroll
+                for (int q = 0; q < V; ++q) s[v][q] = 0.f;
+            }
+        }
+        // Shift K: the row's first stored element, read by every thread from shared memory.
+        const float K = HAS_RES ? IO::round(IO::to_f(xs[0]) + IO::to_f(rsm[0])) : IO::to_f(xs[0]);
+        float dv[VPT * V];
+        int cnt = 0;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+#pragma unroll
+            for (int q = 0; q < V; ++q) dv[v * V + q] = s[v][q] - K;
+            if (v * nthreads + tid < nvec) cnt += V;
+        }
+        RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
+        warp_stats(st);
+        if (lane == 0) {
+            red[0][warp] = st.n;
+            red[1][warp] = st.s;
+            red[2][warp] = st.c;
+            red[3][warp] = st.q;
+        }
+        __syncthreads();  // the one cross-warp exchange of the row
+        if (abort_flag) break;
+        st = RowStats{red[0][0], red[1][0], red[2][0], red[3][0]};
+        for (int w = 1; w < nw; ++w)  // same order in every thread: same bits everywhere
+            stats_merge(st, RowStats{red[0][w], red[1][w], red[2][w], red[3][w]});
+        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
+        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+        if (tid == 0) {
+            mean[row] = K + md;
+            rstd[row] = rs;
+        }
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int vi = v * nthreads + tid;
+            if (vi < nvec) {
+                float g[V], b[V], o[V];
+                IO::unpack(gv[v], g);
+                IO::unpack(bv[v], b);
+#pragma unroll
+                for (int q = 0; q < V; ++q) o[q] = g[q] * ((s[v][q] - K - md) * rs) + b[q];
+                st_stream(out + base + (size_t)vi * V, IO::pack(o));
+            }
+        }
+        __syncthreads();  // the slot and `red` are free again
+        if (tid == 0) issue(k + stages);
+    }
+
+    if (abort_flag) {
+        // A copy did not complete in time: record it, then give every issued copy a bounded
+        // chance to land before the block's shared memory is released.
+        if (tid == 0) {
+            raise_status(status, kStatusTimeout);
+            for (int j = k; j < k + stages; ++j) {
+                const int row = blockIdx.x + j * gridDim.x;
+                if (row >= rows) break;
+                (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, wait_limit_ns);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Scalar block per row: any alignment, any width.  Two passes over global memory (the
+// second one hits L1/L2); the statistics are the same mergeable summaries.
+// ---------------------------------------------------------------------------------------
+template <typename T, bool HAS_RES>
+__global__ void __launch_bounds__(kFwdScalarThreads)
+    fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ res,
+                      const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
+                      int rows, int cols, T* __restrict__ out, T* __restrict__ res_out,
+                      float* __restrict__ mean, float* __restrict__ rstd) {
+    using IO = Io<T>;
+    constexpr int NW = kFwdScalarThreads / 32;
+    __shared__ float red[4][NW];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float fcols = (float)cols;
+    const bool write_res = res_out != nullptr;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        const size_t base = (size_t)row * cols;
+        auto load_s = [&](int j) -> float {
+            float v = IO::to_f(x[base + j]);
+            if (HAS_RES) v = IO::round(v + IO::to_f(res[base + j]));
+            return v;
+        };
+        const float K = load_s(0);
+        // This thread's summary of d = s - K: compensated sum plus Welford's running M2.
+        RowStats st{0.f, 0.f, 0.f, 0.f};
+        float wm = 0.f;  // Welford's running mean
+        for (int j = tid; j < cols; j += kFwdScalarThreads) {
+            const float sv = load_s(j);
+            if (write_res) res_out[base + j] = IO::from_f(sv);
+            const float d = sv - K;
+            st.n += 1.f;
+            float sum, e;
+            two_sum_f(st.s, d, sum, e);
+            st.s = sum;
+            st.c = __fadd_rn(st.c, e);
+            const float delta = d - wm;
+            wm += delta / st.n;
+            st.q += delta * (d - wm);
+        }
+        warp_stats(st);
+        if (lane == 0) {
+            red[0][warp] = st.n;
+            red[1][warp] = st.s;
+            red[2][warp] = st.c;
+            red[3][warp] = st.q;
+        }
+        __syncthreads();
+        st = RowStats{red[0][0], red[1][0], red[2][0], red[3][0]};
+#pragma unroll
+        for (int w = 1; w < NW; ++w)
+            stats_merge(st, RowStats{red[0][w], red[1][w], red[2][w], red[3][w]});
+        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
+        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+        if (tid == 0) {
+            mean[row] = K + md;
+            rstd[row] = rs;
+        }
+        for (int j = tid; j < cols; j += kFwdScalarThreads) {
+            const float sv = load_s(j);
+            out[base + j] =
+                IO::from_f(IO::to_f(gamma[j]) * ((sv - K - md) * rs) + IO::to_f(beta[j]));
+        }
+        __syncthreads();  // `red` is reused by the next row
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host-side dispatch.
+// ---------------------------------------------------------------------------------------
+template <typename T>
+cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
+    const void* kern = nullptr;
+    const bool has_res = a.res != nullptr;
+#define LNK_FWD_WARP_CASE(N)                                                               \
+    case N:                                                                                \
+        kern = has_res ? (const void*)fwd_warp_kernel<T, N, true>                          \
+                       : (const void*)fwd_warp_kernel<T, N, false>;                        \
+        break;
+    switch (vpl) {
+        LNK_FWD_WARP_CASE(1)
+        LNK_FWD_WARP_CASE(2)
+        LNK_FWD_WARP_CASE(3)
+        LNK_FWD_WARP_CASE(4)
+        LNK_FWD_WARP_CASE(5)
+        LNK_FWD_WARP_CASE(6)
+        LNK_FWD_WARP_CASE(7)
+        LNK_FWD_WARP_CASE(8)
+        default:
+            return cudaErrorInvalidValue;
+    }
+#undef LNK_FWD_WARP_CASE
+    const DeviceInfo& di = device_info(-1);
+    const int warps = kFwdWarpThreads / 32;
+    const int need = (a.rows + warps - 1) / warps;
+    const int occ = std::max(1, blocks_per_sm(kern, kFwdWarpThreads, 0));
+    const int grid = std::max(1, std::min(need, di.sms * occ));
+    const T* x = static_cast<const T*>(a.x);
+    const T* res = static_cast<const T*>(a.res);
+    const T* gamma = static_cast<const T*>(a.gamma);
+    const T* beta = static_cast<const T*>(a.beta);
+    T* out = static_cast<T*>(a.out);
+    T* res_out = static_cast<T*>(a.res_out);
+    float eps = a.eps;
+    int rows = a.rows, cols = a.cols;
+    float* mean = a.mean;
+    float* rstd = a.rstd;
+    void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd};
+    return cudaLaunchKernel(kern, dim3(grid), dim3(kFwdWarpThreads), args, 0, stream);
+}
+
+template <typename T>
+cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
+    constexpr int V = Io<T>::kVec;
+    const int nvec = a.cols / V;
+    const int vpt = (nvec + kFwdBlockMaxThreads - 1) / kFwdBlockMaxThreads;
+    const int threads = std::max(32, ((nvec + vpt - 1) / vpt + 31) / 32 * 32);
+    const bool has_res = a.res != nullptr;
+    const void* kern = nullptr;
+#define LNK_FWD_BLOCK_CASE(N)                                                              \
+    case N:                                                                                \
+        kern = has_res ? (const void*)fwd_block_kernel<T, N, true>                         \
+                       : (const void*)fwd_block_kernel<T, N, false>;                       \
+        break;
+    // cols <= 16384: at most 4 vectors per thread for bf16, 8 for fp32.
+    if constexpr (V == 8) {
+        switch (vpt) {
+            LNK_FWD_BLOCK_CASE(1)
+            LNK_FWD_BLOCK_CASE(2)
+            LNK_FWD_BLOCK_CASE(3)
+            LNK_FWD_BLOCK_CASE(4)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (vpt) {
+            LNK_FWD_BLOCK_CASE(1)
+            LNK_FWD_BLOCK_CASE(2)
+            LNK_FWD_BLOCK_CASE(3)
+            LNK_FWD_BLOCK_CASE(4)
+            LNK_FWD_BLOCK_CASE(5)
+            LNK_FWD_BLOCK_CASE(6)
+            LNK_FWD_BLOCK_CASE(7)
+            LNK_FWD_BLOCK_CASE(8)
+            default:
+                return cudaErrorInvalidValue;
+        }
+    }
+#undef LNK_FWD_BLOCK_CASE
+    const DeviceInfo& di = device_info(-1);
+    const size_t slot_bytes = (size_t)(has_res ? 2 : 1) * a.cols * sizeof(T);
+    // Up to kMaxStages rows in flight per block, within about half of an SM's shared memory
+    // so that two blocks can share an SM when the rows are small enough.
+    const size_t budget = std::max<size_t>(slot_bytes, (size_t)di.smem_optin / 2);
+    int stages = (int)std::min<size_t>(kMaxStages, budget / slot_bytes);
+    stages = std::max(1, stages);
+    const size_t smem = (size_t)stages * slot_bytes;
+    if (smem > (size_t)di.smem_optin) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const int occ = std::max(1, blocks_per_sm(kern, threads, smem));
+    const int grid = std::max(1, std::min(a.rows, di.sms * occ));
+    const T* x = static_cast<const T*>(a.x);
+    const T* res = static_cast<const T*>(a.res);
+    const T* gamma = static_cast<const T*>(a.gamma);
+    const T* beta = static_cast<const T*>(a.beta);
+    T* out = static_cast<T*>(a.out);
+    T* res_out = static_cast<T*>(a.res_out);
+    float eps = a.eps;
+    int rows = a.rows, cols = a.cols;
+    float* mean = a.mean;
+    float* rstd = a.rstd;
+    unsigned* status = a.status;
+    uint64_t limit = a.wait_limit_ns;
+    void* args[] = {&x,   &res,     &gamma, &beta, &eps,   &rows,   &cols,
+                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
+    return cudaLaunchKernel(kern, dim3(grid), dim3(threads), args, smem, stream);
+}
+
+template <typename T>
+cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
+    const bool has_res = a.res != nullptr;
+    const void* kern = has_res ? (const void*)fwd_scalar_kernel<T, true>
+                               : (const void*)fwd_scalar_kernel<T, false>;
+    const DeviceInfo& di = device_info(-1);
+    const int occ = std::max(1, blocks_per_sm(kern, kFwdScalarThreads, 0));
+    const int grid = std::max(1, std::min(a.rows, di.sms * occ));
+    const T* x = static_cast<const T*>(a.x);
+    const T* res = static_cast<const T*>(a.res);
+    const T* gamma = static_cast<const T*>(a.gamma);
+    const T* beta = static_cast<const T*>(a.beta);
+    T* out = static_cast<T*>(a.out);
+    T* res_out = static_cast<T*>(a.res_out);
+    float eps = a.eps;
+    int rows = a.rows, cols = a.cols;
+    float* mean = a.mean;
+    float* rstd = a.rstd;
+    void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd};
+    return cudaLaunchKernel(kern, dim3(grid), dim3(kFwdScalarThreads), args, 0, stream);
+}
+
+template <typename T>
+cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t stream) {
+    constexpr int V = Io<T>::kVec;
+    if (!aligned || path == kPathScalar) return launch_scalar<T>(a, stream);
+    const int nvec = a.cols / V;
+    const int vpl = (nvec + 31) / 32;
+    if (path == kPathBlock) return launch_block<T>(a, stream);
+    if (vpl <= 8) return launch_warp<T>(a, vpl, stream);
+    return launch_block<T>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
+                       cudaStream_t stream, int* launches) {
+    *launches = 0;
+    if (a.rows == 0) return cudaSuccess;
+    cudaError_t e = dt == Dtype::F32 ? launch_fwd_t<float>(a, aligned, path_override, stream)
+                                     : launch_fwd_t<__nv_bfloat16>(a, aligned, path_override, stream);
+    if (e == cudaSuccess) *launches = 1;
+    return e;
+}
+
+}  // namespace lnk

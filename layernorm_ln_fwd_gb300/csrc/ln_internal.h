@@ -1,0 +1,100 @@
+// ln_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lnk {
+
+enum class Dtype { F32, BF16 };
+
+enum Path { kPathAuto = 0, kPathWarp = 1, kPathBlock = 2, kPathScalar = 3 };
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int smem_optin = 0;     // max dynamic shared memory per block (opt-in), bytes
+    int smem_per_sm = 0;    // shared memory per SM, bytes
+    int l2_bytes = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Cached properties of device `dev` (-1: the current device).
+const DeviceInfo& device_info(int dev);
+
+// Per-device status word (a __device__ variable); its device address on the current device.
+unsigned* status_word();
+
+struct FwdArgs {
+    const void* x;
+    const void* res;    // may be null
+    const void* gamma;
+    const void* beta;
+    float eps;
+    int rows;
+    int cols;
+    void* out;
+    void* res_out;      // may be null
+    float* mean;
+    float* rstd;
+    unsigned* status;
+    uint64_t wait_limit_ns;
+};
+
+struct BwdArgs {
+    const void* dy;
+    const void* xr;
+    const void* gamma;
+    const float* mean;
+    const float* rstd;
+    void* dx;
+    void* dgamma;
+    void* dbeta;
+    int rows;
+    int cols;
+    float* partials;      // [2][grid][cols] (hi, lo) fp32 pairs: dgamma, then dbeta
+    unsigned* counters;   // [2]: arrivals, finished finishers
+    unsigned* status;
+    uint64_t wait_limit_ns;
+    unsigned wait_extra;  // test hook: wait for this many more arrivals than exist
+};
+
+// A launch plan for the backward: which kernel, how many blocks (= rows of partials).
+struct BwdPlan {
+    int path = kPathAuto;
+    int per_thread = 0;   // vectors per lane (warp path) or per thread (block path)
+    int threads = 0;
+    int grid = 0;
+    int finishers = 0;
+    int stages = 0;       // rows in flight per block (block path); accumulator place (scalar)
+    size_t smem = 0;
+};
+
+// Whether the 128-bit vector kernels may be used: every pointer 16-byte aligned and a row a
+// multiple of 16 bytes.
+bool vector_ok(Dtype dt, int cols, const void* const* ptrs, int nptrs);
+
+cudaError_t launch_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
+                       cudaStream_t stream, int* launches);
+
+cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_override,
+                     BwdPlan* plan);
+
+// Largest grid any backward plan can use for `rows` rows on a device with `sms` SMs.
+int bwd_max_grid(int rows, int sms);
+
+constexpr size_t kWorkspaceHeader = 256;  // counters live in the first 256 bytes
+
+// Partial sums: [2 statistics][grid][cols] (hi, lo) fp32 pairs.
+inline size_t bwd_workspace_bytes(int grid, int cols) {
+    return kWorkspaceHeader + 2ull * (size_t)grid * (size_t)cols * 2 * sizeof(float);
+}
+
+cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStream_t stream,
+                       int* launches);
+
+// Occupancy (resident blocks per SM) of a kernel, cached per (device, kernel, threads, smem).
+int blocks_per_sm(const void* kernel, int threads, size_t smem);
+
+}  // namespace lnk

@@ -1,0 +1,236 @@
+"""Parity of the CUDA path (called through the C ABI) with the float64 oracle.
+
+Small shapes run the oracle on every element; the five full-size workloads compare sampled
+rows element by element and dgamma/dbeta over all rows, in the launch configuration the
+benchmark uses.  Tolerances are stated in ``lnparity``.
+"""
+import numpy as np
+import pytest
+import torch
+
+import layernorm_ln_fwd_gb300 as ln
+import lnparity as P
+import oracle
+from layernorm_ln_fwd_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+EPS = synth.EPS
+
+COLS = [1, 2, 3, 8, 31, 32, 33, 127, 128, 129, 767, 768, 1000, 1001, 1023, 1024, 1025, 1280,
+        2048, 2056, 4096, 8191, 8192, 16384]
+ROWS = [1, 7, 300]
+
+
+@pytest.fixture(autouse=True)
+def _auto_path():
+    ln.force_path(ln.PATH_AUTO)
+    yield
+    ln.force_path(ln.PATH_AUTO)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", COLS)
+@pytest.mark.parametrize("rows", ROWS)
+def test_shapes_against_oracle(dtype, rows, cols):
+    inp = synth.make_inputs(rows, cols, dtype, seed=rows * 100003 + cols)
+    gpu = P.run_gpu(inp, EPS)
+    ref = P.run_oracle(inp, EPS)
+    P.compare_all(gpu, ref, dtype, conditioned=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", COLS)
+def test_backward_on_identical_stored_inputs(dtype, cols):
+    """The backward alone, fed the same stored inputs on both sides (the oracle forward's
+    res_out, and its mean and rstd rounded to fp32): no conditioning term is needed."""
+    rows = 300
+    inp = synth.make_inputs(rows, cols, dtype, seed=cols + 17)
+    st = P.stored_stats_inputs(inp, EPS)
+    td = synth.torch_dtype(dtype)
+    dev = lambda a, t=td: torch.tensor(a).to(t).cuda()  # noqa: E731  (exact casts)
+    dx, dg, db = ln.bwd(inp["dy"].cuda(), dev(st["res_out"]), inp["gamma"].cuda(),
+                        dev(st["mean"], torch.float32), dev(st["rstd"], torch.float32))
+    torch.cuda.synchronize()
+    dy64 = P.to64(inp["dy"])
+    b = oracle.ln_bwd(dy64, st["res_out"], P.to64(inp["gamma"]), st["mean"], st["rstd"],
+                      io=dtype)
+    allow = P.colsum_allowance(dy64, (st["res_out"] - st["mean"][:, None]) * st["rstd"][:, None])
+    P.compare("dx", P.to64(dx), b["dx"], dtype)
+    P.compare("dgamma", P.to64(dg), b["dgamma"], dtype, extra=allow["dgamma"])
+    P.compare("dbeta", P.to64(db), b["dbeta"], dtype, extra=allow["dbeta"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", [ln.PATH_WARP, ln.PATH_BLOCK, ln.PATH_SCALAR])
+@pytest.mark.parametrize("rows,cols", [(5, 64), (37, 768), (64, 1024), (19, 1000), (9, 4104)])
+def test_every_kernel_family(dtype, path, rows, cols):
+    if dtype == "bf16" and cols == 1000:
+        cols = 1000 - 8  # keep bf16 rows 16-byte multiples so the vector paths apply
+    ln.force_path(path)
+    inp = synth.make_inputs(rows, cols, dtype, seed=7 + path)
+    P.compare_all(P.run_gpu(inp, EPS), P.run_oracle(inp, EPS), dtype, conditioned=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [768, 1000, 8192])
+def test_plain_layernorm_without_residual(dtype, cols):
+    inp = synth.make_inputs(33, cols, dtype, seed=3)
+    gpu = P.run_gpu(inp, EPS, has_res=False)
+    ref = P.run_oracle(inp, EPS, has_res=False)
+    P.compare_all(gpu, ref, dtype)
+    # res_out receives a copy of x.
+    assert torch.equal(gpu["res_out"].cpu(), inp["x"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_forward_without_res_out(dtype):
+    inp = synth.make_inputs(40, 1280, dtype, seed=4)
+    gpu = P.run_gpu(inp, EPS, write_res=False)
+    assert "res_out" not in gpu
+    ref = P.run_oracle(inp, EPS)
+    for k in ("out", "mean", "rstd"):
+        P.compare(k, P.to64(gpu[k]), ref[k], dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("cols", [768, 8192])
+def test_unaligned_pointers_take_the_scalar_kernel(dtype, cols):
+    rows = 23
+    inp = synth.make_inputs(rows, cols, dtype, seed=5)
+    td = synth.torch_dtype(dtype)
+
+    def shifted(t):  # same values, data pointer off by one element (not 16-byte aligned)
+        buf = torch.empty(t.numel() + 1, dtype=td, device="cuda")
+        v = buf[1:].view(t.shape)
+        v.copy_(t.cuda())
+        return v
+
+    d = {k: shifted(v) for k, v in inp.items()}
+    assert d["x"].data_ptr() % 16 != 0
+    out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS,
+                                      out=shifted(inp["x"]), res_out=shifted(inp["x"]))
+    dx, dg, db = ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd, dx=shifted(inp["x"]))
+    torch.cuda.synchronize()
+    gpu = {"out": out, "res_out": res_out, "mean": mean, "rstd": rstd, "dx": dx,
+           "dgamma": dg, "dbeta": db}
+    P.compare_all(gpu, P.run_oracle(inp, EPS), dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_caller_owned_workspace(dtype):
+    rows, cols = 300, 1280
+    inp = synth.make_inputs(rows, cols, dtype, seed=6)
+    ws = torch.zeros(ln.workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    assert ws.data_ptr() % 256 == 0
+    ref = P.run_oracle(inp, EPS)
+    for _ in range(2):  # the counters are left at zero, so the workspace can be reused
+        P.compare_all(P.run_gpu(inp, EPS, workspace=ws), ref, dtype)
+    small = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ln.LnError) as e:
+        P.run_gpu(inp, EPS, workspace=small)
+    assert e.value.status == 6
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_rows(dtype):
+    td = synth.torch_dtype(dtype)
+    x = torch.empty(0, 64, dtype=td, device="cuda")
+    g = torch.ones(64, dtype=td, device="cuda")
+    out, res_out, mean, rstd = ln.fwd(x, x, g, g, EPS)
+    assert out.shape == (0, 64)
+    dgamma = torch.full((64,), 7.0, dtype=td, device="cuda")
+    dbeta = torch.full((64,), 7.0, dtype=td, device="cuda")
+    ln.bwd(x, x, g, mean, rstd, dgamma=dgamma, dbeta=dbeta)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dgamma) == 0 and torch.count_nonzero(dbeta) == 0
+
+
+def test_too_wide_rows_are_rejected():
+    x = torch.zeros(2, ln.MAX_COLS + 8, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(ln.MAX_COLS + 8, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ln.LnError) as e:
+        ln.fwd(x, None, g, g)
+    assert e.value.status == 3
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(8192, 768), (4096, 8192), (2000, 1001)])
+def test_integer_dy_gives_exact_dbeta(dtype, rows, cols):
+    """With dy integer-valued the column sums of dy are exact in fp32, so dbeta must match
+    the oracle bit for bit whatever the order of the additions."""
+    inp = synth.make_inputs(rows, cols, dtype, seed=8, dy=("int", -2, 2))
+    gpu = P.run_gpu(inp, EPS)
+    ref = P.oracle_dparams(inp, EPS)
+    np.testing.assert_array_equal(P.to64(gpu["dbeta"]), ref["dbeta"])
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_workload_full_size(name):
+    """The five workloads at full size, in the benchmark's launch configuration: sampled
+    rows element by element, dgamma/dbeta over all rows, and bitwise-repeatable results."""
+    w = synth.WORKLOADS[name]
+    inp = synth.workload_inputs(name, seed=0)
+    gpu = P.run_gpu(inp, w.eps)
+    rng = np.random.default_rng(1)
+    sample = rng.choice(w.rows, min(254, w.rows), replace=False)
+    rows_idx = np.unique(np.concatenate([[0, w.rows - 1], sample]))
+    ref = P.run_oracle(inp, w.eps, rows_idx=rows_idx)
+    P.compare_all(gpu, ref, w.dtype, rows_idx=rows_idx)
+    ref_p = P.oracle_dparams(inp, w.eps)
+    for k in ("dgamma", "dbeta"):
+        P.compare(k, P.to64(gpu[k]), ref_p[k], w.dtype, extra=ref_p["_colsum"][k])
+    # Run to run: the backward gives the same bits (dgamma, dbeta and dx).
+    d = P.to_device(inp)
+    for _ in range(2):
+        dx2, dg2, db2 = ln.bwd(d["dy"], gpu["res_out"], d["gamma"], gpu["mean"], gpu["rstd"])
+        torch.cuda.synchronize()
+        assert torch.equal(dg2, gpu["dgamma"]) and torch.equal(db2, gpu["dbeta"])
+        assert torch.equal(dx2, gpu["dx"])
+
+
+def test_normalised_rows_property_at_full_size():
+    """gamma = 1, beta = 0: every output row has mean ~0 and variance var/(var+eps); checked
+    on all 4096 rows of the wide mean-100 workload (a property that holds at any size)."""
+    w = synth.WORKLOADS["bf16_4096x8192_mean100"]
+    inp = synth.workload_inputs(w.name, seed=0)
+    d = P.to_device(inp)
+    one = torch.ones(w.cols, dtype=torch.bfloat16, device="cuda")
+    zero = torch.zeros(w.cols, dtype=torch.bfloat16, device="cuda")
+    out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], one, zero, w.eps)
+    o = out.double()
+    s = res_out.double()
+    var = s.var(dim=1, unbiased=False)
+    assert float(o.mean(dim=1).abs().max()) < 2e-3  # bf16 rounding of ~1-sized outputs
+    rel = (o.var(dim=1, unbiased=False) / (var / (var + w.eps)) - 1).abs().max()
+    assert float(rel) < 5e-3
+    np.testing.assert_allclose(mean.double().cpu().numpy(), s.mean(dim=1).cpu().numpy(),
+                               rtol=2e-7, atol=0)
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """The backward's finishers wait for one block more than exists, with a 2 ms limit: the
+    wait runs out, the kernel returns, and ln_device_check reports LN_ETIMEOUT.  Afterwards
+    the same stream computes correct results again."""
+    inp = synth.make_inputs(512, 768, "bf16", seed=9)
+    L = ln.lib()
+    L.ln_debug_wait_test(2000)
+    try:
+        d = P.to_device(inp)
+        out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS)
+        ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
+        assert ln.device_check() == 5
+    finally:
+        L.ln_debug_wait_test(0)
+    assert ln.device_check() == 0
+    P.compare_all(P.run_gpu(inp, EPS), P.run_oracle(inp, EPS), "bf16")
+
+
+def test_launch_count_and_native_library_loaded():
+    inp = synth.make_inputs(64, 768, "f32", seed=10)
+    d = P.to_device(inp)
+    out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS)
+    assert ln.last_launch_count() == 1
+    ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
+    assert ln.last_launch_count() == 1
+    maps = open("/proc/self/maps").read()
+    assert ln.LIB_PATH in maps
