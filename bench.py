@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused residual-add + LayerNorm forward + backward on GB300.
+
+One step = one pass of the whole hot path over one batch: the forward (residual add, row
+statistics, normalisation) and the backward (dx, dgamma, dbeta) of the GPT-2-small-shaped
+bf16 workload, 8 x 1024 = 8192 rows of 768 columns, on synthetic seeded inputs.
+
+Metric: achieved HBM GB/s of the algorithmic bytes (and rows/s), next to the 8 TB/s HBM
+roofline and the measured copy bandwidth.  Algorithmic bytes per step:
+  forward  = 4 R C s + 2 C s + 8 R   (read x, res; write out, res_out; gamma, beta; mean, rstd)
+  backward = 3 R C s + 3 C s + 8 R   (read dy, res_out; write dx; gamma, dgamma, dbeta; stats)
+with s = 2 bytes for bf16.
+
+Timing: inputs are resident in HBM; W warm-up steps, then exactly K steps replayed from a
+CUDA graph (captured in chunks of steps), bracketed by a barrier and a synchronize.  Between
+steps nothing is L2-hot: the step cycles through S buffer sets whose total footprint is more
+than three times the L2 cache, and the backward of a step consumes the forward outputs of
+the set half a cycle back.  The graph launches our kernels only (2 per step).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own replica (replicas only: no data-path collective);
+rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LayerNorm fwd+bwd achieved HBM GB/s and rows/s vs 8 TB/s roofline, 1×GB300"
+ROOFLINE_NOMINAL_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def fwd_bytes(R, C, s):
+    return 4 * R * C * s + 2 * C * s + 8 * R
+
+
+def bwd_bytes(R, C, s):
+    return 3 * R * C * s + 3 * C * s + 8 * R
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "layernorm_ln_fwd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+        self.mark = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 10:  # wait for the first sample
+            time.sleep(0.05)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def begin(self):
+        self.mark = (time.time(), None)
+
+    def end(self):
+        self.mark = (self.mark[0], time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        t0, t1 = self.mark if self.mark and self.mark[1] else (0, time.time())
+        inside = [l for (t, l) in self.lines if t0 - 0.15 <= t <= t1 + 0.15] or \
+            [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in inside:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except Exception:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# The reference arm: the float64 oracle on the host cores (the pages ship no runnable code).
+# ------------------------------------------------------------------------------------------
+def time_oracle(workload: str, steps: int, warmup: int, budget_s: float, target_s: float = 0.0):
+    """Time the oracle's fwd+bwd on the workload.  Each step covers all rows unless that
+    would overrun `budget_s`; with `target_s` > 0 the number of steps is instead chosen to
+    take about that long (the CPU-baseline sample)."""
+    import numpy as np
+
+    import oracle
+    from layernorm_ln_fwd_gb300 import synth
+    w = synth.WORKLOADS[workload]
+    s = 4 if w.dtype == "f32" else 2
+    inp = synth.workload_inputs(workload, seed=0)
+    f64 = {k: v.float().numpy().astype(np.float64) for k, v in inp.items()}
+    cores = len(os.sched_getaffinity(0))
+    oracle.build()
+
+    def step(rows):
+        f = oracle.ln_fwd(f64["x"][:rows], f64["res"][:rows], f64["gamma"], f64["beta"], w.eps,
+                          io=w.dtype, threads=cores)
+        oracle.ln_bwd(f64["dy"][:rows], f["res_out"], f64["gamma"], f["mean"], f["rstd"],
+                      io=w.dtype, threads=cores)
+
+    t = time.perf_counter()
+    step(w.rows)
+    t_full = time.perf_counter() - t
+    # Size each step so that warm-up plus timed steps stay within the budget.
+    rows = w.rows
+    if target_s > 0:
+        steps = max(1, min(100, int(target_s / max(t_full, 1e-3))))
+    elif t_full * (steps + warmup) > budget_s:
+        rows = max(64, int(w.rows * budget_s / ((steps + warmup) * t_full)))
+    for _ in range(warmup):
+        step(rows)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step(rows)
+    dt = time.perf_counter() - t0
+    nbytes = fwd_bytes(rows, w.cols, s) + bwd_bytes(rows, w.cols, s)
+    gbs = nbytes * steps / dt / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "rows_per_s": rows * steps / dt, "ms_per_step": dt / steps * 1e3,
+            "sample": f"{steps} step(s) of {rows} of the {w.rows} rows x {w.cols} columns "
+                      f"({w.dtype}), float64 C oracle fwd+bwd, OpenMP on {cores} threads"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from layernorm_ln_fwd_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    r = time_oracle(args.workload, args.steps, args.warmup, budget_s=120.0)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": w.rows, "cols": w.cols,
+                   "io_dtype": w.dtype, "note": "the float64 CPU oracle: the pages ship no "
+                   "runnable reference code"},
+        "rows_per_s": r["rows_per_s"],
+        "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"],
+                         "kind": "oracle", "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "world_size": world,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------------------------------
+# Our arm.
+# ------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import layernorm_ln_fwd_gb300 as ln
+    from layernorm_ln_fwd_gb300 import build as lnbuild
+    from layernorm_ln_fwd_gb300 import synth
+
+    lnbuild.build()
+    world, rank, local = dist_setup()
+    w = synth.WORKLOADS[args.workload]
+    R, C, td = w.rows, w.cols, synth.torch_dtype(w.dtype)
+    s = 4 if w.dtype == "f32" else 2
+    props = torch.cuda.get_device_properties(local)
+    l2 = props.L2_cache_size
+    step_bytes = fwd_bytes(R, C, s) + bwd_bytes(R, C, s)
+    set_bytes = 6 * R * C * s + 8 * R + 5 * C * s
+    nsets = max(4, -(-3 * l2 // set_bytes) + 1)
+    nsets += nsets % 2
+
+    # Seeded inputs (set i uses seed i, rank-offset so replicas differ), resident in HBM.
+    sets = []
+    for i in range(nsets):
+        inp = synth.workload_inputs(args.workload, seed=1000 * rank + i)
+        d = {k: v.cuda() for k, v in inp.items()}
+        d.update(out=torch.empty_like(d["x"]), res_out=torch.empty_like(d["x"]),
+                 dx=torch.empty_like(d["x"]),
+                 mean=torch.empty(R, dtype=torch.float32, device="cuda"),
+                 rstd=torch.empty(R, dtype=torch.float32, device="cuda"),
+                 dgamma=torch.empty(C, dtype=td, device="cuda"),
+                 dbeta=torch.empty(C, dtype=td, device="cuda"))
+        sets.append(d)
+    ws = torch.zeros(ln.workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def fwd(i):
+        S = sets[i % nsets]
+        ln.fwd(S["x"], S["res"], S["gamma"], S["beta"], w.eps, out=S["out"],
+               res_out=S["res_out"], mean=S["mean"], rstd=S["rstd"], stream=stream)
+
+    def bwd(i):
+        S = sets[i % nsets]
+        ln.bwd(S["dy"], S["res_out"], S["gamma"], S["mean"], S["rstd"], dx=S["dx"],
+               dgamma=S["dgamma"], dbeta=S["dbeta"], workspace=ws, stream=stream)
+
+    def step(k):  # one pass of the hot path; the backward reads set k + S/2's forward
+        fwd(k)
+        bwd(k + nsets // 2)
+
+    with torch.cuda.stream(stream):
+        for i in range(nsets):
+            fwd(i)
+        for k in range(max(args.warmup, 3)):
+            step(k)
+    torch.cuda.synchronize()
+
+    def capture(fn, n, start):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n):
+                fn(start + k)
+        return g
+
+    chunk = min(args.steps, 500)
+    while args.steps % chunk:
+        chunk -= 1
+    g_step = capture(step, chunk, 0)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(2):
+            g_step.replay()
+    torch.cuda.synchronize()
+
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-")
+                           else (str(uuid) if uuid is not None else local))
+    if rank == 0:
+        sampler.start()
+    # ---- timed region: exactly K steps ----
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.begin()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps // chunk):
+            g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.end()
+    ms_total = max_over_ranks(world, e0.elapsed_time(e1))
+    ms_step = ms_total / args.steps
+
+    # ---- per-kernel launch durations (same stream, same rotation, separate loops) ----
+    nk = min(args.steps, 500)
+    kern = {}
+    for name, fn, nb in (("fwd", fwd, fwd_bytes(R, C, s)), ("bwd", lambda k: bwd(k + nsets // 2), bwd_bytes(R, C, s))):
+        g = capture(fn, nk, 0)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        reps = max(1, 2000 // nk)
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * nk)
+        kern[name] = {"us_per_launch": us, "algorithmic_bytes": nb, "gbs": nb / us / 1e3}
+    sampler.stop()
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region ----
+    e2e_steps = min(args.steps, 200)
+    host = {k: sets[0][k].cpu().pin_memory() for k in ("x", "res", "dy", "gamma", "beta")}
+    outs_h = {k: torch.empty(sets[0][k].shape, dtype=sets[0][k].dtype).pin_memory()
+              for k in ("out", "res_out", "dx", "mean", "rstd", "dgamma", "dbeta")}
+    dev = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for k, t in host.items():
+                dev[k].copy_(t, non_blocking=True)
+            fwd(0)
+            ln.bwd(dev["dy"], dev["res_out"], dev["gamma"], dev["mean"], dev["rstd"],
+                   dx=dev["dx"], dgamma=dev["dgamma"], dbeta=dev["dbeta"], workspace=ws,
+                   stream=stream)
+            for k, t in outs_h.items():
+                t.copy_(dev[k], non_blocking=True)
+    stream.synchronize()
+    e2e_s = max_over_ranks(world, time.perf_counter() - t0)
+    barrier(world)
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
+    dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
+    kname = {"fwd": "ln_fwd", "bwd": "ln_bwd"}[dom]
+    achieved = kern[dom]["gbs"]
+    cpu = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=10.0)
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "rows": R, "cols": C, "io_dtype": w.dtype,
+                   "accumulate": "fp32", "global_batch_rows": R * world,
+                   "l2": f"rotating {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB > "
+                         f"3x L2 ({l2 / 1e6:.0f} MB); backward reads the set half a cycle back",
+                   "timing": f"CUDA graph of {chunk} steps replayed {args.steps // chunk} times",
+                   "parallelism": f"replicas x{world}"},
+        "rows_per_s": world * R * args.steps / (ms_total * 1e-3),
+        "frac_of_8tbs": value / world / ROOFLINE_NOMINAL_GBS,
+        "kernels": kern,
+        "clocks": clocks,
+        "e2e": {"value": world * step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_s / e2e_steps * 1e3},
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": profiled_traffic(kname)},
+        "cpu_baseline": {"value": cpu["value"], "unit": "GB/s", "cores": cpu["cores"],
+                         "kind": "oracle", "sample": cpu["sample"]},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_8192x768")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
