@@ -154,6 +154,31 @@ ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const l
                          size_t workspace_bytes, ln_stream_t stream);
 
 /*
+ * Backward (bf16) that allocates nothing.  The pages have no counterpart to this entry
+ * point: it exists for callers that cannot call cudaMalloc when they run the backward --
+ * a serving process that reserved its whole device-memory budget at start-up, or a plugin
+ * whose host framework owns every device allocation -- and cannot hand in a workspace
+ * either.  Arguments, results and errors are those of ln_bwd_bf16; the scratch (counters
+ * and per-block partial sums) lives in a fixed array of LN_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * compiled into the library, which every GPU that loads the library holds until exit.
+ *  - Problems whose scratch would exceed that size are rejected with LN_EUNSUPPORTED
+ *    (roughly: 16 * cols * min(rows, 8 * SM count) + 256 bytes must fit; 8192 x 768 and
+ *    8192 x 1280 do, 4096 x 8192 does not).
+ *  - The first call on each device looks up the array's device address (once, with that
+ *    device current); make that first call before any stream capture begins.
+ *  - All calls share the one array, and each call first clears its counters on `stream`:
+ *    calls whose work overlaps on the GPU (different streams, or different host threads
+ *    without ordering) race and corrupt each other's results; order them.
+ *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ */
+#define LN_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_res_out,
+                              const ln_bf16* gamma, const float* mean, const float* rstd,
+                              ln_bf16* dx, ln_bf16* dgamma, ln_bf16* dbeta, int64_t rows,
+                              int64_t cols, ln_stream_t stream);
+
+/*
  * Device-side status.  Every wait inside a kernel (the bulk-copy barrier of the wide-row
  * kernels, the backward's wait for the last blocks) is bounded; when one runs out the
  * kernel records LN_ETIMEOUT in a per-device status word and returns early without

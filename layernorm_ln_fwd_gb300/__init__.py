@@ -48,6 +48,7 @@ SIGNATURES = {
     "ln_debug_force_path": (_INT, [_INT]),
     "ln_debug_wait_test": (None, [ctypes.c_uint]),
     "ln_last_launch_count": (_INT, []),
+    "ln_bwd_bf16_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
 }
 
 

@@ -96,6 +96,8 @@ int blocks_per_sm(const void* kernel, int threads, size_t smem) {
     return n;
 }
 
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
+
 bool vector_ok(Dtype dt, int cols, const void* const* ptrs, int nptrs) {
     const int esize = dt == Dtype::F32 ? 4 : 2;
     if (((size_t)cols * esize) % 16 != 0) return false;

@@ -97,4 +97,7 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStre
 // Occupancy (resident blocks per SM) of a kernel, cached per (device, kernel, threads, smem).
 int blocks_per_sm(const void* kernel, int threads, size_t smem);
 
+// Records `e` as the value ln_last_cuda_error() reports on this host thread.
+void record_cuda_error(cudaError_t e);
+
 }  // namespace lnk
