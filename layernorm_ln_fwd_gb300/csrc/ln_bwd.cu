@@ -721,8 +721,20 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.finishers = p.finishers;
     k.stages = p.stages;
     void* args[] = {&k};
-    cudaError_t e = cudaLaunchCooperativeKernel(kern, dim3(p.grid), dim3(p.threads), args,
-                                                p.smem, stream);
+    // A cooperative launch (all blocks co-resident, checked by the driver against the
+    // occupancy), issued through cudaLaunchKernelEx so that it can also be captured into a
+    // CUDA graph.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(p.threads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
     if (e == cudaSuccess) *launches = 1;
     return e;
 }
