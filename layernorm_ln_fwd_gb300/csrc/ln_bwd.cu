@@ -32,8 +32,8 @@
 //    register holds the rounding error of every addition) whenever a thread owns at most 16
 //    columns (rows up to 8192 columns wide; wider rows keep plain fp32 sums: the registers
 //    for compensation are not there);
-//  * the warp kernel (bf16, short per-lane chains) keeps plain per-lane sums and combines
-//    its warps with error-free additions (TwoSum);
+//  * the warp (tile) kernel (bf16, short per-lane chains) keeps plain per-lane sums and
+//    combines its warps with error-free additions (TwoSum);
 //  * partial sums are stored as (hi, lo) fp32 pairs and the finishers add them with TwoSum,
 //    so the only rounding left at the end is the final one to the output type.
 #include <algorithm>
@@ -44,7 +44,10 @@
 namespace lnk {
 namespace {
 
-constexpr int kBwdWarpThreads = 256;  // 8 warps, one row per warp at a time
+// Consumer warps = rows per tile, plus one producer warp: 8 warps, because registers are
+// allocated to warps in groups of four (a 9-warp block would pay for 12).
+constexpr int kTileRows = 7;
+constexpr int kTileThreads = (kTileRows + 1) * 32;
 constexpr int kBwdBlockMaxThreads = 512;
 constexpr int kBwdScalarThreads = 256;
 constexpr int kMaxStages = 4;
@@ -212,110 +215,169 @@ __device__ void arrive_and_finish(const KParams& a, float* scratch) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Warp per row.  Lane l owns the columns of vectors l, l+32, ... in every row its warp
-// handles, so its column sums stay in registers; the 8 warps of a block are then added in
-// warp order with TwoSum through shared memory, one statistic at a time.
+// Warp per row, fed by a bulk-copy (TMA) pipeline (the forward's tile kernel, for dy and x).
+// The block owns a fixed contiguous range of tiles (7 consecutive rows each); the producer
+// warp's lane 0 fetches each tile of dy and of x with one cp.async.bulk apiece, `stages`
+// tiles ahead; consumer warp w handles row w of every tile.  Lane l owns the columns of
+// vectors l, l+32, ... in every row, so its column sums stay in registers; at the end the
+// 7 consumer warps' sums are added in warp order with TwoSum through shared memory (the
+// drained ring), one statistic at a time, into the block's (hi, lo) partial row.
 // ---------------------------------------------------------------------------------------
 template <typename T, int VPL>
-__global__ void __launch_bounds__(kBwdWarpThreads) bwd_warp_kernel(const KParams a) {
+__global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kernel(const KParams a) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
-    constexpr int W = kBwdWarpThreads / 32;
-    extern __shared__ __align__(16) float smem_f[];  // [W][cols]; later the finish scratch
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cols = a.cols, nvec = cols / V;
+    const int cols = a.cols, nvec = cols / V, stages = a.stages, rows = a.rows;
     const float fcols = (float)cols;
+    const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
+    const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
+    const unsigned slot_bytes = 2u * tile_bytes;
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
     const T* __restrict__ xr = static_cast<const T*>(a.xr);
     const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
     T* __restrict__ dx = static_cast<T*>(a.dx);
-    int r0, r1;
-    row_range(a.rows, r0, r1);
+    int t0, t1;
+    row_range((rows + kTileRows - 1) / kTileRows, t0, t1);  // this block's tiles
+    const int my_tiles = t1 - t0;
 
-    uint4 gv[VPL];
+    if (tid == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kTileRows);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
     float accg[VPL][V], accb[VPL][V];
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-        const int vi = v * 32 + lane;
-        gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+    for (int v = 0; v < VPL; ++v)
 #pragma unroll
         for (int k = 0; k < V; ++k) accg[v][k] = accb[v][k] = 0.f;
-    }
 
-    for (int row = r0 + warp; row < r1; row += W) {
-        const size_t base = (size_t)row * cols;
-        uint4 dv[VPL], xv[VPL];
+    if (warp == kTileRows) {  // producer
+        if (lane == 0) {
+            int k = 0;
+            for (; k < my_tiles; ++k) {
+                const int slot = k % stages;
+                if (k >= stages &&
+                    !mbar_wait(&empty_bar[slot], (unsigned)(k / stages - 1) & 1u, a.limit_ns)) {
+                    raise_status(a.status, kStatusTimeout);
+                    break;
+                }
+                const int r0 = (t0 + k) * kTileRows;
+                const unsigned bytes = (unsigned)min(kTileRows, rows - r0) * row_bytes;
+                unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
+                mbar_arrive_expect_tx(&full_bar[slot], 2u * bytes);
+                bulk_g2s(dst, dy + (size_t)r0 * cols, bytes, &full_bar[slot]);
+                bulk_g2s(dst + tile_bytes, xr + (size_t)r0 * cols, bytes, &full_bar[slot]);
+            }
+            for (int j = max(0, k - stages); j < k; ++j)  // drain: every copy has landed
+                (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
+        }
+    } else {  // consumers
+        uint4 gv[VPL];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
             const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                dv[v] = ld_stream(dy + base + (size_t)vi * V);
-                xv[v] = ld_stream(xr + base + (size_t)vi * V);
-            }
+            gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
         }
-        const float mu = a.mean[row], rs = a.rstd[row];
-        float sg = 0.f, sgx = 0.f;
+        // mean and rstd of the warp's row in the next tile are loaded one tile ahead, so
+        // their latency is not on the row's critical path.
+        int row = t0 * kTileRows + warp;
+        float mu_next = row < rows ? a.mean[row] : 0.f;
+        float rs_next = row < rows ? a.rstd[row] : 0.f;
+        for (int k = 0; k < my_tiles; ++k, row += kTileRows) {
+            const int slot = k % stages;
+            const float mu = mu_next, rs = rs_next;
+            if (row + kTileRows < rows && k + 1 < my_tiles) {
+                mu_next = a.mean[row + kTileRows];
+                rs_next = a.rstd[row + kTileRows];
+            }
+            const bool ok = mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, a.limit_ns);
+            if (!__all_sync(kFullMask, ok)) {
+                if (lane == 0) raise_status(a.status, kStatusTimeout);
+                break;
+            }
+            if (row < rows) {
+                const size_t base = (size_t)row * cols;
+                const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
+                                                          (size_t)warp * row_bytes);
+                const T* xs = dys + (size_t)kTileRows * cols;
+                float sg = 0.f, sgx = 0.f;
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            if (v * 32 + lane < nvec) {
-                float d[V], xx[V], gm[V];
-                IO::unpack(dv[v], d);
-                IO::unpack(xv[v], xx);
-                IO::unpack(gv[v], gm);
+                for (int v = 0; v < VPL; ++v) {
+                    const int vi = v * 32 + lane;
+                    if (vi < nvec) {
+                        float d[V], xx[V], gm[V];
+                        IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                        IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        IO::unpack(gv[v], gm);
 #pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float xh = (xx[k] - mu) * rs;
-                    const float g = __fmul_rn(gm[k], d[k]);
-                    sg += g;
-                    sgx += g * xh;
-                    accg[v][k] += d[k] * xh;
-                    accb[v][k] += d[k];
+                        for (int q = 0; q < V; ++q) {
+                            const float xh = (xx[q] - mu) * rs;
+                            const float g = __fmul_rn(gm[q], d[q]);
+                            sg += g;
+                            sgx += g * xh;
+                            accg[v][q] += d[q] * xh;
+                            accb[v][q] += d[q];
+                        }
+                    }
+                }
+                warp_sum2(sg, sgx);  // the one reduction of the row: both sums together
+                const float mg = sg / fcols, mgx = sgx / fcols;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                    const int vi = v * 32 + lane;
+                    if (vi < nvec) {  // second pass re-reads the row from shared memory
+                        float d[V], xx[V], gm[V], o[V];
+                        IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                        IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        IO::unpack(gv[v], gm);
+#pragma unroll
+                        for (int q = 0; q < V; ++q) {
+                            const float xh = (xx[q] - mu) * rs;
+                            o[q] = rs * (__fmul_rn(gm[q], d[q]) - (mg + xh * mgx));
+                        }
+                        st_stream(dx + base + (size_t)vi * V, IO::pack(o));
+                    }
                 }
             }
-        }
-        warp_sum2(sg, sgx);  // the one reduction of the row: both sums together
-        const float mg = sg / fcols, mgx = sgx / fcols;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                float d[V], xx[V], gm[V], o[V];
-                IO::unpack(dv[v], d);
-                IO::unpack(xv[v], xx);
-                IO::unpack(gv[v], gm);
-#pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float xh = (xx[k] - mu) * rs;
-                    o[k] = rs * (__fmul_rn(gm[k], d[k]) - (mg + xh * mgx));
-                }
-                st_stream(dx + base + (size_t)vi * V, IO::pack(o));
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[slot]);
         }
     }
+    __syncthreads();  // the ring is drained and no warp reads it any more
 
-    // Block partial row: add the W warps' sums in warp order (TwoSum), one statistic at a
-    // time, and store the (hi, lo) pair.
+    // Block partial row: add the consumer warps' sums in warp order (TwoSum), one statistic
+    // at a time, and store the (hi, lo) pair.
+    float* smem_f = reinterpret_cast<float*>(smem_raw);  // [kTileRows][cols]
     const int P = gridDim.x;
 #pragma unroll
     for (int stat = 0; stat < 2; ++stat) {
+        if (warp < kTileRows) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                float* dst = smem_f + (size_t)warp * cols + (size_t)vi * V;
+            for (int v = 0; v < VPL; ++v) {
+                const int vi = v * 32 + lane;
+                if (vi < nvec) {
+                    float* dst = smem_f + (size_t)warp * cols + (size_t)vi * V;
 #pragma unroll
-                for (int k = 0; k < V; k += 4)
-                    *reinterpret_cast<float4*>(dst + k) =
-                        stat == 0 ? make_float4(accg[v][k], accg[v][k + 1], accg[v][k + 2], accg[v][k + 3])
-                                  : make_float4(accb[v][k], accb[v][k + 1], accb[v][k + 2], accb[v][k + 3]);
+                    for (int k = 0; k < V; k += 4)
+                        *reinterpret_cast<float4*>(dst + k) =
+                            stat == 0 ? make_float4(accg[v][k], accg[v][k + 1], accg[v][k + 2], accg[v][k + 3])
+                                      : make_float4(accb[v][k], accb[v][k + 1], accb[v][k + 2], accb[v][k + 3]);
+                }
             }
         }
         __syncthreads();
         float2* prow = a.part + ((size_t)stat * P + blockIdx.x) * cols;
-        for (int c = tid; c < cols; c += kBwdWarpThreads) {
+        for (int c = tid; c < cols; c += blockDim.x) {
             float S = 0.f, C = 0.f;
 #pragma unroll
-            for (int w = 0; w < W; ++w) comp_add(S, C, smem_f[(size_t)w * cols + c], 0.f);
+            for (int w = 0; w < kTileRows; ++w) comp_add(S, C, smem_f[(size_t)w * cols + c], 0.f);
             prow[c] = make_float2(S, C);
         }
         __syncthreads();
@@ -385,13 +447,19 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         for (int k = 0; k < V; ++k) sg_c[v][k] = sb_c[v][k] = 0.f;
 
     int k = 0;
+    // mean and rstd are loaded one row ahead (off the row's critical path).
+    float mu_next = r0 < r1 ? a.mean[r0] : 0.f, rs_next = r0 < r1 ? a.rstd[r0] : 0.f;
     for (int row = r0; row < r1; ++row, ++k) {
         const int slot = k % stages;
+        const float mu = mu_next, rs = rs_next;
+        if (row + 1 < r1) {
+            mu_next = a.mean[row + 1];
+            rs_next = a.rstd[row + 1];
+        }
         if (!mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, a.limit_ns)) abort_flag = 1;
         const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
-        const float mu = a.mean[row], rs = a.rstd[row];
         float sg = 0.f, sgx = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -570,23 +638,23 @@ template <typename T>
 const void* warp_kernel(int vpl) {
     if constexpr (Io<T>::kVec == 8) {
         switch (vpl) {
-            case 1: return (const void*)bwd_warp_kernel<T, 1>;
-            case 2: return (const void*)bwd_warp_kernel<T, 2>;
-            case 3: return (const void*)bwd_warp_kernel<T, 3>;
-            case 4: return (const void*)bwd_warp_kernel<T, 4>;
-            case 5: return (const void*)bwd_warp_kernel<T, 5>;
+            case 1: return (const void*)bwd_tile_kernel<T, 1>;
+            case 2: return (const void*)bwd_tile_kernel<T, 2>;
+            case 3: return (const void*)bwd_tile_kernel<T, 3>;
+            case 4: return (const void*)bwd_tile_kernel<T, 4>;
+            case 5: return (const void*)bwd_tile_kernel<T, 5>;
             default: return nullptr;
         }
     } else {
         switch (vpl) {
-            case 1: return (const void*)bwd_warp_kernel<T, 1>;
-            case 2: return (const void*)bwd_warp_kernel<T, 2>;
-            case 3: return (const void*)bwd_warp_kernel<T, 3>;
-            case 4: return (const void*)bwd_warp_kernel<T, 4>;
-            case 5: return (const void*)bwd_warp_kernel<T, 5>;
-            case 6: return (const void*)bwd_warp_kernel<T, 6>;
-            case 7: return (const void*)bwd_warp_kernel<T, 7>;
-            case 8: return (const void*)bwd_warp_kernel<T, 8>;
+            case 1: return (const void*)bwd_tile_kernel<T, 1>;
+            case 2: return (const void*)bwd_tile_kernel<T, 2>;
+            case 3: return (const void*)bwd_tile_kernel<T, 3>;
+            case 4: return (const void*)bwd_tile_kernel<T, 4>;
+            case 5: return (const void*)bwd_tile_kernel<T, 5>;
+            case 6: return (const void*)bwd_tile_kernel<T, 6>;
+            case 7: return (const void*)bwd_tile_kernel<T, 7>;
+            case 8: return (const void*)bwd_tile_kernel<T, 8>;
             default: return nullptr;
         }
     }
@@ -659,9 +727,14 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
                           (path_override == kPathAuto && warp_auto))) {
             p.path = kPathWarp;
             p.per_thread = vpl;
-            p.threads = kBwdWarpThreads;
-            p.smem = std::max<size_t>((size_t)(kBwdWarpThreads / 32) * cols * 4,
-                                      (size_t)kBwdWarpThreads * 16);
+            p.threads = kTileThreads;
+            const size_t slot = 2ull * kTileRows * cols * esize;  // a tile of dy and of x
+            int stages = (int)std::min<size_t>(kMaxStages, ((size_t)di.smem_optin / 2) / slot);
+            stages = std::max(2, stages);
+            p.stages = stages;
+            // The ring, reused afterwards for the warps' sums and the finish scratch.
+            p.smem = std::max<size_t>({(size_t)stages * slot, (size_t)kTileRows * cols * 4,
+                                       (size_t)kTileThreads * 16});
         } else {
             p.path = kPathBlock;
             p.per_thread = (nvec + kBwdBlockMaxThreads - 1) / kBwdBlockMaxThreads;
@@ -690,7 +763,7 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
     if (e != cudaSuccess) return e;
     const int occ = blocks_per_sm(kern, p.threads, p.smem);
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int need = p.path == kPathWarp ? (rows + 7) / 8 : rows;
+    const int need = p.path == kPathWarp ? (rows + kTileRows - 1) / kTileRows : rows;
     p.grid = std::max(1, std::min(need, di.sms * occ));
     p.finishers = pick_finishers(p.grid, cols, p.threads);
     *plan = p;

@@ -122,7 +122,9 @@ __device__ __forceinline__ void stats_merge(RowStats& a, const RowStats& b) {
         const float sa = __fadd_rn(a.s, a.c), sb = __fadd_rn(b.s, b.c);
         const float t = __fsub_rn(__fmul_rn(a.n, sb), __fmul_rn(b.n, sa));
         const float den = __fmul_rn(__fmul_rn(a.n, b.n), nn);
-        a.q = __fadd_rn(__fadd_rn(a.q, b.q), __fdiv_rn(__fmul_rn(t, t), den));
+        // A correction term: the fast division's ~2 ulp error is immaterial, and both lanes
+        // of a pair divide the same operands.
+        a.q = __fadd_rn(__fadd_rn(a.q, b.q), __fdividef(__fmul_rn(t, t), den));
     } else {
         a.q = __fadd_rn(a.q, b.q);
     }
@@ -145,31 +147,43 @@ __device__ __forceinline__ void warp_stats(RowStats& r) {
     }
 }
 
-// A thread's own summary of the values v[0..count) (already shifted): compensated sum, then
-// M2 about the thread's mean in a second pass over its registers.
+// Merge the summaries of a block's warps (red[0..3][w], w < nw) the same way in every warp:
+// lane w holds warp w's summary and one butterfly combines them, so every thread of the block
+// ends with the same bits without a per-thread sequential merge.
+__device__ __forceinline__ RowStats block_stats(const float (*red)[32], int nw) {
+    const int lane = threadIdx.x & 31;
+    RowStats r{0.f, 0.f, 0.f, 0.f};
+    if (lane < nw) r = RowStats{red[0][lane], red[1][lane], red[2][lane], red[3][lane]};
+    warp_stats(r);
+    return r;
+}
+
+// A thread's own summary of the values v[0..count) (already shifted): their sum in four
+// independent partial sums (short chains, so the adds overlap), then M2 about the thread's
+// mean, again in four partial sums.  A thread holds at most 64 values; across threads the
+// sums are combined by stats_merge, which keeps the compensation.
 template <int N>
 __device__ __forceinline__ RowStats thread_stats(const float (&v)[N], int count) {
-    RowStats r{0.f, 0.f, 0.f, 0.f};
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        if (i < count) {
-            float s, e;
-            two_sum_f(r.s, v[i], s, e);
-            r.s = s;
-            r.c = __fadd_rn(r.c, e);
-        }
-    }
+    for (int i = 0; i < N; ++i)
+        if (i < count) s4[i & 3] += v[i];
+    RowStats r;
+    r.s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    r.c = 0.f;
     r.n = (float)count;
+    float q4[4] = {0.f, 0.f, 0.f, 0.f};
     if (count > 0) {
-        const float m = __fdiv_rn(__fadd_rn(r.s, r.c), r.n);
+        const float m = __fdiv_rn(r.s, r.n);
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             if (i < count) {
                 const float e = v[i] - m;
-                r.q += e * e;
+                q4[i & 3] += e * e;
             }
         }
     }
+    r.q = (q4[0] + q4[1]) + (q4[2] + q4[3]);
     return r;
 }
 
@@ -229,6 +243,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned by
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes,

@@ -17,8 +17,9 @@
 // mean = K + mean(d) and rstd = 1 / sqrt(M2 / n + eps) are stored in fp32.
 //
 // Three kernel families compute the same function:
-//  * warp per row (rows of at most 256 vectors of 16 bytes): each lane holds its part of
-//    the row in registers, 128-bit loads and stores, one xor butterfly, no block barrier;
+//  * warp per row (rows of at most 256 vectors of 16 bytes): tiles of 7 rows are staged in
+//    shared memory by bulk copies several tiles ahead; each warp normalises one row with
+//    128-bit reads and stores and one xor butterfly, no block barrier;
 //  * block per row (wider rows): a persistent block streams rows into shared memory with
 //    bulk copies (cp.async.bulk, completed on an mbarrier) several rows ahead, so each row
 //    is read from HBM once; one warp butterfly plus one cross-warp exchange per row;
@@ -31,28 +32,80 @@
 namespace lnk {
 namespace {
 
-constexpr int kFwdWarpThreads = 256;  // 8 warps, one row per warp at a time
+// Consumer warps = rows per tile, plus one producer warp: 8 warps, because registers are
+// allocated to warps in groups of four (a 9-warp block would pay for 12).
+constexpr int kTileRows = 7;
+constexpr int kTileThreads = (kTileRows + 1) * 32;
 constexpr int kFwdBlockMaxThreads = 512;
 constexpr int kFwdScalarThreads = 256;
 constexpr int kMaxStages = 4;
 
 // ---------------------------------------------------------------------------------------
-// Warp per row.
+// Warp per row, fed by a bulk-copy (TMA) pipeline.
+//
+// A block has kTileRows (7) consumer warps and one producer warp.  A tile is kTileRows
+// consecutive rows -- one contiguous stretch of memory per tensor -- so the producer's lane 0
+// fetches a whole tile of x (and of res) with one cp.async.bulk each, `stages` tiles ahead,
+// into a ring of shared-memory slots.  Each consumer warp normalises one row of the tile
+// from shared memory (128-bit reads, lane l holds vectors l, l+32, ...), writes res_out and
+// out with 128-bit streaming stores, and releases the slot.  The full barrier of a slot
+// completes when its copies land; the empty barrier when all consumer warps are done.
+// The bytes in flight per SM are set by the ring, not by the registers of resident warps.
 // ---------------------------------------------------------------------------------------
 template <typename T, int VPL, bool HAS_RES>
-__global__ void __launch_bounds__(kFwdWarpThreads)
-    fwd_warp_kernel(const T* __restrict__ x, const T* __restrict__ res,
+__global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
+    fwd_tile_kernel(const T* __restrict__ x, const T* __restrict__ res,
                     const T* __restrict__ gamma, const T* __restrict__ beta, float eps, int rows,
                     int cols, T* __restrict__ out, T* __restrict__ res_out,
-                    float* __restrict__ mean, float* __restrict__ rstd) {
+                    float* __restrict__ mean, float* __restrict__ rstd, int stages,
+                    unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
-    const int lane = threadIdx.x & 31;
-    const int warps_per_block = kFwdWarpThreads / 32;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = cols / V;
     const float fcols = (float)cols;
+    const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
+    const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
+    const unsigned slot_bytes = (HAS_RES ? 2u : 1u) * tile_bytes;
+    const int ntiles = (rows + kTileRows - 1) / kTileRows;
+    const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
-    // gamma and beta stay in registers (packed) for all rows this warp normalises.
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], kTileRows);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kTileRows) {  // producer
+        if (lane == 0) {
+            int k = 0;
+            for (; k < my_tiles; ++k) {
+                const int slot = k % stages;
+                if (k >= stages &&
+                    !mbar_wait(&empty_bar[slot], (unsigned)(k / stages - 1) & 1u, wait_limit_ns)) {
+                    raise_status(status, kStatusTimeout);
+                    break;
+                }
+                const int r0 = ((int)blockIdx.x + k * (int)gridDim.x) * kTileRows;
+                const unsigned bytes = (unsigned)min(kTileRows, rows - r0) * row_bytes;
+                unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
+                mbar_arrive_expect_tx(&full_bar[slot], (HAS_RES ? 2u : 1u) * bytes);
+                bulk_g2s(dst, x + (size_t)r0 * cols, bytes, &full_bar[slot]);
+                if (HAS_RES) bulk_g2s(dst + tile_bytes, res + (size_t)r0 * cols, bytes, &full_bar[slot]);
+            }
+            // Every copy issued has landed before this block's shared memory is released.
+            for (int j = max(0, k - stages); j < k; ++j)
+                (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, wait_limit_ns);
+        }
+        return;
+    }
+
+    // Consumers: gamma and beta stay packed in registers for every row.
     uint4 gv[VPL], bv[VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
@@ -60,69 +113,72 @@ __global__ void __launch_bounds__(kFwdWarpThreads)
         gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
         bv[v] = vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
     }
-
     const bool write_res = res_out != nullptr;
-    for (int row = blockIdx.x * warps_per_block + (threadIdx.x >> 5); row < rows;
-         row += gridDim.x * warps_per_block) {
-        const size_t base = (size_t)row * cols;
-        uint4 xv[VPL], rv[VPL];
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                xv[v] = ld_stream(x + base + (size_t)vi * V);
-                if (HAS_RES) rv[v] = ld_stream(res + base + (size_t)vi * V);
-            }
+    for (int k = 0; k < my_tiles; ++k) {
+        const int slot = k % stages;
+        const bool ok = mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, wait_limit_ns);
+        if (!__all_sync(kFullMask, ok)) {
+            if (lane == 0) raise_status(status, kStatusTimeout);
+            break;
         }
-        // s = x + res, rounded to the stored type; it is what gets normalised.
-        float s[VPL][V];
+        const int row = ((int)blockIdx.x + k * (int)gridDim.x) * kTileRows + warp;
+        if (row < rows) {
+            const size_t base = (size_t)row * cols;
+            const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
+                                                     (size_t)warp * row_bytes);
+            const T* rsm = xs + (size_t)kTileRows * cols;
+            // s = x + res, rounded to the stored type; it is what gets normalised.
+            float s[VPL][V];
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                IO::unpack(xv[v], s[v]);
-                if (HAS_RES) {
-                    float r[V];
-                    IO::unpack(rv[v], r);
+            for (int v = 0; v < VPL; ++v) {
+                const int vi = v * 32 + lane;
+                if (vi < nvec) {
+                    IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), s[v]);
+                    if (HAS_RES) {
+                        float r[V];
+                        IO::unpack(*reinterpret_cast<const uint4*>(rsm + (size_t)vi * V), r);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) s[v][k] = IO::round(s[v][k] + r[k]);
+                        for (int q = 0; q < V; ++q) s[v][q] = IO::round(s[v][q] + r[q]);
+                    }
+                    if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < V; ++q) s[v][q] = 0.f;
                 }
-                if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
-            } else {
+            }
+            // Shift: the row's first stored element (lane 0 always holds it).
+            const float K = __shfl_sync(kFullMask, s[0][0], 0);
+            float dv[VPL * V];
+            int cnt = 0;
 #pragma unroll
-                for (int k = 0; k < V; ++k) s[v][k] = 0.f;
+            for (int v = 0; v < VPL; ++v) {
+#pragma unroll
+                for (int q = 0; q < V; ++q) dv[v * V + q] = s[v][q] - K;
+                if (v * 32 + lane < nvec) cnt += V;
+            }
+            RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
+            warp_stats(st);                        // the one reduction of the row
+            const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
+            const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+            if (lane == 0) {
+                mean[row] = K + md;
+                rstd[row] = rs;
+            }
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const int vi = v * 32 + lane;
+                if (vi < nvec) {
+                    float g[V], b[V], o[V];
+                    IO::unpack(gv[v], g);
+                    IO::unpack(bv[v], b);
+#pragma unroll
+                    for (int q = 0; q < V; ++q) o[q] = g[q] * ((s[v][q] - K - md) * rs) + b[q];
+                    st_stream(out + base + (size_t)vi * V, IO::pack(o));
+                }
             }
         }
-        // Shift: the row's first stored element (lane 0 always holds it).
-        const float K = __shfl_sync(kFullMask, s[0][0], 0);
-        float dv[VPL * V];
-        int cnt = 0;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-#pragma unroll
-            for (int k = 0; k < V; ++k) dv[v * V + k] = s[v][k] - K;
-            if (v * 32 + lane < nvec) cnt += V;
-        }
-        RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
-        warp_stats(st);                        // the one reduction of the row
-        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
-        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
-        if (lane == 0) {
-            mean[row] = K + md;
-            rstd[row] = rs;
-        }
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                float g[V], b[V], o[V];
-                IO::unpack(gv[v], g);
-                IO::unpack(bv[v], b);
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = g[k] * ((s[v][k] - K - md) * rs) + b[k];
-                st_stream(out + base + (size_t)vi * V, IO::pack(o));
-            }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp is done with the slot
     }
 }
 
@@ -143,10 +199,9 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                      unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
-    constexpr int MAXW = kFwdBlockMaxThreads / 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages];
-    __shared__ float red[4][MAXW];
+    __shared__ float red[4][32];
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -235,9 +290,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         }
         __syncthreads();  // the one cross-warp exchange of the row
         if (abort_flag) break;
-        st = RowStats{red[0][0], red[1][0], red[2][0], red[3][0]};
-        for (int w = 1; w < nw; ++w)  // same order in every thread: same bits everywhere
-            stats_merge(st, RowStats{red[0][w], red[1][w], red[2][w], red[3][w]});
+        st = block_stats(red, nw);  // the same bits in every thread
         const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
         const float rs = 1.0f / sqrtf(st.q / fcols + eps);
         if (tid == 0) {
@@ -287,7 +340,7 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
                       float* __restrict__ mean, float* __restrict__ rstd) {
     using IO = Io<T>;
     constexpr int NW = kFwdScalarThreads / 32;
-    __shared__ float red[4][NW];
+    __shared__ float red[4][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float fcols = (float)cols;
     const bool write_res = res_out != nullptr;
@@ -323,10 +376,7 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
             red[3][warp] = st.q;
         }
         __syncthreads();
-        st = RowStats{red[0][0], red[1][0], red[2][0], red[3][0]};
-#pragma unroll
-        for (int w = 1; w < NW; ++w)
-            stats_merge(st, RowStats{red[0][w], red[1][w], red[2][w], red[3][w]});
+        st = block_stats(red, NW);
         const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
         const float rs = 1.0f / sqrtf(st.q / fcols + eps);
         if (tid == 0) {
@@ -349,29 +399,37 @@ template <typename T>
 cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     const void* kern = nullptr;
     const bool has_res = a.res != nullptr;
-#define LNK_FWD_WARP_CASE(N)                                                               \
+#define LNK_FWD_TILE_CASE(N)                                                               \
     case N:                                                                                \
-        kern = has_res ? (const void*)fwd_warp_kernel<T, N, true>                          \
-                       : (const void*)fwd_warp_kernel<T, N, false>;                        \
+        kern = has_res ? (const void*)fwd_tile_kernel<T, N, true>                          \
+                       : (const void*)fwd_tile_kernel<T, N, false>;                        \
         break;
     switch (vpl) {
-        LNK_FWD_WARP_CASE(1)
-        LNK_FWD_WARP_CASE(2)
-        LNK_FWD_WARP_CASE(3)
-        LNK_FWD_WARP_CASE(4)
-        LNK_FWD_WARP_CASE(5)
-        LNK_FWD_WARP_CASE(6)
-        LNK_FWD_WARP_CASE(7)
-        LNK_FWD_WARP_CASE(8)
+        LNK_FWD_TILE_CASE(1)
+        LNK_FWD_TILE_CASE(2)
+        LNK_FWD_TILE_CASE(3)
+        LNK_FWD_TILE_CASE(4)
+        LNK_FWD_TILE_CASE(5)
+        LNK_FWD_TILE_CASE(6)
+        LNK_FWD_TILE_CASE(7)
+        LNK_FWD_TILE_CASE(8)
         default:
             return cudaErrorInvalidValue;
     }
-#undef LNK_FWD_WARP_CASE
+#undef LNK_FWD_TILE_CASE
     const DeviceInfo& di = device_info(-1);
-    const int warps = kFwdWarpThreads / 32;
-    const int need = (a.rows + warps - 1) / warps;
-    const int occ = std::max(1, blocks_per_sm(kern, kFwdWarpThreads, 0));
-    const int grid = std::max(1, std::min(need, di.sms * occ));
+    const size_t slot_bytes = (size_t)(has_res ? 2 : 1) * kTileRows * a.cols * sizeof(T);
+    // Two to four tiles in flight per block, two blocks per SM when they fit.
+    int stages = (int)std::min<size_t>(kMaxStages, ((size_t)di.smem_optin / 2) / slot_bytes);
+    stages = std::max(2, stages);
+    const size_t smem = (size_t)stages * slot_bytes;
+    if (smem > (size_t)di.smem_optin) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const int ntiles = (a.rows + kTileRows - 1) / kTileRows;
+    const int occ = std::max(1, blocks_per_sm(kern, kTileThreads, smem));
+    const int grid = std::max(1, std::min(ntiles, di.sms * occ));
     const T* x = static_cast<const T*>(a.x);
     const T* res = static_cast<const T*>(a.res);
     const T* gamma = static_cast<const T*>(a.gamma);
@@ -382,15 +440,22 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     int rows = a.rows, cols = a.cols;
     float* mean = a.mean;
     float* rstd = a.rstd;
-    void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd};
-    return cudaLaunchKernel(kern, dim3(grid), dim3(kFwdWarpThreads), args, 0, stream);
+    unsigned* status = a.status;
+    uint64_t limit = a.wait_limit_ns;
+    void* args[] = {&x,   &res,     &gamma, &beta, &eps,    &rows,   &cols,
+                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
+    return cudaLaunchKernel(kern, dim3(grid), dim3(kTileThreads), args, smem, stream);
 }
 
 template <typename T>
 cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
     const int nvec = a.cols / V;
-    const int vpt = (nvec + kFwdBlockMaxThreads - 1) / kFwdBlockMaxThreads;
+    // 256 threads per row keep two blocks (two rows being normalised) on an SM; rows too
+    // wide for that (more than 4 bf16 or 8 fp32 vectors per thread) take 512 threads.
+    constexpr int kMaxVpt = V == 8 ? 4 : 8;
+    int vpt = (nvec + 255) / 256;
+    if (vpt > kMaxVpt) vpt = (nvec + kFwdBlockMaxThreads - 1) / kFwdBlockMaxThreads;
     const int threads = std::max(32, ((nvec + vpt - 1) / vpt + 31) / 32 * 32);
     const bool has_res = a.res != nullptr;
     const void* kern = nullptr;
