@@ -279,11 +279,11 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
                 (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
         }
     } else {  // consumers
-        uint4 gv[VPL];
+        float gm[VPL][V];  // gamma of this lane's columns, unpacked once
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
             const int vi = v * 32 + lane;
-            gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+            IO::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
         }
         // mean and rstd of the warp's row in the next tile are loaded one tile ahead, so
         // their latency is not on the row's critical path.
@@ -307,40 +307,46 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
                 const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
                                                           (size_t)warp * row_bytes);
                 const T* xs = dys + (size_t)kTileRows * cols;
-                float sg = 0.f, sgx = 0.f;
+                float sg0 = 0.f, sg1 = 0.f, sgx0 = 0.f, sgx1 = 0.f;
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
                     const int vi = v * 32 + lane;
                     if (vi < nvec) {
-                        float d[V], xx[V], gm[V];
+                        float d[V], xx[V];
                         IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
                         IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-                        IO::unpack(gv[v], gm);
 #pragma unroll
-                        for (int q = 0; q < V; ++q) {
-                            const float xh = (xx[q] - mu) * rs;
-                            const float g = __fmul_rn(gm[q], d[q]);
-                            sg += g;
-                            sgx += g * xh;
-                            accg[v][q] += d[q] * xh;
+                        for (int q = 0; q < V; q += 2) {
+                            const float xh0 = (xx[q] - mu) * rs, xh1 = (xx[q + 1] - mu) * rs;
+                            const float g0 = __fmul_rn(gm[v][q], d[q]);
+                            const float g1 = __fmul_rn(gm[v][q + 1], d[q + 1]);
+                            sg0 += g0;
+                            sg1 += g1;
+                            sgx0 = fmaf(g0, xh0, sgx0);
+                            sgx1 = fmaf(g1, xh1, sgx1);
+                            accg[v][q] = fmaf(d[q], xh0, accg[v][q]);
+                            accg[v][q + 1] = fmaf(d[q + 1], xh1, accg[v][q + 1]);
                             accb[v][q] += d[q];
+                            accb[v][q + 1] += d[q + 1];
                         }
                     }
                 }
+                float sg = sg0 + sg1, sgx = sgx0 + sgx1;
                 warp_sum2(sg, sgx);  // the one reduction of the row: both sums together
+                // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
+                // g - mg cancels exactly where it should (a one-column row gives dx = 0).
                 const float mg = sg / fcols, mgx = sgx / fcols;
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
                     const int vi = v * 32 + lane;
                     if (vi < nvec) {  // second pass re-reads the row from shared memory
-                        float d[V], xx[V], gm[V], o[V];
+                        float d[V], xx[V], o[V];
                         IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
                         IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-                        IO::unpack(gv[v], gm);
 #pragma unroll
                         for (int q = 0; q < V; ++q) {
                             const float xh = (xx[q] - mu) * rs;
-                            o[q] = rs * (__fmul_rn(gm[q], d[q]) - (mg + xh * mgx));
+                            o[q] = rs * (__fmul_rn(gm[v][q], d[q]) - fmaf(xh, mgx, mg));
                         }
                         st_stream(dx + base + (size_t)vi * V, IO::pack(o));
                     }

@@ -39,6 +39,13 @@ struct Io<float> {
         return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                           __float_as_uint(f[3]));
     }
+    // Element-wise a + b of two vectors, rounded to the I/O type.
+    static __device__ __forceinline__ uint4 add_round(const uint4& a, const uint4& b) {
+        return make_uint4(__float_as_uint(__uint_as_float(a.x) + __uint_as_float(b.x)),
+                          __float_as_uint(__uint_as_float(a.y) + __uint_as_float(b.y)),
+                          __float_as_uint(__uint_as_float(a.z) + __uint_as_float(b.z)),
+                          __float_as_uint(__uint_as_float(a.w) + __uint_as_float(b.w)));
+    }
 };
 
 template <>
@@ -69,6 +76,21 @@ struct Io<__nv_bfloat16> {
         return make_uint4(pair_bits(f[0], f[1]), pair_bits(f[2], f[3]), pair_bits(f[4], f[5]),
                           pair_bits(f[6], f[7]));
     }
+    // Element-wise a + b of two vectors, rounded to bf16: one packed add.rn.bf16x2 per pair.
+    // The exact sum of two bf16 values is rounded once, which is the same number as the
+    // fp32 sum (exact for two bf16 operands) rounded to bf16.
+    static __device__ __forceinline__ uint32_t add2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 x, y;
+        memcpy(&x, &a, 4);
+        memcpy(&y, &b, 4);
+        const __nv_bfloat162 z = __hadd2(x, y);
+        uint32_t w;
+        memcpy(&w, &z, 4);
+        return w;
+    }
+    static __device__ __forceinline__ uint4 add_round(const uint4& a, const uint4& b) {
+        return make_uint4(add2(a.x, b.x), add2(a.y, b.y), add2(a.z, b.z), add2(a.w, b.w));
+    }
 };
 
 // ---------------------------------------------------------------------------------------
@@ -96,6 +118,20 @@ __device__ __forceinline__ void warp_sum2(float& a, float& b) {
         a += __shfl_xor_sync(kFullMask, a, o);
         b += __shfl_xor_sync(kFullMask, b, o);
     }
+}
+
+// The shift of a row for its shifted sums: the mean of the row's first vector (its first 4
+// fp32 or 8 bf16 stored values), rounded to the I/O type.  It lies within about a third of a
+// standard deviation of the row's mean, so sum d^2/n - (sum d/n)^2 with d = s - K loses
+// almost nothing to cancellation, and for bf16 every d is exact.
+template <typename T>
+__device__ __forceinline__ float row_shift(const uint4& first) {
+    float f[Io<T>::kVec];
+    Io<T>::unpack(first, f);
+    float k = 0.f;
+#pragma unroll
+    for (int i = 0; i < Io<T>::kVec; ++i) k += f[i];
+    return Io<T>::round(k * (1.0f / Io<T>::kVec));
 }
 
 // Row statistics as a mergeable summary: count n, the sum S + c of the shifted values (S and

@@ -7,14 +7,15 @@
 //
 // Statistics in one reduction, without the cancellation of E[s^2] - E[s]^2 that breaks rows
 // whose mean dwarfs their spread ("Accelerating Transformer on GPU (I)", section 4.2):
-//  * every row is shifted by K = its first stored element, d = s - K (exact for bf16 rows),
-//    so the centre is carried as K + mean(d) and never as one large rounded number;
-//  * each thread summarises its own values of d as (count, compensated sum, M2 about its
-//    own mean) and the summaries are combined with the Welford/Chan pairwise merge (same
-//    section) in one xor butterfly -- one reduction; M2 is a sum of non-negative terms, so
-//    nothing cancels, and the compensated sum keeps mean(d) accurate to about one rounding;
-//  * xhat = (d - mean(d)) * rstd, which never subtracts two large numbers either.
-// mean = K + mean(d) and rstd = 1 / sqrt(M2 / n + eps) are stored in fp32.
+//  * vector kernels: shifted sums.  K = the mean of the row's first 16-byte vector, rounded
+//    to the I/O type, so d = s - K is exact for bf16 and K lies within about a third of a
+//    standard deviation of the mean; sum d and sum d^2 are reduced together (one xor
+//    butterfly, plus one cross-warp exchange for a block per row) and
+//    var = sum d^2 / n - (sum d / n)^2 then has both terms of the order of var itself;
+//  * scalar kernel: each thread keeps a Welford summary (count, compensated sum, M2) and the
+//    summaries are combined with the Welford/Chan pairwise merge of the same section;
+//  * xhat = (d - mean(d)) * rstd, which never subtracts two large numbers.
+// mean = K + mean(d) and rstd = 1 / sqrt(var + eps) are stored in fp32.
 //
 // Three kernel families compute the same function:
 //  * warp per row (rows of at most 256 vectors of 16 bytes): tiles of 7 rows are staged in
@@ -127,39 +128,45 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
             const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
                                                      (size_t)warp * row_bytes);
             const T* rsm = xs + (size_t)kTileRows * cols;
-            // s = x + res, rounded to the stored type; it is what gets normalised.
-            float s[VPL][V];
+            // s = x + res, rounded to the stored type (one packed add per pair for bf16);
+            // it is what gets normalised.
+            uint4 sp[VPL];
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 const int vi = v * 32 + lane;
                 if (vi < nvec) {
-                    IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), s[v]);
-                    if (HAS_RES) {
-                        float r[V];
-                        IO::unpack(*reinterpret_cast<const uint4*>(rsm + (size_t)vi * V), r);
-#pragma unroll
-                        for (int q = 0; q < V; ++q) s[v][q] = IO::round(s[v][q] + r[q]);
-                    }
-                    if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
+                    const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
+                    sp[v] = HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
+                                    : xv;
+                    if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
                 } else {
-#pragma unroll
-                    for (int q = 0; q < V; ++q) s[v][q] = 0.f;
+                    sp[v] = make_uint4(0, 0, 0, 0);
                 }
             }
-            // Shift: the row's first stored element (lane 0 always holds it).
-            const float K = __shfl_sync(kFullMask, s[0][0], 0);
-            float dv[VPL * V];
-            int cnt = 0;
+            // Shifted sums: K = the mean of the row's first vector (lane 0's), rounded.
+            const float K = __shfl_sync(kFullMask, row_shift<T>(sp[0]), 0);
+            float s[VPL][V];
+            float a0 = 0.f, a1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
+                IO::unpack(sp[v], s[v]);
+                if (v * 32 + lane < nvec) {
 #pragma unroll
-                for (int q = 0; q < V; ++q) dv[v * V + q] = s[v][q] - K;
-                if (v * 32 + lane < nvec) cnt += V;
+                    for (int q = 0; q < V; q += 2) {
+                        const float d0 = s[v][q] - K, d1 = s[v][q + 1] - K;
+                        a0 += d0;
+                        a1 += d1;
+                        q0 = fmaf(d0, d0, q0);
+                        q1 = fmaf(d1, d1, q1);
+                    }
+                }
             }
-            RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
-            warp_stats(st);                        // the one reduction of the row
-            const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
-            const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+            float sd = a0 + a1, sd2 = q0 + q1;
+            warp_sum2(sd, sd2);  // the one reduction of the row
+            const float md = sd / fcols;
+            const float var = fmaxf(sd2 / fcols - md * md, 0.f);
+            const float rs = 1.0f / sqrtf(var + eps);
+            const float nmr = -md * rs;
             if (lane == 0) {
                 mean[row] = K + md;
                 rstd[row] = rs;
@@ -172,7 +179,8 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     IO::unpack(gv[v], g);
                     IO::unpack(bv[v], b);
 #pragma unroll
-                    for (int q = 0; q < V; ++q) o[q] = g[q] * ((s[v][q] - K - md) * rs) + b[q];
+                    for (int q = 0; q < V; ++q)
+                        o[q] = fmaf(g[q], fmaf(s[v][q] - K, rs, nmr), b[q]);
                     st_stream(out + base + (size_t)vi * V, IO::pack(o));
                 }
             }
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages];
-    __shared__ float red[4][32];
+    __shared__ float red[2][32];
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -252,47 +260,59 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
 
-        float s[VPT][V];
+        uint4 sp[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
-                IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), s[v]);
-                if (HAS_RES) {
-                    float r[V];
-                    IO::unpack(*reinterpret_cast<const uint4*>(rsm + (size_t)vi * V), r);
-#pragma unroll
-                    for (int q = 0; q < V; ++q) s[v][q] = IO::round(s[v][q] + r[q]);
-                }
-                if (write_res) st_stream(res_out + base + (size_t)vi * V, IO::pack(s[v]));
+                const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
+                sp[v] = HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
+                                : xv;
+                if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
             } else {
-#pragma unroll
-                for (int q = 0; q < V; ++q) s[v][q] = 0.f;
+                sp[v] = make_uint4(0, 0, 0, 0);
             }
         }
-        // Shift K: the row's first stored element, read by every thread from shared memory.
-        const float K = HAS_RES ? IO::round(IO::to_f(xs[0]) + IO::to_f(rsm[0])) : IO::to_f(xs[0]);
-        float dv[VPT * V];
-        int cnt = 0;
+        // Shifted sums: K = the mean of the row's first vector (every thread reads it from
+        // shared memory and computes the same bits).
+        const uint4 first = HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
+                                                   *reinterpret_cast<const uint4*>(rsm))
+                                    : *reinterpret_cast<const uint4*>(xs);
+        const float K = row_shift<T>(first);
+        float s[VPT][V];
+        float a0 = 0.f, a1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
+            IO::unpack(sp[v], s[v]);
+            if (v * nthreads + tid < nvec) {
 #pragma unroll
-            for (int q = 0; q < V; ++q) dv[v * V + q] = s[v][q] - K;
-            if (v * nthreads + tid < nvec) cnt += V;
+                for (int q = 0; q < V; q += 2) {
+                    const float d0 = s[v][q] - K, d1 = s[v][q + 1] - K;
+                    a0 += d0;
+                    a1 += d1;
+                    q0 = fmaf(d0, d0, q0);
+                    q1 = fmaf(d1, d1, q1);
+                }
+            }
         }
-        RowStats st = thread_stats(dv, cnt);  // valid vectors come first in dv
-        warp_stats(st);
+        float sd = a0 + a1, sd2 = q0 + q1;
+        warp_sum2(sd, sd2);
         if (lane == 0) {
-            red[0][warp] = st.n;
-            red[1][warp] = st.s;
-            red[2][warp] = st.c;
-            red[3][warp] = st.q;
+            red[0][warp] = sd;
+            red[1][warp] = sd2;
         }
         __syncthreads();  // the one cross-warp exchange of the row
         if (abort_flag) break;
-        st = block_stats(red, nw);  // the same bits in every thread
-        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
-        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+        sd = 0.f;
+        sd2 = 0.f;
+        for (int w = 0; w < nw; ++w) {  // same order in every thread: same bits everywhere
+            sd += red[0][w];
+            sd2 += red[1][w];
+        }
+        const float md = sd / fcols;
+        const float var = fmaxf(sd2 / fcols - md * md, 0.f);
+        const float rs = 1.0f / sqrtf(var + eps);
+        const float nmr = -md * rs;
         if (tid == 0) {
             mean[row] = K + md;
             rstd[row] = rs;
@@ -305,7 +325,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                 IO::unpack(gv[v], g);
                 IO::unpack(bv[v], b);
 #pragma unroll
-                for (int q = 0; q < V; ++q) o[q] = g[q] * ((s[v][q] - K - md) * rs) + b[q];
+                for (int q = 0; q < V; ++q) o[q] = fmaf(g[q], fmaf(s[v][q] - K, rs, nmr), b[q]);
                 st_stream(out + base + (size_t)vi * V, IO::pack(o));
             }
         }
