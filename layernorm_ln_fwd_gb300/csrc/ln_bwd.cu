@@ -71,7 +71,8 @@ struct KParams {
     unsigned* status;
     uint64_t limit_ns;
     unsigned wait_extra;
-    int finishers;
+    int unit;   // columns per finishing unit: 4, 2 or 1
+    int group;  // lanes per finishing unit: a power of two up to 32
     int stages;
 };
 
@@ -88,6 +89,14 @@ __device__ __forceinline__ void comp_add(float& S, float& C, float h, float l) {
     C += e + l;
 }
 
+// Kahan step on fp32 pairs: the running value is s - c.
+__device__ __forceinline__ void kahan2(f2& s, f2& c, f2 x) {
+    const f2 y = f2_sub(x, c);
+    const f2 t = f2_add(s, y);
+    c = f2_sub(f2_sub(t, s), y);
+    s = t;
+}
+
 // Kahan step: the running value is s - c.
 __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
     const float y = __fsub_rn(x, c);
@@ -97,102 +106,91 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Stage 2: the finishers.  Finisher f of F owns the column groups [g0, g1) (a group is U
-// adjacent columns).  Threads are arranged as Q subsets of the blocks times the (stat,
-// group) units of the slice; thread (q, u) adds the (hi, lo) partials of blocks q, q+Q,
-// q+2Q, ... in increasing order, then the Q subtotals of each unit are added in q order.
-// `scratch` is shared memory of at least blockDim.x * 4 floats.
+// Stage 2: every block finishes a slice.  A unit is U adjacent columns of one statistic;
+// block f of P owns units [f * n / P, (f + 1) * n / P).  A unit is summed by a group of G
+// lanes (G a power of two, 32 / G units per warp at a time): lane g of the group adds the
+// (hi, lo) partials of blocks g, g + G, g + 2G, ... in increasing order, the loads of a batch
+// of 16 / U of them issued before the first addition so that the L2 latency is paid once per
+// batch; then the group's lane totals are folded into its lane 0 by a fixed shuffle tree.
+// Every step is a compensated (TwoSum) addition, and the order depends only on P, G and the
+// unit.
 // ---------------------------------------------------------------------------------------
 template <typename T, int U>
-__device__ void finish_slice(const KParams& a, int P, int F, int f, float* scratch) {
+__device__ void finish_units(const KParams& a, int P, int f) {
     using IO = Io<T>;
+    constexpr int L = 16 / U;  // partial rows one lane loads per batch: 32 registers of data
     const int cols = a.cols;
-    const int threads = blockDim.x;
     const int ngroups = cols / U;
-    const int g0 = (int)((long long)f * ngroups / F);
-    const int g1 = (int)((long long)(f + 1) * ngroups / F);
-    const int wg = g1 - g0;
-    const int units = 2 * wg;
-    if (units == 0) return;
-    T* dst[2] = {static_cast<T*>(a.dgamma), static_cast<T*>(a.dbeta)};
+    const int nunits = 2 * ngroups;
+    const int u0 = (int)((long long)f * nunits / P);
+    const int u1 = (int)((long long)(f + 1) * nunits / P);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int G = a.group, per_warp = 32 / G;
+    const int gl = lane & (G - 1);
     const size_t stat_stride = (size_t)P * cols;
-    const int tid = threadIdx.x;
-
-    auto add_group = [&](float (&S)[U], float (&C)[U], const float2* src) {
-        if constexpr (U == 2) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-            comp_add(S[0], C[0], v.x, v.y);
-            comp_add(S[1], C[1], v.z, v.w);
-        } else {
-            const float2 v = __ldcg(src);
-            comp_add(S[0], C[0], v.x, v.y);
-        }
-    };
-    auto store = [&](int u, const float (&S)[U], const float (&C)[U]) {
-        const int stat = u / wg, grp = g0 + u % wg;
-#pragma unroll
-        for (int i = 0; i < U; ++i) dst[stat][(size_t)grp * U + i] = IO::from_f(S[i] + C[i]);
-    };
-
-    if (units >= threads) {
-        for (int u = tid; u < units; u += threads) {
-            const int stat = u / wg, grp = g0 + u % wg;
-            const float2* src = a.part + stat * stat_stride + (size_t)grp * U;
-            float S[U], C[U];
-#pragma unroll
-            for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-#pragma unroll 8
-            for (int p = 0; p < P; ++p) add_group(S, C, src + (size_t)p * cols);
-            store(u, S, C);
-        }
-        return;
-    }
-    const int Q = threads / units;
-    const int q = tid / units, u = tid % units;
-    if (q < Q) {
-        const int stat = u / wg, grp = g0 + u % wg;
+    for (int ub = u0 + warp * per_warp; ub < u1; ub += nwarps * per_warp) {  // warp-uniform
+        const int u = ub + lane / G;
+        const bool active = u < u1;
+        const int stat = u >= ngroups ? 1 : 0, grp = u - stat * ngroups;
         const float2* src = a.part + stat * stat_stride + (size_t)grp * U;
         float S[U], C[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-#pragma unroll 8
-        for (int p = q; p < P; p += Q) add_group(S, C, src + (size_t)p * cols);
-        float* sc = scratch + ((size_t)q * units + u) * (2 * U);
+        for (int p0 = 0; p0 < P; p0 += G * L) {
+            float2 v[L][U];
 #pragma unroll
-        for (int i = 0; i < U; ++i) {
-            sc[2 * i] = S[i];
-            sc[2 * i + 1] = C[i];
+            for (int j = 0; j < L; ++j) {
+                const int p = p0 + j * G + gl;
+                const bool ok = active && p < P;
+                const float2* q = src + (size_t)p * cols;
+                if constexpr (U == 1) {
+                    v[j][0] = ok ? __ldcg(q) : make_float2(0.f, 0.f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < U; i += 2) {
+                        const float4 w = ok ? __ldcg(reinterpret_cast<const float4*>(q + i))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[j][i] = make_float2(w.x, w.y);
+                        v[j][i + 1] = make_float2(w.z, w.w);
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < L; ++j)
+#pragma unroll
+                for (int i = 0; i < U; ++i) comp_add(S[i], C[i], v[j][i].x, v[j][i].y);
         }
-    }
-    __syncthreads();
-    for (int v = tid; v < units; v += threads) {
-        float S[U], C[U];
+        // Fold the group into its lane 0: at offset o, lane g < o takes lane g + o, which is
+        // in the same group.
+        for (int o = G >> 1; o > 0; o >>= 1) {
 #pragma unroll
-        for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-        for (int qq = 0; qq < Q; ++qq) {
-            const float* sc = scratch + ((size_t)qq * units + v) * (2 * U);
-#pragma unroll
-            for (int i = 0; i < U; ++i) comp_add(S[i], C[i], sc[2 * i], sc[2 * i + 1]);
+            for (int i = 0; i < U; ++i) {
+                const float s2 = __shfl_down_sync(kFullMask, S[i], o);
+                const float c2 = __shfl_down_sync(kFullMask, C[i], o);
+                comp_add(S[i], C[i], s2, c2);
+            }
         }
-        store(v, S, C);
+        if (gl == 0 && active) {
+            T* dst = static_cast<T*>(stat == 0 ? a.dgamma : a.dbeta) + (size_t)grp * U;
+#pragma unroll
+            for (int i = 0; i < U; ++i) dst[i] = IO::from_f(S[i] + C[i]);
+        }
     }
 }
 
-// Called by every thread of every block after its partial row is written.
+// Called by every thread of every block once the block's partial row is written.  One
+// thread per block publishes the row (block barrier, then a GPU-scope fence and the
+// counter increment) and waits, bounded, until all P blocks have done the same; then the
+// block finishes its slice.  The block that is last past the wait puts the counters back
+// to 0 for the next call.
 template <typename T>
-__device__ void arrive_and_finish(const KParams& a, float* scratch) {
-    __shared__ unsigned s_ticket;
+__device__ void arrive_and_finish(const KParams& a) {
     __shared__ int s_ok;
-    __threadfence();  // this thread's partial sums are visible GPU-wide before the ticket
-    __syncthreads();
     const unsigned P = gridDim.x;
-    const unsigned F = (unsigned)a.finishers;
-    if (threadIdx.x == 0) s_ticket = atomicAdd(&a.ctr[0], 1u);
-    __syncthreads();
-    const unsigned ticket = s_ticket;
-    if (ticket < P - F) return;  // not among the last F arrivals: done
-    const int f = (int)(ticket - (P - F));
+    __syncthreads();  // every thread's partial sums are written
     if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(&a.ctr[0], 1u);
         const bool ok = wait_counter_geq(&a.ctr[0], P + a.wait_extra, a.limit_ns);
         __threadfence();
         s_ok = ok ? 1 : 0;
@@ -200,14 +198,15 @@ __device__ void arrive_and_finish(const KParams& a, float* scratch) {
     }
     __syncthreads();
     if (!s_ok) return;
-    if (a.cols % 2 == 0)
-        finish_slice<T, 2>(a, (int)P, (int)F, f, scratch);
+    if (a.unit == 4)
+        finish_units<T, 4>(a, (int)P, (int)blockIdx.x);
+    else if (a.unit == 2)
+        finish_units<T, 2>(a, (int)P, (int)blockIdx.x);
     else
-        finish_slice<T, 1>(a, (int)P, (int)F, f, scratch);
-    __syncthreads();
+        finish_units<T, 1>(a, (int)P, (int)blockIdx.x);
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(&a.ctr[1], 1u);
-        if (done == F - 1) {  // every finisher is past its wait: reset for the next call
+        if (done == P - 1) {  // every block is past its wait: reset for the next call
             atomicExch(&a.ctr[0], 0u);
             atomicExch(&a.ctr[1], 0u);
         }
@@ -219,12 +218,21 @@ __device__ void arrive_and_finish(const KParams& a, float* scratch) {
 // The block owns a fixed contiguous range of tiles (7 consecutive rows each); the producer
 // warp's lane 0 fetches each tile of dy and of x with one cp.async.bulk apiece, `stages`
 // tiles ahead; consumer warp w handles row w of every tile.  Lane l owns the columns of
-// vectors l, l+32, ... in every row, so its column sums stay in registers; at the end the
-// 7 consumer warps' sums are added in warp order with TwoSum through shared memory (the
-// drained ring), one statistic at a time, into the block's (hi, lo) partial row.
+// vectors l, l+32, ... in every row, so its column sums stay in registers (Kahan-compensated
+// when KAHAN, for fp32 I/O and for long chains of rows); at the end the 7 consumer warps'
+// sums are added in warp order with TwoSum through shared memory (the drained ring) into
+// the block's (hi, lo) partial row.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPL>
-__global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kernel(const KParams a) {
+// Two blocks per SM when the per-lane state (gamma, column sums and their compensations,
+// in fp32 pairs) leaves room: at most 128 registers per thread.
+template <typename T, int VPL, bool KAHAN>
+constexpr int tile_min_blocks() {
+    return (KAHAN ? 5 : 3) * VPL * Pairs<T>::kPairs <= 36 ? 2 : 1;
+}
+
+template <typename T, int VPL, bool KAHAN>
+__global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>())
+    bwd_tile_kernel(const KParams a) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -252,11 +260,19 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
     }
     __syncthreads();
 
-    float accg[VPL][V], accb[VPL][V];
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    constexpr int KV = KAHAN ? VPL : 1;
+    f2 accg[VPL][H], accb[VPL][H];  // this lane's column sums of dy * xhat and dy
+    f2 cmpg[KV][H], cmpb[KV][H];    // their Kahan compensations (the value is s - c)
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
 #pragma unroll
-        for (int k = 0; k < V; ++k) accg[v][k] = accb[v][k] = 0.f;
+        for (int h = 0; h < H; ++h) accg[v][h] = accb[v][h] = f2_splat(0.f);
+#pragma unroll
+    for (int v = 0; v < KV; ++v)
+#pragma unroll
+        for (int h = 0; h < H; ++h) cmpg[v][h] = cmpb[v][h] = f2_splat(0.f);
 
     if (warp == kTileRows) {  // producer
         if (lane == 0) {
@@ -279,11 +295,11 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
                 (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
         }
     } else {  // consumers
-        float gm[VPL][V];  // gamma of this lane's columns, unpacked once
+        f2 gm[VPL][H];  // gamma of this lane's columns as fp32 pairs, loaded once
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
             const int vi = v * 32 + lane;
-            IO::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
+            PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
         }
         // mean and rstd of the warp's row in the next tile are loaded one tile ahead, so
         // their latency is not on the row's critical path.
@@ -307,48 +323,51 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
                 const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
                                                           (size_t)warp * row_bytes);
                 const T* xs = dys + (size_t)kTileRows * cols;
-                float sg0 = 0.f, sg1 = 0.f, sgx0 = 0.f, sgx1 = 0.f;
+                const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
+                // Row sums; the low halves take the even columns, the high halves the odd.
+                f2 sg = f2_splat(0.f), sgx = f2_splat(0.f);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
                     const int vi = v * 32 + lane;
                     if (vi < nvec) {
-                        float d[V], xx[V];
-                        IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                        IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        f2 d[H], xx[H];
+                        PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                        PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
 #pragma unroll
-                        for (int q = 0; q < V; q += 2) {
-                            const float xh0 = (xx[q] - mu) * rs, xh1 = (xx[q + 1] - mu) * rs;
-                            const float g0 = __fmul_rn(gm[v][q], d[q]);
-                            const float g1 = __fmul_rn(gm[v][q + 1], d[q + 1]);
-                            sg0 += g0;
-                            sg1 += g1;
-                            sgx0 = fmaf(g0, xh0, sgx0);
-                            sgx1 = fmaf(g1, xh1, sgx1);
-                            accg[v][q] = fmaf(d[q], xh0, accg[v][q]);
-                            accg[v][q + 1] = fmaf(d[q + 1], xh1, accg[v][q + 1]);
-                            accb[v][q] += d[q];
-                            accb[v][q + 1] += d[q + 1];
+                        for (int h = 0; h < H; ++h) {
+                            const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                            const f2 g = f2_mul(gm[v][h], d[h]);
+                            sg = f2_add(sg, g);
+                            sgx = f2_fma(g, xh, sgx);
+                            if constexpr (KAHAN) {
+                                kahan2(accg[v][h], cmpg[v][h], f2_mul(d[h], xh));
+                                kahan2(accb[v][h], cmpb[v][h], d[h]);
+                            } else {
+                                accg[v][h] = f2_fma(d[h], xh, accg[v][h]);
+                                accb[v][h] = f2_add(accb[v][h], d[h]);
+                            }
                         }
                     }
                 }
-                float sg = sg0 + sg1, sgx = sgx0 + sgx1;
-                warp_sum2(sg, sgx);  // the one reduction of the row: both sums together
+                float tg = f2_lo(sg) + f2_hi(sg), tgx = f2_lo(sgx) + f2_hi(sgx);
+                warp_sum2(tg, tgx);  // the one reduction of the row: both sums together
                 // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
                 // g - mg cancels exactly where it should (a one-column row gives dx = 0).
-                const float mg = sg / fcols, mgx = sgx / fcols;
+                const f2 mg2 = f2_splat(tg / fcols), mgx2 = f2_splat(tgx / fcols);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
                     const int vi = v * 32 + lane;
                     if (vi < nvec) {  // second pass re-reads the row from shared memory
-                        float d[V], xx[V], o[V];
-                        IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                        IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        f2 d[H], xx[H], o[H];
+                        PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                        PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
 #pragma unroll
-                        for (int q = 0; q < V; ++q) {
-                            const float xh = (xx[q] - mu) * rs;
-                            o[q] = rs * (__fmul_rn(gm[v][q], d[q]) - fmaf(xh, mgx, mg));
+                        for (int h = 0; h < H; ++h) {
+                            const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                            const f2 g = f2_mul(gm[v][h], d[h]);
+                            o[h] = f2_mul(rs2, f2_sub(g, f2_fma(xh, mgx2, mg2)));
                         }
-                        st_stream(dx + base + (size_t)vi * V, IO::pack(o));
+                        st_stream(dx + base + (size_t)vi * V, PR::pack(o));
                     }
                 }
             }
@@ -358,37 +377,55 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 3 ? 2 : 1) bwd_tile_kerne
     }
     __syncthreads();  // the ring is drained and no warp reads it any more
 
-    // Block partial row: add the consumer warps' sums in warp order (TwoSum), one statistic
-    // at a time, and store the (hi, lo) pair.
-    float* smem_f = reinterpret_cast<float*>(smem_raw);  // [kTileRows][cols]
-    const int P = gridDim.x;
+    // Block partial row.  The consumer warps put their sums in shared memory as
+    // [stat][warp][cols] floats (the drained ring), followed by the negated compensations in
+    // the same layout when KAHAN; then each thread adds the 7 warps' values of a pair of
+    // columns in warp order with TwoSum and stores the (hi, lo) pairs of both.
+    float* smem_f = reinterpret_cast<float*>(smem_raw);
+    const size_t lo_off = (size_t)2 * kTileRows * cols;
+    auto put = [&](float* dst, f2 a0, f2 a1) {
+        *reinterpret_cast<float4*>(dst) = make_float4(f2_lo(a0), f2_hi(a0), f2_lo(a1), f2_hi(a1));
+    };
+    if (warp < kTileRows) {
 #pragma unroll
-    for (int stat = 0; stat < 2; ++stat) {
-        if (warp < kTileRows) {
+        for (int v = 0; v < VPL; ++v) {
+            const int vi = v * 32 + lane;
+            if (vi < nvec) {
+                float* dg = smem_f + (size_t)warp * cols + (size_t)vi * V;
+                float* db = dg + (size_t)kTileRows * cols;
 #pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
-                if (vi < nvec) {
-                    float* dst = smem_f + (size_t)warp * cols + (size_t)vi * V;
-#pragma unroll
-                    for (int k = 0; k < V; k += 4)
-                        *reinterpret_cast<float4*>(dst + k) =
-                            stat == 0 ? make_float4(accg[v][k], accg[v][k + 1], accg[v][k + 2], accg[v][k + 3])
-                                      : make_float4(accb[v][k], accb[v][k + 1], accb[v][k + 2], accb[v][k + 3]);
+                for (int h = 0; h < H; h += 2) {
+                    put(dg + 2 * h, accg[v][h], accg[v][h + 1]);
+                    put(db + 2 * h, accb[v][h], accb[v][h + 1]);
+                    if constexpr (KAHAN) {
+                        const f2 z = f2_splat(0.f);
+                        put(dg + lo_off + 2 * h, f2_sub(z, cmpg[v][h]), f2_sub(z, cmpg[v][h + 1]));
+                        put(db + lo_off + 2 * h, f2_sub(z, cmpb[v][h]), f2_sub(z, cmpb[v][h + 1]));
+                    }
                 }
             }
         }
-        __syncthreads();
-        float2* prow = a.part + ((size_t)stat * P + blockIdx.x) * cols;
-        for (int c = tid; c < cols; c += blockDim.x) {
-            float S = 0.f, C = 0.f;
-#pragma unroll
-            for (int w = 0; w < kTileRows; ++w) comp_add(S, C, smem_f[(size_t)w * cols + c], 0.f);
-            prow[c] = make_float2(S, C);
-        }
-        __syncthreads();
     }
-    arrive_and_finish<T>(a, smem_f);
+    __syncthreads();
+    const int P = gridDim.x;
+    const int half = cols >> 1;  // column pairs per statistic (cols is a multiple of 4)
+    for (int u = tid; u < 2 * half; u += blockDim.x) {
+        const int stat = u >= half ? 1 : 0;
+        const int c = 2 * (u - stat * half);
+        const float* src = smem_f + (size_t)stat * kTileRows * cols + c;
+        float S0 = 0.f, C0 = 0.f, S1 = 0.f, C1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTileRows; ++w) {
+            const float2 t = *reinterpret_cast<const float2*>(src + (size_t)w * cols);
+            float2 l = make_float2(0.f, 0.f);
+            if constexpr (KAHAN) l = *reinterpret_cast<const float2*>(src + lo_off + (size_t)w * cols);
+            comp_add(S0, C0, t.x, l.x);
+            comp_add(S1, C1, t.y, l.y);
+        }
+        *reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c) =
+            make_float4(S0, C0, S1, C1);
+    }
+    arrive_and_finish<T>(a);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -437,20 +474,23 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     if (tid == 0)
         for (int k = 0; k < stages; ++k) issue(k);
 
-    uint4 gv[VPT];
-    float sg_hi[VPT][V], sb_hi[VPT][V];  // running sums of dy * xhat and dy
-    float sg_c[KAHAN ? VPT : 1][V], sb_c[KAHAN ? VPT : 1][V];  // Kahan compensations
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    constexpr int KV = KAHAN ? VPT : 1;
+    f2 gp[VPT][H];            // gamma of this thread's columns as fp32 pairs
+    f2 sg[VPT][H], sb[VPT][H];  // running column sums of dy * xhat and dy
+    f2 cg[KV][H], cb[KV][H];    // their Kahan compensations (the value is s - c)
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int vi = v * nthreads + tid;
-        gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+        PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
 #pragma unroll
-        for (int k = 0; k < V; ++k) sg_hi[v][k] = sb_hi[v][k] = 0.f;
+        for (int h = 0; h < H; ++h) sg[v][h] = sb[v][h] = f2_splat(0.f);
     }
 #pragma unroll
-    for (int v = 0; v < (KAHAN ? VPT : 1); ++v)
+    for (int v = 0; v < KV; ++v)
 #pragma unroll
-        for (int k = 0; k < V; ++k) sg_c[v][k] = sb_c[v][k] = 0.f;
+        for (int h = 0; h < H; ++h) cg[v][h] = cb[v][h] = f2_splat(0.f);
 
     int k = 0;
     // mean and rstd are loaded one row ahead (off the row's critical path).
@@ -466,58 +506,60 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
-        float sg = 0.f, sgx = 0.f;
+        const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
+        f2 rg = f2_splat(0.f), rgx = f2_splat(0.f);  // row sums: even columns low, odd high
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
-                float d[V], xx[V], gm[V];
-                IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-                IO::unpack(gv[v], gm);
+                f2 d[H], xx[H];
+                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
 #pragma unroll
-                for (int q = 0; q < V; ++q) {
-                    const float xh = (xx[q] - mu) * rs;
-                    const float g = __fmul_rn(gm[q], d[q]);
-                    sg += g;
-                    sgx += g * xh;
+                for (int h = 0; h < H; ++h) {
+                    const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                    const f2 g = f2_mul(gp[v][h], d[h]);
+                    rg = f2_add(rg, g);
+                    rgx = f2_fma(g, xh, rgx);
                     if constexpr (KAHAN) {
-                        kahan_add(sg_hi[v][q], sg_c[v][q], __fmul_rn(d[q], xh));
-                        kahan_add(sb_hi[v][q], sb_c[v][q], d[q]);
+                        kahan2(sg[v][h], cg[v][h], f2_mul(d[h], xh));
+                        kahan2(sb[v][h], cb[v][h], d[h]);
                     } else {
-                        sg_hi[v][q] += d[q] * xh;
-                        sb_hi[v][q] += d[q];
+                        sg[v][h] = f2_fma(d[h], xh, sg[v][h]);
+                        sb[v][h] = f2_add(sb[v][h], d[h]);
                     }
                 }
             }
         }
-        warp_sum2(sg, sgx);
+        float tg = f2_lo(rg) + f2_hi(rg), tgx = f2_lo(rgx) + f2_hi(rgx);
+        warp_sum2(tg, tgx);
         if (lane == 0) {
-            red[0][warp] = sg;
-            red[1][warp] = sgx;
+            red[0][warp] = tg;
+            red[1][warp] = tgx;
         }
         __syncthreads();  // the one cross-warp exchange of the row
         if (abort_flag) break;
-        float tg = 0.f, tgx = 0.f;
+        tg = 0.f;
+        tgx = 0.f;
         for (int w = 0; w < nw; ++w) {  // same order in every thread
             tg += red[0][w];
             tgx += red[1][w];
         }
-        const float mg = tg / fcols, mgx = tgx / fcols;
+        const f2 mg2 = f2_splat(tg / fcols), mgx2 = f2_splat(tgx / fcols);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
-                float d[V], xx[V], gm[V], o[V];
-                IO::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                IO::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-                IO::unpack(gv[v], gm);
+                f2 d[H], xx[H], o[H];
+                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
+                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
 #pragma unroll
-                for (int q = 0; q < V; ++q) {
-                    const float xh = (xx[q] - mu) * rs;
-                    o[q] = rs * (__fmul_rn(gm[q], d[q]) - (mg + xh * mgx));
+                for (int h = 0; h < H; ++h) {
+                    const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                    const f2 g = f2_mul(gp[v][h], d[h]);
+                    o[h] = f2_mul(rs2, f2_sub(g, f2_fma(xh, mgx2, mg2)));
                 }
-                st_stream(dx + base + (size_t)vi * V, IO::pack(o));
+                st_stream(dx + base + (size_t)vi * V, PR::pack(o));
             }
         }
         __syncthreads();  // slot and `red` free again
@@ -531,33 +573,34 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
                 (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
         }
         __syncthreads();
-        return;  // no partial row: the finishers' bounded wait runs out as well
+        return;  // no partial row: every other block's bounded wait runs out as well
     }
 
+    // Partial row: (hi, lo) for each column, two columns per 16-byte store.
     const int P = gridDim.x;
+    float2* pg = a.part + (size_t)blockIdx.x * cols;
+    float2* pb = a.part + ((size_t)P + blockIdx.x) * cols;
 #pragma unroll
-    for (int stat = 0; stat < 2; ++stat) {
-        float2* prow = a.part + ((size_t)stat * P + blockIdx.x) * cols;
+    for (int v = 0; v < VPT; ++v) {
+        const int vi = v * nthreads + tid;
+        if (vi < nvec) {
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int vi = v * nthreads + tid;
-            if (vi < nvec) {
-#pragma unroll
-                for (int q = 0; q < V; q += 2) {
-                    float h0, h1, l0 = 0.f, l1 = 0.f;
-                    h0 = stat == 0 ? sg_hi[v][q] : sb_hi[v][q];
-                    h1 = stat == 0 ? sg_hi[v][q + 1] : sb_hi[v][q + 1];
-                    if constexpr (KAHAN) {  // Kahan's value is s - c
-                        l0 = -(stat == 0 ? sg_c[v][q] : sb_c[v][q]);
-                        l1 = -(stat == 0 ? sg_c[v][q + 1] : sb_c[v][q + 1]);
-                    }
-                    *reinterpret_cast<float4*>(prow + (size_t)vi * V + q) =
-                        make_float4(h0, l0, h1, l1);
+            for (int h = 0; h < H; ++h) {
+                float lg0 = 0.f, lg1 = 0.f, lb0 = 0.f, lb1 = 0.f;
+                if constexpr (KAHAN) {
+                    lg0 = -f2_lo(cg[v][h]);
+                    lg1 = -f2_hi(cg[v][h]);
+                    lb0 = -f2_lo(cb[v][h]);
+                    lb1 = -f2_hi(cb[v][h]);
                 }
+                *reinterpret_cast<float4*>(pg + (size_t)vi * V + 2 * h) =
+                    make_float4(f2_lo(sg[v][h]), lg0, f2_hi(sg[v][h]), lg1);
+                *reinterpret_cast<float4*>(pb + (size_t)vi * V + 2 * h) =
+                    make_float4(f2_lo(sb[v][h]), lb0, f2_hi(sb[v][h]), lb1);
             }
         }
     }
-    arrive_and_finish<T>(a, reinterpret_cast<float*>(smem_raw));
+    arrive_and_finish<T>(a);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -631,63 +674,68 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
         a.part[(size_t)blockIdx.x * cols + j] = make_float2(pg.x, -pg.y);
         a.part[((size_t)P + blockIdx.x) * cols + j] = make_float2(pb.x, -pb.y);
     }
-    __syncthreads();  // the shared accumulators become the finish scratch
-    arrive_and_finish<T>(a, smem_f);
+    arrive_and_finish<T>(a);
 }
 
 // ---------------------------------------------------------------------------------------
 // Host side.
 // ---------------------------------------------------------------------------------------
-// Warp path: up to 8 vectors per lane for fp32 (1024 columns), 5 for bf16 (1280 columns):
-// beyond that the register-resident column sums no longer fit without spilling.
-template <typename T>
-const void* warp_kernel(int vpl) {
+// Warp path: up to 8 vectors per lane for fp32 (1024 columns), 5 for bf16 (1280 columns),
+// 4 for bf16 with compensated sums: beyond that the register-resident column sums no
+// longer fit without spilling.
+template <typename T, bool K>
+const void* warp_kernel_k(int vpl) {
+    switch (vpl) {
+        case 1: return (const void*)bwd_tile_kernel<T, 1, K>;
+        case 2: return (const void*)bwd_tile_kernel<T, 2, K>;
+        case 3: return (const void*)bwd_tile_kernel<T, 3, K>;
+        case 4: return (const void*)bwd_tile_kernel<T, 4, K>;
+        default: break;
+    }
     if constexpr (Io<T>::kVec == 8) {
-        switch (vpl) {
-            case 1: return (const void*)bwd_tile_kernel<T, 1>;
-            case 2: return (const void*)bwd_tile_kernel<T, 2>;
-            case 3: return (const void*)bwd_tile_kernel<T, 3>;
-            case 4: return (const void*)bwd_tile_kernel<T, 4>;
-            case 5: return (const void*)bwd_tile_kernel<T, 5>;
-            default: return nullptr;
-        }
+        if (vpl == 5 && !K) return (const void*)bwd_tile_kernel<T, 5, false>;
     } else {
         switch (vpl) {
-            case 1: return (const void*)bwd_tile_kernel<T, 1>;
-            case 2: return (const void*)bwd_tile_kernel<T, 2>;
-            case 3: return (const void*)bwd_tile_kernel<T, 3>;
-            case 4: return (const void*)bwd_tile_kernel<T, 4>;
-            case 5: return (const void*)bwd_tile_kernel<T, 5>;
-            case 6: return (const void*)bwd_tile_kernel<T, 6>;
-            case 7: return (const void*)bwd_tile_kernel<T, 7>;
-            case 8: return (const void*)bwd_tile_kernel<T, 8>;
-            default: return nullptr;
+            case 5: return (const void*)bwd_tile_kernel<T, 5, K>;
+            case 6: return (const void*)bwd_tile_kernel<T, 6, K>;
+            case 7: return (const void*)bwd_tile_kernel<T, 7, K>;
+            case 8: return (const void*)bwd_tile_kernel<T, 8, K>;
+            default: break;
         }
     }
+    return nullptr;
 }
 
-// Block path: cols <= 16384 and 512 threads give at most 4 vectors per thread for bf16 and
-// 8 for fp32.  Kahan compensation when a thread owns at most 16 columns.
 template <typename T>
-const void* block_kernel(int vpt) {
+const void* warp_kernel(int vpl, bool kahan) {
+    return kahan ? warp_kernel_k<T, true>(vpl) : warp_kernel_k<T, false>(vpl);
+}
+
+int warp_max_vpl(Dtype dt, bool kahan) { return dt == Dtype::F32 ? 8 : (kahan ? 4 : 5); }
+
+// Block path: cols <= 16384 and 512 threads give at most 4 vectors per thread for bf16 and
+// 8 for fp32.  Compensated (Kahan) column sums where the plan asks for them: the registers
+// are there for at most 16 columns per thread.
+template <typename T>
+const void* block_kernel(int vpt, bool kahan) {
     if constexpr (Io<T>::kVec == 8) {
         switch (vpt) {
-            case 1: return (const void*)bwd_block_kernel<T, 1, true>;
-            case 2: return (const void*)bwd_block_kernel<T, 2, true>;
-            case 3: return (const void*)bwd_block_kernel<T, 3, false>;
-            case 4: return (const void*)bwd_block_kernel<T, 4, false>;
+            case 1: return kahan ? (const void*)bwd_block_kernel<T, 1, true> : (const void*)bwd_block_kernel<T, 1, false>;
+            case 2: return kahan ? (const void*)bwd_block_kernel<T, 2, true> : (const void*)bwd_block_kernel<T, 2, false>;
+            case 3: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 3, false>;
+            case 4: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 4, false>;
             default: return nullptr;
         }
     } else {
         switch (vpt) {
-            case 1: return (const void*)bwd_block_kernel<T, 1, true>;
-            case 2: return (const void*)bwd_block_kernel<T, 2, true>;
-            case 3: return (const void*)bwd_block_kernel<T, 3, true>;
-            case 4: return (const void*)bwd_block_kernel<T, 4, true>;
-            case 5: return (const void*)bwd_block_kernel<T, 5, false>;
-            case 6: return (const void*)bwd_block_kernel<T, 6, false>;
-            case 7: return (const void*)bwd_block_kernel<T, 7, false>;
-            case 8: return (const void*)bwd_block_kernel<T, 8, false>;
+            case 1: return kahan ? (const void*)bwd_block_kernel<T, 1, true> : (const void*)bwd_block_kernel<T, 1, false>;
+            case 2: return kahan ? (const void*)bwd_block_kernel<T, 2, true> : (const void*)bwd_block_kernel<T, 2, false>;
+            case 3: return kahan ? (const void*)bwd_block_kernel<T, 3, true> : (const void*)bwd_block_kernel<T, 3, false>;
+            case 4: return kahan ? (const void*)bwd_block_kernel<T, 4, true> : (const void*)bwd_block_kernel<T, 4, false>;
+            case 5: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 5, false>;
+            case 6: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 6, false>;
+            case 7: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 7, false>;
+            case 8: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 8, false>;
             default: return nullptr;
         }
     }
@@ -695,22 +743,38 @@ const void* block_kernel(int vpt) {
 
 const void* kernel_for(Dtype dt, const BwdPlan& p) {
     const bool f = dt == Dtype::F32;
-    if (p.path == kPathWarp) return f ? warp_kernel<float>(p.per_thread) : warp_kernel<__nv_bfloat16>(p.per_thread);
-    if (p.path == kPathBlock) return f ? block_kernel<float>(p.per_thread) : block_kernel<__nv_bfloat16>(p.per_thread);
+    if (p.path == kPathWarp)
+        return f ? warp_kernel<float>(p.per_thread, p.kahan)
+                 : warp_kernel<__nv_bfloat16>(p.per_thread, p.kahan);
+    if (p.path == kPathBlock)
+        return f ? block_kernel<float>(p.per_thread, p.kahan)
+                 : block_kernel<__nv_bfloat16>(p.per_thread, p.kahan);
     return f ? (const void*)bwd_scalar_kernel<float> : (const void*)bwd_scalar_kernel<__nv_bfloat16>;
 }
 
-// Number of finishing blocks: enough that each finishing thread adds about 8 partial
-// vectors, and no more than there are blocks or column groups.
-int pick_finishers(int grid, int cols, int threads) {
-    const int U = cols % 2 == 0 ? 2 : 1;
-    const int ngroups = cols / U;
-    const int want_q = std::max(1, (grid + 7) / 8);
-    const int units_max = std::max(2, threads / want_q);
-    const int wg_max = std::max(1, units_max / 2);
-    int F = (ngroups + wg_max - 1) / wg_max;
-    F = std::max(1, std::min(F, std::min(grid, ngroups)));
-    return F;
+// Shape of the finish: columns per unit U and lanes per unit G.  A lane loads 16 / U partial
+// rows per batch; G is the smallest power of two whose batch covers all P partial rows (at
+// most 32); a warp then sums 32 / G units at a time.  Each pass of a warp over its units and
+// each batch costs an L2 round trip, so pick the U that needs the fewest, the narrower on a
+// tie.
+void pick_finish(int grid, int cols, int threads, int* unit, int* group) {
+    const long long warps_per_block = threads / 32;
+    long long best_rounds = -1;
+    for (int u : {1, 2, 4}) {
+        if (cols % u != 0) continue;
+        const int L = 16 / u;
+        int G = 1;
+        while (G < 32 && (long long)G * L < grid) G <<= 1;
+        const long long units_per_block = (2LL * (cols / u) + grid - 1) / grid;
+        const long long per_pass = warps_per_block * (32 / G);
+        const long long rounds = ((units_per_block + per_pass - 1) / per_pass) *
+                                 (((long long)grid + (long long)G * L - 1) / ((long long)G * L));
+        if (best_rounds < 0 || rounds < best_rounds) {
+            *unit = u;
+            *group = G;
+            best_rounds = rounds;
+        }
+    }
 }
 
 }  // namespace
@@ -726,21 +790,29 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
     if (aligned && path_override != kPathScalar) {
         const int nvec = cols / V;
         const int vpl = (nvec + 31) / 32;
-        const int warp_max = dt == Dtype::F32 ? 8 : 5;
-        const bool warp_fits = vpl <= warp_max;
-        const bool warp_auto = dt == Dtype::BF16 && rows <= kWarpPathMaxRows;
-        if (warp_fits && (path_override == kPathWarp ||
-                          (path_override == kPathAuto && warp_auto))) {
+        // The warp path keeps each lane's column sums over all the rows its warp handles:
+        // compensated for fp32 I/O, and for bf16 once those chains can get long.
+        const bool wk = dt == Dtype::F32 || rows > kWarpPathMaxRows;
+        const bool warp_fits = vpl <= warp_max_vpl(dt, wk);
+        if (warp_fits && (path_override == kPathWarp || path_override == kPathAuto)) {
             p.path = kPathWarp;
             p.per_thread = vpl;
             p.threads = kTileThreads;
+            p.kahan = wk;
             const size_t slot = 2ull * kTileRows * cols * esize;  // a tile of dy and of x
-            int stages = (int)std::min<size_t>(kMaxStages, ((size_t)di.smem_optin / 2) / slot);
+            const size_t combine = (wk ? 4ull : 2ull) * kTileRows * cols * 4;
+            // As many tiles in flight as the block's share of the SM's shared memory holds,
+            // at the number of blocks per SM the registers allow.
+            const void* kern = kernel_for(dt, p);
+            if (!kern) return cudaErrorInvalidValue;
+            const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
+            const size_t share = std::min<size_t>(
+                (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
+            int stages = (int)std::min<size_t>(kMaxStages, share / slot);
             stages = std::max(2, stages);
             p.stages = stages;
-            // The ring, reused afterwards for the warps' sums and the finish scratch.
-            p.smem = std::max<size_t>({(size_t)stages * slot, (size_t)kTileRows * cols * 4,
-                                       (size_t)kTileThreads * 16});
+            // The ring, reused afterwards for the warps' sums.
+            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)kTileThreads * 16});
         } else {
             p.path = kPathBlock;
             p.per_thread = (nvec + kBwdBlockMaxThreads - 1) / kBwdBlockMaxThreads;
@@ -752,6 +824,12 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
             stages = std::max(1, stages);
             p.smem = std::max<size_t>((size_t)stages * slot, (size_t)p.threads * 16);
             p.stages = stages;
+            // Compensated column sums: always for fp32 I/O (as far as the registers go); for
+            // bf16 only when a thread's chain of rows can be long (more than 64 rows per
+            // block even at one block per SM): over short chains an fp32 sum is far more
+            // accurate than the bf16 result it is rounded to.
+            p.kahan = dt == Dtype::F32 ? p.per_thread <= 4
+                                       : (p.per_thread <= 2 && rows > 64 * di.sms);
         }
     } else {
         p.path = kPathScalar;
@@ -771,7 +849,7 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int need = p.path == kPathWarp ? (rows + kTileRows - 1) / kTileRows : rows;
     p.grid = std::max(1, std::min(need, di.sms * occ));
-    p.finishers = pick_finishers(p.grid, cols, p.threads);
+    pick_finish(p.grid, cols, p.threads, &p.unit, &p.group);
     *plan = p;
     return cudaSuccess;
 }
@@ -797,7 +875,8 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.status = a.status;
     k.limit_ns = a.wait_limit_ns;
     k.wait_extra = a.wait_extra;
-    k.finishers = p.finishers;
+    k.unit = p.unit;
+    k.group = p.group;
     k.stages = p.stages;
     void* args[] = {&k};
     // A cooperative launch (all blocks co-resident, checked by the driver against the

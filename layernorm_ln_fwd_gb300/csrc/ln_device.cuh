@@ -94,6 +94,96 @@ struct Io<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------------------------------
+// Packed fp32 pairs.  sm_100-family SMs execute add, sub, mul and fma on two fp32 values
+// held in a 64-bit register pair as one instruction (PTX .f32x2).  Each half is an ordinary
+// IEEE fp32 operation rounded to nearest even, so a pair computes bit for bit what two
+// scalar __fadd_rn / __fmul_rn / fmaf calls would, in half the issue slots.  Nothing is
+// contracted across these calls: a product rounded by f2_mul stays rounded.
+// ---------------------------------------------------------------------------------------
+struct f2 {
+    unsigned long long v;
+};
+
+__device__ __forceinline__ f2 f2_make(float lo, float hi) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f2 f2_splat(float a) { return f2_make(a, a); }
+__device__ __forceinline__ float f2_lo(f2 a) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(f2 a) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return hi;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+    f2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+// a * b + c with one rounding per half.
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return d;
+}
+
+// A 16-byte vector as fp32 pairs: element 2h in the low half of pair h, 2h + 1 in the high.
+template <typename T>
+struct Pairs;
+
+template <>
+struct Pairs<float> {
+    static constexpr int kPairs = 2;
+    static __device__ __forceinline__ void unpack(const uint4& u, f2 (&p)[2]) {
+        p[0].v = (unsigned long long)u.x | ((unsigned long long)u.y << 32);
+        p[1].v = (unsigned long long)u.z | ((unsigned long long)u.w << 32);
+    }
+    static __device__ __forceinline__ uint4 pack(const f2 (&p)[2]) {
+        return make_uint4((uint32_t)p[0].v, (uint32_t)(p[0].v >> 32), (uint32_t)p[1].v,
+                          (uint32_t)(p[1].v >> 32));
+    }
+};
+
+template <>
+struct Pairs<__nv_bfloat16> {
+    static constexpr int kPairs = 4;
+    // A bf16 value is the upper half of the fp32 value it stands for.
+    static __device__ __forceinline__ f2 word(uint32_t w) {
+        return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    static __device__ __forceinline__ void unpack(const uint4& u, f2 (&p)[4]) {
+        p[0] = word(u.x);
+        p[1] = word(u.y);
+        p[2] = word(u.z);
+        p[3] = word(u.w);
+    }
+    // Both halves rounded to bf16 (nearest even) into one 32-bit word, low half first.
+    static __device__ __forceinline__ uint32_t bits(f2 a) {
+        uint32_t w;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(f2_hi(a)), "f"(f2_lo(a)));
+        return w;
+    }
+    static __device__ __forceinline__ uint4 pack(const f2 (&p)[4]) {
+        return make_uint4(bits(p[0]), bits(p[1]), bits(p[2]), bits(p[3]));
+    }
+};
+
+// ---------------------------------------------------------------------------------------
 // Global memory access with cache hints.  Streamed tensors are read and written once per
 // kernel: they use the evict-first ("cs") policy so they do not push gamma/beta or the
 // backward's partial sums out of L2.

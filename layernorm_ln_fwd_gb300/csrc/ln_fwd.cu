@@ -106,13 +106,15 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
         return;
     }
 
-    // Consumers: gamma and beta stay packed in registers for every row.
-    uint4 gv[VPL], bv[VPL];
+    // Consumers: gamma and beta of this lane's columns, as fp32 pairs, for every row.
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    f2 gp[VPL][H], bp[VPL][H];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
         const int vi = v * 32 + lane;
-        gv[v] = vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
-        bv[v] = vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0);
+        PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
+        PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
     const bool write_res = res_out != nullptr;
     for (int k = 0; k < my_tiles; ++k) {
@@ -143,45 +145,42 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     sp[v] = make_uint4(0, 0, 0, 0);
                 }
             }
-            // Shifted sums: K = the mean of the row's first vector (lane 0's), rounded.
-            const float K = __shfl_sync(kFullMask, row_shift<T>(sp[0]), 0);
-            float s[VPL][V];
-            float a0 = 0.f, a1 = 0.f, q0 = 0.f, q1 = 0.f;
+            // Shifted sums: K = the mean of the row's first vector (lane 0's), rounded.  The
+            // low halves of the pairs sum the even columns, the high halves the odd ones.
+            const f2 K2 = f2_splat(__shfl_sync(kFullMask, row_shift<T>(sp[0]), 0));
+            f2 d[VPL][H];
+            f2 a = f2_splat(0.f), q = f2_splat(0.f);
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
-                IO::unpack(sp[v], s[v]);
+                PR::unpack(sp[v], d[v]);
                 if (v * 32 + lane < nvec) {
 #pragma unroll
-                    for (int q = 0; q < V; q += 2) {
-                        const float d0 = s[v][q] - K, d1 = s[v][q + 1] - K;
-                        a0 += d0;
-                        a1 += d1;
-                        q0 = fmaf(d0, d0, q0);
-                        q1 = fmaf(d1, d1, q1);
+                    for (int h = 0; h < H; ++h) {
+                        d[v][h] = f2_sub(d[v][h], K2);
+                        a = f2_add(a, d[v][h]);
+                        q = f2_fma(d[v][h], d[v][h], q);
                     }
                 }
             }
-            float sd = a0 + a1, sd2 = q0 + q1;
+            float sd = f2_lo(a) + f2_hi(a), sd2 = f2_lo(q) + f2_hi(q);
             warp_sum2(sd, sd2);  // the one reduction of the row
             const float md = sd / fcols;
             const float var = fmaxf(sd2 / fcols - md * md, 0.f);
             const float rs = 1.0f / sqrtf(var + eps);
-            const float nmr = -md * rs;
             if (lane == 0) {
-                mean[row] = K + md;
+                mean[row] = f2_lo(K2) + md;
                 rstd[row] = rs;
             }
+            // out = gamma * ((s - K) * rs - md * rs) + beta
+            const f2 rs2 = f2_splat(rs), nmr2 = f2_splat(-md * rs);
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 const int vi = v * 32 + lane;
                 if (vi < nvec) {
-                    float g[V], b[V], o[V];
-                    IO::unpack(gv[v], g);
-                    IO::unpack(bv[v], b);
+                    f2 o[H];
 #pragma unroll
-                    for (int q = 0; q < V; ++q)
-                        o[q] = fmaf(g[q], fmaf(s[v][q] - K, rs, nmr), b[q]);
-                    st_stream(out + base + (size_t)vi * V, IO::pack(o));
+                    for (int h = 0; h < H; ++h) o[h] = f2_fma(gp[v][h], f2_fma(d[v][h], rs2, nmr2), bp[v][h]);
+                    st_stream(out + base + (size_t)vi * V, PR::pack(o));
                 }
             }
         }
@@ -239,15 +238,15 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     if (tid == 0)
         for (int k = 0; k < stages; ++k) issue(k);
 
-    // gamma, beta for this thread's vectors (the same columns in every row).
-    uint4 gv[VPT], bv[VPT];
+    // gamma, beta for this thread's vectors (the same columns in every row), as fp32 pairs.
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    f2 gp[VPT][H], bp[VPT][H];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int vi = v * nthreads + tid;
-        if (vi < nvec) {
-            gv[v] = ld_keep(gamma + (size_t)vi * V);
-            bv[v] = ld_keep(beta + (size_t)vi * V);
-        }
+        PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
+        PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
 
     const bool write_res = res_out != nullptr;
@@ -274,28 +273,27 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
             }
         }
         // Shifted sums: K = the mean of the row's first vector (every thread reads it from
-        // shared memory and computes the same bits).
+        // shared memory and computes the same bits).  The low halves of the pairs sum the
+        // even columns, the high halves the odd ones.
         const uint4 first = HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
                                                    *reinterpret_cast<const uint4*>(rsm))
                                     : *reinterpret_cast<const uint4*>(xs);
-        const float K = row_shift<T>(first);
-        float s[VPT][V];
-        float a0 = 0.f, a1 = 0.f, q0 = 0.f, q1 = 0.f;
+        const f2 K2 = f2_splat(row_shift<T>(first));
+        f2 d[VPT][H];
+        f2 a2 = f2_splat(0.f), q2 = f2_splat(0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
-            IO::unpack(sp[v], s[v]);
+            PR::unpack(sp[v], d[v]);
             if (v * nthreads + tid < nvec) {
 #pragma unroll
-                for (int q = 0; q < V; q += 2) {
-                    const float d0 = s[v][q] - K, d1 = s[v][q + 1] - K;
-                    a0 += d0;
-                    a1 += d1;
-                    q0 = fmaf(d0, d0, q0);
-                    q1 = fmaf(d1, d1, q1);
+                for (int h = 0; h < H; ++h) {
+                    d[v][h] = f2_sub(d[v][h], K2);
+                    a2 = f2_add(a2, d[v][h]);
+                    q2 = f2_fma(d[v][h], d[v][h], q2);
                 }
             }
         }
-        float sd = a0 + a1, sd2 = q0 + q1;
+        float sd = f2_lo(a2) + f2_hi(a2), sd2 = f2_lo(q2) + f2_hi(q2);
         warp_sum2(sd, sd2);
         if (lane == 0) {
             red[0][warp] = sd;
@@ -312,21 +310,20 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         const float md = sd / fcols;
         const float var = fmaxf(sd2 / fcols - md * md, 0.f);
         const float rs = 1.0f / sqrtf(var + eps);
-        const float nmr = -md * rs;
         if (tid == 0) {
-            mean[row] = K + md;
+            mean[row] = f2_lo(K2) + md;
             rstd[row] = rs;
         }
+        // out = gamma * ((s - K) * rs - md * rs) + beta
+        const f2 rs2 = f2_splat(rs), nmr2 = f2_splat(-md * rs);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
-                float g[V], b[V], o[V];
-                IO::unpack(gv[v], g);
-                IO::unpack(bv[v], b);
+                f2 o[H];
 #pragma unroll
-                for (int q = 0; q < V; ++q) o[q] = fmaf(g[q], fmaf(s[v][q] - K, rs, nmr), b[q]);
-                st_stream(out + base + (size_t)vi * V, IO::pack(o));
+                for (int h = 0; h < H; ++h) o[h] = f2_fma(gp[v][h], f2_fma(d[v][h], rs2, nmr2), bp[v][h]);
+                st_stream(out + base + (size_t)vi * V, PR::pack(o));
             }
         }
         __syncthreads();  // the slot and `red` are free again

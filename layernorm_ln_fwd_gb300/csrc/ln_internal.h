@@ -54,7 +54,7 @@ struct BwdArgs {
     int rows;
     int cols;
     float* partials;      // [2][grid][cols] (hi, lo) fp32 pairs: dgamma, then dbeta
-    unsigned* counters;   // [2]: arrivals, finished finishers
+    unsigned* counters;   // [2]: blocks arrived, blocks finished
     unsigned* status;
     uint64_t wait_limit_ns;
     unsigned wait_extra;  // test hook: wait for this many more arrivals than exist
@@ -66,7 +66,9 @@ struct BwdPlan {
     int per_thread = 0;   // vectors per lane (warp path) or per thread (block path)
     int threads = 0;
     int grid = 0;
-    int finishers = 0;
+    int unit = 0;         // columns per finishing unit (4, 2 or 1)
+    int group = 32;       // lanes per finishing unit (a power of two up to 32)
+    bool kahan = false;   // compensated per-thread column sums (block path)
     int stages = 0;       // rows in flight per block (block path); accumulator place (scalar)
     size_t smem = 0;
 };
