@@ -50,7 +50,8 @@ constexpr int kTileRows = 7;
 constexpr int kTileThreads = (kTileRows + 1) * 32;
 constexpr int kBwdBlockMaxThreads = 512;
 constexpr int kBwdScalarThreads = 256;
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
+constexpr int kBlockStages = 4;
 // The warp kernel is used for bf16 rows of up to 5 vectors per lane (1280 columns) and at
 // most this many rows, which keeps its plain per-lane chains short.
 constexpr int kWarpPathMaxRows = 65536;
@@ -66,13 +67,12 @@ struct KParams {
     void* dbeta;
     int rows;
     int cols;
-    float2* part;  // [2][gridDim.x][cols] (hi, lo) pairs
+    float2* part;  // [2][gridDim.x][cols] (hi, lo) pairs, or plain fp32 sums when compact
+    int compact;   // partials without the lo half (kernels whose column sums are plain)
     unsigned* ctr;
     unsigned* status;
     uint64_t limit_ns;
     unsigned wait_extra;
-    int unit;   // columns per finishing unit: 4, 2 or 1
-    int group;  // lanes per finishing unit: a power of two up to 32
     int stages;
 };
 
@@ -106,71 +106,98 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Stage 2: every block finishes a slice.  A unit is U adjacent columns of one statistic;
-// block f of P owns units [f * n / P, (f + 1) * n / P).  A unit is summed by a group of G
-// lanes (G a power of two, 32 / G units per warp at a time): lane g of the group adds the
-// (hi, lo) partials of blocks g, g + G, g + 2G, ... in increasing order, the loads of a batch
-// of 16 / U of them issued before the first addition so that the L2 latency is paid once per
-// batch; then the group's lane totals are folded into its lane 0 by a fixed shuffle tree.
-// Every step is a compensated (TwoSum) addition, and the order depends only on P, G and the
-// unit.
+// Stage 2: every block finishes a slice.  A unit is U adjacent columns of one statistic; a
+// partial is a (hi, lo) pair per column, or one plain fp32 sum when COMPACT, and U is chosen
+// so that one unit of one partial row is a single 16-byte load where the row length allows.
+// Block f of P owns units [f * n / P, (f + 1) * n / P).  The block's threads form an R x nk
+// grid over (subset of the partial rows, unit), the unit index varying fastest so that a
+// load instruction of a warp reads adjacent partials.  Thread (r, k) adds the partials of
+// blocks r, r + R, r + 2R, ... in increasing order, the loads of a batch (up to 32 / W rows)
+// issued before the first addition so that the L2 latency is paid once per batch; R is the
+// smallest power of two that needs one batch, where the block has the threads for it; then
+// the R subtotals of each
+// unit are folded by a fixed binary tree in shared memory.  Every step is a compensated
+// (TwoSum) addition, and the order depends only on P, the block size and the unit.
+// `scratch` holds at least 2 * U floats per thread.
 // ---------------------------------------------------------------------------------------
-template <typename T, int U>
-__device__ void finish_units(const KParams& a, int P, int f) {
+template <typename T, int U, bool COMPACT>
+__device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     using IO = Io<T>;
-    constexpr int L = 16 / U;  // partial rows one lane loads per batch: 32 registers of data
+    constexpr int E = COMPACT ? 1 : 2;  // floats per column of a partial
+    constexpr int W = E * U;            // floats per unit of a partial row: 1, 2 or 4
+    constexpr int L = 32 / W;           // partial rows one thread loads per batch (32 registers)
     const int cols = a.cols;
     const int ngroups = cols / U;
     const int nunits = 2 * ngroups;
     const int u0 = (int)((long long)f * nunits / P);
     const int u1 = (int)((long long)(f + 1) * nunits / P);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int G = a.group, per_warp = 32 / G;
-    const int gl = lane & (G - 1);
-    const size_t stat_stride = (size_t)P * cols;
-    for (int ub = u0 + warp * per_warp; ub < u1; ub += nwarps * per_warp) {  // warp-uniform
-        const int u = ub + lane / G;
-        const bool active = u < u1;
+    const int nt = blockDim.x, t = threadIdx.x;
+    const float* part = reinterpret_cast<const float*>(a.part);
+    const size_t stat_stride = (size_t)P * cols * E;
+    const size_t row_stride = (size_t)cols * E;
+    for (int kb = u0; kb < u1; kb += nt) {
+        const int nk = min(nt, u1 - kb);
+        // R: the smallest power of two for which one batch covers all P partial rows (the
+        // shallowest tree), or as many as the block has threads for.
+        int R = 1;
+        while (2 * R * nk <= nt && R * L < P) R <<= 1;
+        const int r = t / nk, k = t - r * nk;
+        const bool act = r < R;
+        const int u = kb + k;
         const int stat = u >= ngroups ? 1 : 0, grp = u - stat * ngroups;
-        const float2* src = a.part + stat * stat_stride + (size_t)grp * U;
         float S[U], C[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-        for (int p0 = 0; p0 < P; p0 += G * L) {
-            float2 v[L][U];
+        if (act) {
+            const float* src = part + stat * stat_stride + (size_t)grp * W;
+            for (int p0 = r; p0 < P; p0 += R * L) {
+                float v[L][W];
 #pragma unroll
-            for (int j = 0; j < L; ++j) {
-                const int p = p0 + j * G + gl;
-                const bool ok = active && p < P;
-                const float2* q = src + (size_t)p * cols;
-                if constexpr (U == 1) {
-                    v[j][0] = ok ? __ldcg(q) : make_float2(0.f, 0.f);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < U; i += 2) {
-                        const float4 w = ok ? __ldcg(reinterpret_cast<const float4*>(q + i))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[j][i] = make_float2(w.x, w.y);
-                        v[j][i + 1] = make_float2(w.z, w.w);
+                for (int j = 0; j < L; ++j) {
+                    const int p = p0 + j * R;
+                    const float* q = src + (size_t)p * row_stride;
+                    if constexpr (W == 4) {
+                        const float4 w = p < P ? __ldcg(reinterpret_cast<const float4*>(q))
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[j][0] = w.x; v[j][1] = w.y; v[j][2] = w.z; v[j][3] = w.w;
+                    } else if constexpr (W == 2) {
+                        const float2 w = p < P ? __ldcg(reinterpret_cast<const float2*>(q))
+                                               : make_float2(0.f, 0.f);
+                        v[j][0] = w.x; v[j][1] = w.y;
+                    } else {
+                        v[j][0] = p < P ? __ldcg(q) : 0.f;
                     }
                 }
+#pragma unroll
+                for (int j = 0; j < L; ++j)
+#pragma unroll
+                    for (int i = 0; i < U; ++i)
+                        comp_add(S[i], C[i], v[j][E * i], E == 2 ? v[j][E * i + E - 1] : 0.f);
             }
-#pragma unroll
-            for (int j = 0; j < L; ++j)
-#pragma unroll
-                for (int i = 0; i < U; ++i) comp_add(S[i], C[i], v[j][i].x, v[j][i].y);
         }
-        // Fold the group into its lane 0: at offset o, lane g < o takes lane g + o, which is
-        // in the same group.
-        for (int o = G >> 1; o > 0; o >>= 1) {
+        // Tree over r: at step s, subtotal r < s takes in subtotal r + s.
+        float* mine = scratch + (size_t)t * 2 * U;
+        if (act) {
 #pragma unroll
             for (int i = 0; i < U; ++i) {
-                const float s2 = __shfl_down_sync(kFullMask, S[i], o);
-                const float c2 = __shfl_down_sync(kFullMask, C[i], o);
-                comp_add(S[i], C[i], s2, c2);
+                mine[2 * i] = S[i];
+                mine[2 * i + 1] = C[i];
             }
         }
-        if (gl == 0 && active) {
+        __syncthreads();
+        for (int st = R >> 1; st > 0; st >>= 1) {
+            if (r < st) {
+                const float* other = scratch + (size_t)(t + st * nk) * 2 * U;
+#pragma unroll
+                for (int i = 0; i < U; ++i) {
+                    comp_add(S[i], C[i], other[2 * i], other[2 * i + 1]);
+                    mine[2 * i] = S[i];
+                    mine[2 * i + 1] = C[i];
+                }
+            }
+            __syncthreads();
+        }
+        if (r == 0) {
             T* dst = static_cast<T*>(stat == 0 ? a.dgamma : a.dbeta) + (size_t)grp * U;
 #pragma unroll
             for (int i = 0; i < U; ++i) dst[i] = IO::from_f(S[i] + C[i]);
@@ -178,13 +205,8 @@ __device__ void finish_units(const KParams& a, int P, int f) {
     }
 }
 
-// Called by every thread of every block once the block's partial row is written.  One
-// thread per block publishes the row (block barrier, then a GPU-scope fence and the
-// counter increment) and waits, bounded, until all P blocks have done the same; then the
-// block finishes its slice.  The block that is last past the wait puts the counters back
-// to 0 for the next call.
 template <typename T>
-__device__ void arrive_and_finish(const KParams& a) {
+__device__ void arrive_and_finish(const KParams& a, float* scratch) {
     __shared__ int s_ok;
     const unsigned P = gridDim.x;
     __syncthreads();  // every thread's partial sums are written
@@ -198,12 +220,19 @@ __device__ void arrive_and_finish(const KParams& a) {
     }
     __syncthreads();
     if (!s_ok) return;
-    if (a.unit == 4)
-        finish_units<T, 4>(a, (int)P, (int)blockIdx.x);
-    else if (a.unit == 2)
-        finish_units<T, 2>(a, (int)P, (int)blockIdx.x);
-    else
-        finish_units<T, 1>(a, (int)P, (int)blockIdx.x);
+    if (a.compact) {
+        if (a.cols % 4 == 0)
+            finish_units<T, 4, true>(a, (int)P, (int)blockIdx.x, scratch);
+        else if (a.cols % 2 == 0)
+            finish_units<T, 2, true>(a, (int)P, (int)blockIdx.x, scratch);
+        else
+            finish_units<T, 1, true>(a, (int)P, (int)blockIdx.x, scratch);
+    } else {
+        if (a.cols % 2 == 0)
+            finish_units<T, 2, false>(a, (int)P, (int)blockIdx.x, scratch);
+        else
+            finish_units<T, 1, false>(a, (int)P, (int)blockIdx.x, scratch);
+    }
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(&a.ctr[1], 1u);
         if (done == P - 1) {  // every block is past its wait: reset for the next call
@@ -380,7 +409,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     // Block partial row.  The consumer warps put their sums in shared memory as
     // [stat][warp][cols] floats (the drained ring), followed by the negated compensations in
     // the same layout when KAHAN; then each thread adds the 7 warps' values of a pair of
-    // columns in warp order with TwoSum and stores the (hi, lo) pairs of both.
+    // columns in warp order (with TwoSum when KAHAN) and stores the (hi, lo) pairs of both.
     float* smem_f = reinterpret_cast<float*>(smem_raw);
     const size_t lo_off = (size_t)2 * kTileRows * cols;
     auto put = [&](float* dst, f2 a0, f2 a1) {
@@ -417,15 +446,23 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
         for (int w = 0; w < kTileRows; ++w) {
             const float2 t = *reinterpret_cast<const float2*>(src + (size_t)w * cols);
-            float2 l = make_float2(0.f, 0.f);
-            if constexpr (KAHAN) l = *reinterpret_cast<const float2*>(src + lo_off + (size_t)w * cols);
-            comp_add(S0, C0, t.x, l.x);
-            comp_add(S1, C1, t.y, l.y);
+            if constexpr (KAHAN) {
+                const float2 l = *reinterpret_cast<const float2*>(src + lo_off + (size_t)w * cols);
+                comp_add(S0, C0, t.x, l.x);
+                comp_add(S1, C1, t.y, l.y);
+            } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
+                S0 += t.x;
+                S1 += t.y;
+            }
         }
-        *reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c) =
-            make_float4(S0, C0, S1, C1);
+        if constexpr (KAHAN)
+            *reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c) =
+                make_float4(S0, C0, S1, C1);
+        else
+            *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.part) +
+                                       ((size_t)stat * P + blockIdx.x) * cols + c) = make_float2(S0, S1);
     }
-    arrive_and_finish<T>(a);
+    arrive_and_finish<T>(a, smem_f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -576,31 +613,37 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         return;  // no partial row: every other block's bounded wait runs out as well
     }
 
-    // Partial row: (hi, lo) for each column, two columns per 16-byte store.
+    // Partial row: (hi, lo) for each column, two columns per 16-byte store; plain sums four
+    // columns per 16-byte store when the sums are not compensated.
     const int P = gridDim.x;
-    float2* pg = a.part + (size_t)blockIdx.x * cols;
-    float2* pb = a.part + ((size_t)P + blockIdx.x) * cols;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int vi = v * nthreads + tid;
         if (vi < nvec) {
+            if constexpr (KAHAN) {
+                float2* pg = a.part + (size_t)blockIdx.x * cols + (size_t)vi * V;
+                float2* pb = a.part + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
 #pragma unroll
-            for (int h = 0; h < H; ++h) {
-                float lg0 = 0.f, lg1 = 0.f, lb0 = 0.f, lb1 = 0.f;
-                if constexpr (KAHAN) {
-                    lg0 = -f2_lo(cg[v][h]);
-                    lg1 = -f2_hi(cg[v][h]);
-                    lb0 = -f2_lo(cb[v][h]);
-                    lb1 = -f2_hi(cb[v][h]);
+                for (int h = 0; h < H; ++h) {
+                    *reinterpret_cast<float4*>(pg + 2 * h) =
+                        make_float4(f2_lo(sg[v][h]), -f2_lo(cg[v][h]), f2_hi(sg[v][h]), -f2_hi(cg[v][h]));
+                    *reinterpret_cast<float4*>(pb + 2 * h) =
+                        make_float4(f2_lo(sb[v][h]), -f2_lo(cb[v][h]), f2_hi(sb[v][h]), -f2_hi(cb[v][h]));
                 }
-                *reinterpret_cast<float4*>(pg + (size_t)vi * V + 2 * h) =
-                    make_float4(f2_lo(sg[v][h]), lg0, f2_hi(sg[v][h]), lg1);
-                *reinterpret_cast<float4*>(pb + (size_t)vi * V + 2 * h) =
-                    make_float4(f2_lo(sb[v][h]), lb0, f2_hi(sb[v][h]), lb1);
+            } else {
+                float* pg = reinterpret_cast<float*>(a.part) + (size_t)blockIdx.x * cols + (size_t)vi * V;
+                float* pb = reinterpret_cast<float*>(a.part) + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
+#pragma unroll
+                for (int h = 0; h < H; h += 2) {
+                    *reinterpret_cast<float4*>(pg + 2 * h) =
+                        make_float4(f2_lo(sg[v][h]), f2_hi(sg[v][h]), f2_lo(sg[v][h + 1]), f2_hi(sg[v][h + 1]));
+                    *reinterpret_cast<float4*>(pb + 2 * h) =
+                        make_float4(f2_lo(sb[v][h]), f2_hi(sb[v][h]), f2_lo(sb[v][h + 1]), f2_hi(sb[v][h + 1]));
+                }
             }
         }
     }
-    arrive_and_finish<T>(a);
+    arrive_and_finish<T>(a, reinterpret_cast<float*>(smem_raw));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -674,7 +717,8 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
         a.part[(size_t)blockIdx.x * cols + j] = make_float2(pg.x, -pg.y);
         a.part[((size_t)P + blockIdx.x) * cols + j] = make_float2(pb.x, -pb.y);
     }
-    arrive_and_finish<T>(a);
+    __syncthreads();  // the shared accumulators become the finish scratch
+    arrive_and_finish<T>(a, smem_f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -752,31 +796,6 @@ const void* kernel_for(Dtype dt, const BwdPlan& p) {
     return f ? (const void*)bwd_scalar_kernel<float> : (const void*)bwd_scalar_kernel<__nv_bfloat16>;
 }
 
-// Shape of the finish: columns per unit U and lanes per unit G.  A lane loads 16 / U partial
-// rows per batch; G is the smallest power of two whose batch covers all P partial rows (at
-// most 32); a warp then sums 32 / G units at a time.  Each pass of a warp over its units and
-// each batch costs an L2 round trip, so pick the U that needs the fewest, the narrower on a
-// tie.
-void pick_finish(int grid, int cols, int threads, int* unit, int* group) {
-    const long long warps_per_block = threads / 32;
-    long long best_rounds = -1;
-    for (int u : {1, 2, 4}) {
-        if (cols % u != 0) continue;
-        const int L = 16 / u;
-        int G = 1;
-        while (G < 32 && (long long)G * L < grid) G <<= 1;
-        const long long units_per_block = (2LL * (cols / u) + grid - 1) / grid;
-        const long long per_pass = warps_per_block * (32 / G);
-        const long long rounds = ((units_per_block + per_pass - 1) / per_pass) *
-                                 (((long long)grid + (long long)G * L - 1) / ((long long)G * L));
-        if (best_rounds < 0 || rounds < best_rounds) {
-            *unit = u;
-            *group = G;
-            best_rounds = rounds;
-        }
-    }
-}
-
 }  // namespace
 
 int bwd_max_grid(int rows, int sms) { return std::max(1, std::min(rows, sms * 8)); }
@@ -812,26 +831,32 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
             stages = std::max(2, stages);
             p.stages = stages;
             // The ring, reused afterwards for the warps' sums.
-            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)kTileThreads * 16});
+            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)kTileThreads * 32});
         } else {
             p.path = kPathBlock;
             p.per_thread = (nvec + kBwdBlockMaxThreads - 1) / kBwdBlockMaxThreads;
             const int t = (nvec + p.per_thread - 1) / p.per_thread;
             p.threads = std::max(32, (t + 31) / 32 * 32);
-            const size_t slot = 2ull * cols * esize;
-            const size_t budget = std::max<size_t>(slot, (size_t)di.smem_optin / 2);
-            int stages = (int)std::min<size_t>(kMaxStages, budget / slot);
-            stages = std::max(1, stages);
-            p.smem = std::max<size_t>((size_t)stages * slot, (size_t)p.threads * 16);
-            p.stages = stages;
             // Compensated column sums: always for fp32 I/O (as far as the registers go); for
             // bf16 only when a thread's chain of rows can be long (more than 64 rows per
             // block even at one block per SM): over short chains an fp32 sum is far more
             // accurate than the bf16 result it is rounded to.
             p.kahan = dt == Dtype::F32 ? p.per_thread <= 4
                                        : (p.per_thread <= 2 && rows > 64 * di.sms);
+            const size_t slot = 2ull * cols * esize;  // a row of dy and of x
+            const void* kern = kernel_for(dt, p);
+            if (!kern) return cudaErrorInvalidValue;
+            const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
+            const size_t share = std::min<size_t>(
+                (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
+            // Rows in flight: up to 4, within the block's share of shared memory (measured on
+            // GB300, deeper prefetch only delays every block's first row).
+            const int stages = (int)std::min<size_t>(kBlockStages, share / slot);
+            p.stages = std::max(1, stages);
+            p.smem = std::max<size_t>((size_t)p.stages * slot, (size_t)p.threads * 32);
         }
-    } else {
+    }
+    if (p.path == kPathAuto) {
         p.path = kPathScalar;
         p.threads = kBwdScalarThreads;
         const size_t acc = 16ull * cols;  // (hi, lo) pairs for both statistics
@@ -849,7 +874,6 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int need = p.path == kPathWarp ? (rows + kTileRows - 1) / kTileRows : rows;
     p.grid = std::max(1, std::min(need, di.sms * occ));
-    pick_finish(p.grid, cols, p.threads, &p.unit, &p.group);
     *plan = p;
     return cudaSuccess;
 }
@@ -871,12 +895,11 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.rows = a.rows;
     k.cols = a.cols;
     k.part = reinterpret_cast<float2*>(a.partials);
+    k.compact = (p.path == kPathScalar || p.kahan) ? 0 : 1;
     k.ctr = a.counters;
     k.status = a.status;
     k.limit_ns = a.wait_limit_ns;
     k.wait_extra = a.wait_extra;
-    k.unit = p.unit;
-    k.group = p.group;
     k.stages = p.stages;
     void* args[] = {&k};
     // A cooperative launch (all blocks co-resident, checked by the driver against the

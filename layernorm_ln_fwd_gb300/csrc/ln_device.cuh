@@ -337,12 +337,10 @@ __device__ __forceinline__ bool wait_counter_geq(const unsigned* ctr, unsigned t
                                                  uint64_t limit_ns) {
     if (ld_acquire_u32(ctr) >= target) return true;
     const uint64_t t0 = global_ns();
-    unsigned sleep_ns = 32;
     while (true) {
-        __nanosleep(sleep_ns);
+        __nanosleep(64);
         if (ld_acquire_u32(ctr) >= target) return true;
         if (global_ns() - t0 > limit_ns) return false;
-        if (sleep_ns < 512) sleep_ns <<= 1;
     }
 }
 
@@ -384,24 +382,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+// Test the phase with the given parity; a thread whose phase is not complete yet is
+// suspended in hardware until it completes or about `hint_ns` have passed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity, unsigned hint_ns) {
     unsigned ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
+// Bounded wait for the phase with the given parity to complete.  The suspend hint keeps a
+// waiting warp off the issue slots; the time limit is checked between suspensions.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    constexpr unsigned kHintNs = 100000;
+    if (mbar_try_wait(bar, parity, kHintNs)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, kHintNs)) return true;
         if (global_ns() - t0 > limit_ns) return false;
     }
 }

@@ -66,8 +66,6 @@ struct BwdPlan {
     int per_thread = 0;   // vectors per lane (warp path) or per thread (block path)
     int threads = 0;
     int grid = 0;
-    int unit = 0;         // columns per finishing unit (4, 2 or 1)
-    int group = 32;       // lanes per finishing unit (a power of two up to 32)
     bool kahan = false;   // compensated per-thread column sums (block path)
     int stages = 0;       // rows in flight per block (block path); accumulator place (scalar)
     size_t smem = 0;
