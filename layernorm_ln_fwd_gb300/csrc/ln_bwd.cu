@@ -69,6 +69,7 @@ struct KParams {
     int cols;
     float2* part;  // [2][gridDim.x][cols] (hi, lo) pairs, or plain fp32 sums when compact
     int compact;   // partials without the lo half (kernels whose column sums are plain)
+    int fin_rw;    // warps per unit group in the finish (divides the block's warp count)
     unsigned* ctr;
     unsigned* status;
     uint64_t limit_ns;
@@ -106,78 +107,103 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 }
 
 // ---------------------------------------------------------------------------------------
-// Stage 2: every block finishes a slice.  A unit is U adjacent columns of one statistic; a
-// partial is a (hi, lo) pair per column, or one plain fp32 sum when COMPACT, and U is chosen
-// so that one unit of one partial row is a single 16-byte load where the row length allows.
-// Block f of P owns units [f * n / P, (f + 1) * n / P).  The block's threads form an R x nk
-// grid over (subset of the partial rows, unit), the unit index varying fastest so that a
-// load instruction of a warp reads adjacent partials.  Thread (r, k) adds the partials of
-// blocks r, r + R, r + 2R, ... in increasing order, the loads of a batch (up to 32 / W rows)
-// issued before the first addition so that the L2 latency is paid once per batch; R is the
-// smallest power of two that needs one batch, where the block has the threads for it; then
-// the R subtotals of each
-// unit are folded by a fixed binary tree in shared memory.  Every step is a compensated
-// (TwoSum) addition, and the order depends only on P, the block size and the unit.
+// Stage 2: the finish.  A unit is U adjacent columns of one statistic; a partial is a
+// (hi, lo) pair per column, or one plain fp32 sum when COMPACT, and U is chosen so that one
+// unit of one partial row is a single 16-byte load where the row length allows.  Units are
+// taken in groups of kFinUnits adjacent ones (128 contiguous bytes of a partial row); block f
+// of P owns groups [f * g / P, (f + 1) * g / P).  The block's warps work on GW groups at a
+// time, RW warps per group (RW * GW = the warp count, RW chosen by the host so that a lane's
+// rows fit in one batch).  Warp r of a group's RW takes the contiguous range of partial rows
+// [r * P / RW, (r + 1) * P / RW); lane (s, k), s < kFinSub, k < kFinUnits, adds unit k of
+// rows s, s + kFinSub, ... of that range in increasing order (the loads of a batch issued
+// before the first addition, so the L2 latency is paid once per batch, and a warp's load
+// touches kFinSub lines); the kFinSub lane totals are folded by a fixed shuffle tree, and
+// the RW warp totals are added in warp order through shared memory.  The order depends
+// only on P, RW and the unit.
+// Compensated partials are added with TwoSum; COMPACT partials (plain fp32 sums from
+// kernels with bf16 results) with plain fp32 additions: their error, about 2^-24 * sqrt(P)
+// times the partials' size, is far below a bf16 unit in the last place.
 // `scratch` holds at least 2 * U floats per thread.
 // ---------------------------------------------------------------------------------------
+constexpr int kFinUnits = 8;
+constexpr int kFinSub = 32 / kFinUnits;
+constexpr int kFinBatch = 48;  // floats of partials a lane loads per batch
+
 template <typename T, int U, bool COMPACT>
 __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     using IO = Io<T>;
     constexpr int E = COMPACT ? 1 : 2;  // floats per column of a partial
     constexpr int W = E * U;            // floats per unit of a partial row: 1, 2 or 4
-    constexpr int L = 32 / W;           // partial rows one thread loads per batch (32 registers)
+    constexpr int L = kFinBatch / W;    // partial rows one lane loads per batch
     const int cols = a.cols;
-    const int ngroups = cols / U;
+    const int ngroups = cols / U;       // units per statistic
     const int nunits = 2 * ngroups;
-    const int u0 = (int)((long long)f * nunits / P);
-    const int u1 = (int)((long long)(f + 1) * nunits / P);
-    const int nt = blockDim.x, t = threadIdx.x;
+    const int ng = (nunits + kFinUnits - 1) / kFinUnits;
+    const int g0 = (int)((long long)f * ng / P);
+    const int g1 = (int)((long long)(f + 1) * ng / P);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int RW = a.fin_rw, GW = nw / RW;
+    const int gw = warp / RW, rw = warp - gw * RW;
+    const int k = lane % kFinUnits, sub = lane / kFinUnits;
+    const int p_lo = (int)((long long)rw * P / RW), p_hi = (int)((long long)(rw + 1) * P / RW);
     const float* part = reinterpret_cast<const float*>(a.part);
     const size_t stat_stride = (size_t)P * cols * E;
     const size_t row_stride = (size_t)cols * E;
-    for (int kb = u0; kb < u1; kb += nt) {
-        const int nk = min(nt, u1 - kb);
-        // R: the smallest power of two for which one batch covers all P partial rows (the
-        // shallowest tree), or as many as the block has threads for.
-        int R = 1;
-        while (2 * R * nk <= nt && R * L < P) R <<= 1;
-        const int r = t / nk, k = t - r * nk;
-        const bool act = r < R;
-        const int u = kb + k;
+    for (int gb = g0; gb < g1; gb += GW) {  // block-uniform
+        const int gi = gb + gw;
+        const int u = gi * kFinUnits + k;
+        const bool act = gi < g1 && u < nunits;
         const int stat = u >= ngroups ? 1 : 0, grp = u - stat * ngroups;
         float S[U], C[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
         if (act) {
             const float* src = part + stat * stat_stride + (size_t)grp * W;
-            for (int p0 = r; p0 < P; p0 += R * L) {
+            for (int p0 = p_lo + sub; p0 < p_hi; p0 += kFinSub * L) {
                 float v[L][W];
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
-                    const int p = p0 + j * R;
+                    const int p = p0 + j * kFinSub;
                     const float* q = src + (size_t)p * row_stride;
                     if constexpr (W == 4) {
-                        const float4 w = p < P ? __ldcg(reinterpret_cast<const float4*>(q))
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float4 w = p < p_hi ? __ldcg(reinterpret_cast<const float4*>(q))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                         v[j][0] = w.x; v[j][1] = w.y; v[j][2] = w.z; v[j][3] = w.w;
                     } else if constexpr (W == 2) {
-                        const float2 w = p < P ? __ldcg(reinterpret_cast<const float2*>(q))
-                                               : make_float2(0.f, 0.f);
+                        const float2 w = p < p_hi ? __ldcg(reinterpret_cast<const float2*>(q))
+                                                  : make_float2(0.f, 0.f);
                         v[j][0] = w.x; v[j][1] = w.y;
                     } else {
-                        v[j][0] = p < P ? __ldcg(q) : 0.f;
+                        v[j][0] = p < p_hi ? __ldcg(q) : 0.f;
                     }
                 }
 #pragma unroll
                 for (int j = 0; j < L; ++j)
 #pragma unroll
-                    for (int i = 0; i < U; ++i)
-                        comp_add(S[i], C[i], v[j][E * i], E == 2 ? v[j][E * i + E - 1] : 0.f);
+                    for (int i = 0; i < U; ++i) {
+                        if constexpr (COMPACT)
+                            S[i] += v[j][i];
+                        else
+                            comp_add(S[i], C[i], v[j][2 * i], v[j][2 * i + 1]);
+                    }
             }
         }
-        // Tree over r: at step s, subtotal r < s takes in subtotal r + s.
-        float* mine = scratch + (size_t)t * 2 * U;
-        if (act) {
+        // Fold the row subsets: lane (s, k) takes in lane (s + o, k) for o = 2, 1 (in units
+        // of kFinUnits lanes); lane (0, k) ends with the warp's total of unit k.
+#pragma unroll
+        for (int o = kFinSub / 2; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                const float s2 = __shfl_down_sync(kFullMask, S[i], o * kFinUnits);
+                const float c2 = __shfl_down_sync(kFullMask, C[i], o * kFinUnits);
+                if constexpr (COMPACT)
+                    S[i] += s2;
+                else
+                    comp_add(S[i], C[i], s2, c2);
+            }
+        }
+        if (sub == 0) {
+            float* mine = scratch + ((size_t)warp * kFinUnits + k) * 2 * U;
 #pragma unroll
             for (int i = 0; i < U; ++i) {
                 mine[2 * i] = S[i];
@@ -185,23 +211,25 @@ __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
             }
         }
         __syncthreads();
-        for (int st = R >> 1; st > 0; st >>= 1) {
-            if (r < st) {
-                const float* other = scratch + (size_t)(t + st * nk) * 2 * U;
+        if (rw == 0 && sub == 0 && act) {  // the group's warp totals, in warp order
+            float T2[U], C2[U];
+#pragma unroll
+            for (int i = 0; i < U; ++i) T2[i] = C2[i] = 0.f;
+            for (int w = warp; w < warp + RW; ++w) {
+                const float* o = scratch + ((size_t)w * kFinUnits + k) * 2 * U;
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
-                    comp_add(S[i], C[i], other[2 * i], other[2 * i + 1]);
-                    mine[2 * i] = S[i];
-                    mine[2 * i + 1] = C[i];
+                    if constexpr (COMPACT)
+                        T2[i] += o[2 * i];
+                    else
+                        comp_add(T2[i], C2[i], o[2 * i], o[2 * i + 1]);
                 }
             }
-            __syncthreads();
-        }
-        if (r == 0) {
             T* dst = static_cast<T*>(stat == 0 ? a.dgamma : a.dbeta) + (size_t)grp * U;
 #pragma unroll
-            for (int i = 0; i < U; ++i) dst[i] = IO::from_f(S[i] + C[i]);
+            for (int i = 0; i < U; ++i) dst[i] = IO::from_f(T2[i] + C2[i]);
         }
+        __syncthreads();  // scratch is reused by the next group
     }
 }
 
@@ -306,10 +334,11 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     if (warp == kTileRows) {  // producer
         if (lane == 0) {
             int k = 0;
-            for (; k < my_tiles; ++k) {
-                const int slot = k % stages;
-                if (k >= stages &&
-                    !mbar_wait(&empty_bar[slot], (unsigned)(k / stages - 1) & 1u, a.limit_ns)) {
+            RingPos pos;
+            for (; k < my_tiles; ++k, pos.next(stages)) {
+                const int slot = pos.slot;
+                // A slot's second and later fills wait for the consumers of the previous pass.
+                if (k >= stages && !mbar_wait(&empty_bar[slot], pos.phase ^ 1u, a.limit_ns)) {
                     raise_status(a.status, kStatusTimeout);
                     break;
                 }
@@ -335,14 +364,15 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
         int row = t0 * kTileRows + warp;
         float mu_next = row < rows ? a.mean[row] : 0.f;
         float rs_next = row < rows ? a.rstd[row] : 0.f;
-        for (int k = 0; k < my_tiles; ++k, row += kTileRows) {
-            const int slot = k % stages;
+        RingPos pos;
+        for (int k = 0; k < my_tiles; ++k, row += kTileRows, pos.next(stages)) {
+            const int slot = pos.slot;
             const float mu = mu_next, rs = rs_next;
             if (row + kTileRows < rows && k + 1 < my_tiles) {
                 mu_next = a.mean[row + kTileRows];
                 rs_next = a.rstd[row + kTileRows];
             }
-            const bool ok = mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, a.limit_ns);
+            const bool ok = mbar_wait(&full_bar[slot], pos.phase, a.limit_ns);
             if (!__all_sync(kFullMask, ok)) {
                 if (lane == 0) raise_status(a.status, kStatusTimeout);
                 break;
@@ -499,17 +529,16 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         fence_barrier_init();
     }
     __syncthreads();
-    auto issue = [&](int k) {  // thread 0 only: fetch row r0 + k
+    auto issue = [&](int k, int slot) {  // thread 0 only: fetch row r0 + k into `slot`
         const int row = r0 + k;
         if (row >= r1) return;
-        const int slot = k % stages;
         unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], slot_bytes);
         bulk_g2s(dst, dy + (size_t)row * cols, row_bytes, &full_bar[slot]);
         bulk_g2s(dst + row_bytes, xr + (size_t)row * cols, row_bytes, &full_bar[slot]);
     };
     if (tid == 0)
-        for (int k = 0; k < stages; ++k) issue(k);
+        for (int k = 0; k < stages; ++k) issue(k, k);
 
     using PR = Pairs<T>;
     constexpr int H = PR::kPairs;
@@ -532,14 +561,15 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     int k = 0;
     // mean and rstd are loaded one row ahead (off the row's critical path).
     float mu_next = r0 < r1 ? a.mean[r0] : 0.f, rs_next = r0 < r1 ? a.rstd[r0] : 0.f;
-    for (int row = r0; row < r1; ++row, ++k) {
-        const int slot = k % stages;
+    RingPos pos;
+    for (int row = r0; row < r1; ++row, ++k, pos.next(stages)) {
+        const int slot = pos.slot;
         const float mu = mu_next, rs = rs_next;
         if (row + 1 < r1) {
             mu_next = a.mean[row + 1];
             rs_next = a.rstd[row + 1];
         }
-        if (!mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, a.limit_ns)) abort_flag = 1;
+        if (!mbar_wait(&full_bar[slot], pos.phase, a.limit_ns)) abort_flag = 1;
         const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
@@ -600,7 +630,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
             }
         }
         __syncthreads();  // slot and `red` free again
-        if (tid == 0) issue(k + stages);
+        if (tid == 0) issue(k + stages, slot);  // row k + stages takes row k's slot
     }
 
     if (abort_flag) {
@@ -896,6 +926,22 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.cols = a.cols;
     k.part = reinterpret_cast<float2*>(a.partials);
     k.compact = (p.path == kPathScalar || p.kahan) ? 0 : 1;
+    {
+        // Warps per unit group in the finish: the fewest (a divisor of the warp count) for
+        // which one batch of loads per lane covers all P partial rows.
+        const int nw = p.threads / 32;
+        const int U = k.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
+                                : (a.cols % 2 == 0 ? 2 : 1);
+        const int rows_per_warp_batch = kFinSub * (kFinBatch / ((k.compact ? 1 : 2) * U));
+        const int need = (p.grid + rows_per_warp_batch - 1) / rows_per_warp_batch;
+        int rw = nw;
+        for (int d = 1; d <= nw; ++d)
+            if (nw % d == 0 && d >= need) {
+                rw = d;
+                break;
+            }
+        k.fin_rw = rw;
+    }
     k.ctr = a.counters;
     k.status = a.status;
     k.limit_ns = a.wait_limit_ns;

@@ -111,13 +111,13 @@ __device__ __forceinline__ f2 f2_make(float lo, float hi) {
 }
 __device__ __forceinline__ f2 f2_splat(float a) { return f2_make(a, a); }
 __device__ __forceinline__ float f2_lo(f2 a) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    float lo;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {%0, t}, %1;\n\t}" : "=f"(lo) : "l"(a.v));
     return lo;
 }
 __device__ __forceinline__ float f2_hi(f2 a) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    float hi;
+    asm("{\n\t.reg .f32 t;\n\tmov.b64 {t, %0}, %1;\n\t}" : "=f"(hi) : "l"(a.v));
     return hi;
 }
 __device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
@@ -407,6 +407,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, uint64
         if (global_ns() - t0 > limit_ns) return false;
     }
 }
+
+// Position in a ring of n slots: the slot index and the parity of the current pass over the
+// ring (the mbarrier phase parity a waiter on that slot needs), advanced without division.
+struct RingPos {
+    int slot = 0;
+    unsigned phase = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
 
 // Default limit of every device-side wait: 2 seconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -85,10 +85,11 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
     if (warp == kTileRows) {  // producer
         if (lane == 0) {
             int k = 0;
-            for (; k < my_tiles; ++k) {
-                const int slot = k % stages;
-                if (k >= stages &&
-                    !mbar_wait(&empty_bar[slot], (unsigned)(k / stages - 1) & 1u, wait_limit_ns)) {
+            RingPos pos;
+            for (; k < my_tiles; ++k, pos.next(stages)) {
+                const int slot = pos.slot;
+                // A slot's second and later fills wait for the consumers of the previous pass.
+                if (k >= stages && !mbar_wait(&empty_bar[slot], pos.phase ^ 1u, wait_limit_ns)) {
                     raise_status(status, kStatusTimeout);
                     break;
                 }
@@ -117,9 +118,10 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
         PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
     const bool write_res = res_out != nullptr;
-    for (int k = 0; k < my_tiles; ++k) {
-        const int slot = k % stages;
-        const bool ok = mbar_wait(&full_bar[slot], (unsigned)(k / stages) & 1u, wait_limit_ns);
+    RingPos pos;
+    for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
+        const int slot = pos.slot;
+        const bool ok = mbar_wait(&full_bar[slot], pos.phase, wait_limit_ns);
         if (!__all_sync(kFullMask, ok)) {
             if (lane == 0) raise_status(status, kStatusTimeout);
             break;
@@ -226,17 +228,16 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     }
     __syncthreads();
 
-    auto issue = [&](int k) {  // thread 0 only: fetch the k-th row of this block
+    auto issue = [&](int k, int slot) {  // thread 0 only: fetch the k-th row of this block
         const int row = blockIdx.x + k * gridDim.x;
         if (row >= rows) return;
-        const int slot = k % stages;
         unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], slot_bytes);
         bulk_g2s(dst, x + (size_t)row * cols, row_bytes, &full_bar[slot]);
         if (HAS_RES) bulk_g2s(dst + row_bytes, res + (size_t)row * cols, row_bytes, &full_bar[slot]);
     };
     if (tid == 0)
-        for (int k = 0; k < stages; ++k) issue(k);
+        for (int k = 0; k < stages; ++k) issue(k, k);
 
     // gamma, beta for this thread's vectors (the same columns in every row), as fp32 pairs.
     using PR = Pairs<T>;
@@ -251,10 +252,10 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
 
     const bool write_res = res_out != nullptr;
     int k = 0;
-    for (int row = blockIdx.x; row < rows; row += gridDim.x, ++k) {
-        const int slot = k % stages;
-        const unsigned parity = (unsigned)(k / stages) & 1u;
-        if (!mbar_wait(&full_bar[slot], parity, wait_limit_ns)) abort_flag = 1;
+    RingPos pos;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x, ++k, pos.next(stages)) {
+        const int slot = pos.slot;
+        if (!mbar_wait(&full_bar[slot], pos.phase, wait_limit_ns)) abort_flag = 1;
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
             }
         }
         __syncthreads();  // the slot and `red` are free again
-        if (tid == 0) issue(k + stages);
+        if (tid == 0) issue(k + stages, slot);  // row k + stages takes row k's slot
     }
 
     if (abort_flag) {
