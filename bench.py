@@ -185,7 +185,8 @@ def max_over_ranks(world, v: float) -> float:
 # ------------------------------------------------------------------------------------------
 # The reference arm: the float64 oracle on the host cores (the pages ship no runnable code).
 # ------------------------------------------------------------------------------------------
-def time_oracle(workload: str, steps: int, warmup: int, budget_s: float, target_s: float = 0.0):
+def time_oracle(workload: str, steps: int, warmup: int, budget_s: float, target_s: float = 0.0,
+                threads: int = 0):
     """Time the oracle's fwd+bwd on the workload.  Each step covers all rows unless that
     would overrun `budget_s`; with `target_s` > 0 the number of steps is instead chosen to
     take about that long (the CPU-baseline sample)."""
@@ -197,7 +198,7 @@ def time_oracle(workload: str, steps: int, warmup: int, budget_s: float, target_
     s = 4 if w.dtype == "f32" else 2
     inp = synth.workload_inputs(workload, seed=0)
     f64 = {k: v.float().numpy().astype(np.float64) for k, v in inp.items()}
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     oracle.build()
 
     def step(rows):
@@ -352,24 +353,25 @@ def run_ours(args):
     ms_total = max_over_ranks(world, e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
 
-    # ---- per-kernel launch durations (same stream, same rotation, separate loops) ----
-    nk = min(args.steps, 500)
+    # ---- per-kernel launch durations (same stream, same rotation, separate loops): the
+    # median of 5 repeats of a graph of nk launches ----
+    nk = min(args.steps, 400)
     kern = {}
     for name, fn, nb in (("fwd", fwd, fwd_bytes(R, C, s)), ("bwd", lambda k: bwd(k + nsets // 2), bwd_bytes(R, C, s))):
         g = capture(fn, nk, 0)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        reps = max(1, 2000 // nk)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         with torch.cuda.stream(stream):
             g.replay()
             torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(reps):
+            ev[0].record(stream)
+            for r in range(5):
                 g.replay()
-            b.record(stream)
+                ev[r + 1].record(stream)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * nk)
-        kern[name] = {"us_per_launch": us, "algorithmic_bytes": nb, "gbs": nb / us / 1e3}
+        reps_us = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / nk for r in range(5))
+        us = reps_us[2]
+        kern[name] = {"us_per_launch": us, "algorithmic_bytes": nb, "gbs": nb / us / 1e3,
+                      "repeats_us": [round(v, 3) for v in reps_us], "launches_per_repeat": nk}
     sampler.stop()
 
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
@@ -377,23 +379,45 @@ def run_ours(args):
     host = {k: sets[0][k].cpu().pin_memory() for k in ("x", "res", "dy", "gamma", "beta")}
     outs_h = {k: torch.empty(sets[0][k].shape, dtype=sets[0][k].dtype).pin_memory()
               for k in ("out", "res_out", "dx", "mean", "rstd", "dgamma", "dbeta")}
-    dev = sets[0]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    # Steps alternate between two device buffer sets; uploads, kernels and downloads run on
+    # their own streams, so step k's upload overlaps step k-1's kernels and download (the
+    # host link is full duplex).  Events keep each set's upload after its previous download.
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_free = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step(k):
+        b = k % 2
+        dev = sets[b]
+        with torch.cuda.stream(up):
+            if k >= 2:
+                up.wait_event(ev_free[b])
+            for name, t in host.items():
+                dev[name].copy_(t, non_blocking=True)
+            ev_in[b].record(up)
+        stream.wait_event(ev_in[b])
+        fwd(b)
+        ln.bwd(dev["dy"], dev["res_out"], dev["gamma"], dev["mean"], dev["rstd"],
+               dx=dev["dx"], dgamma=dev["dgamma"], dbeta=dev["dbeta"], workspace=ws,
+               stream=stream)
+        ev_done[b].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            for name, t in outs_h.items():
+                t.copy_(dev[name], non_blocking=True)
+            ev_free[b].record(down)
+
+    for k in range(4):  # warm-up
+        e2e_step(k)
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            for k, t in host.items():
-                dev[k].copy_(t, non_blocking=True)
-            fwd(0)
-            ln.bwd(dev["dy"], dev["res_out"], dev["gamma"], dev["mean"], dev["rstd"],
-                   dx=dev["dx"], dgamma=dev["dgamma"], dbeta=dev["dbeta"], workspace=ws,
-                   stream=stream)
-            for k, t in outs_h.items():
-                t.copy_(dev[k], non_blocking=True)
-    stream.synchronize()
+    for k in range(e2e_steps):
+        e2e_step(k)
+    torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     barrier(world)
 
@@ -405,6 +429,7 @@ def run_ours(args):
     kname = {"fwd": "ln_fwd", "bwd": "ln_bwd"}[dom]
     achieved = kern[dom]["gbs"]
     cpu = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=10.0)
+    cpu1 = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=4.0, threads=1)
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -430,7 +455,11 @@ def run_ours(args):
                      "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": profiled_traffic(kname)},
         "cpu_baseline": {"value": cpu["value"], "unit": "GB/s", "cores": cpu["cores"],
-                         "kind": "oracle", "sample": cpu["sample"]},
+                         "kind": "oracle", "sample": cpu["sample"],
+                         "rows_per_s": cpu["rows_per_s"],
+                         "single_thread": {"value": cpu1["value"], "unit": "GB/s",
+                                           "rows_per_s": cpu1["rows_per_s"],
+                                           "sample": cpu1["sample"]}},
     }
     print(json.dumps(line), flush=True)
     return 0

@@ -452,14 +452,33 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             if (vi < nvec) {
                 float* dg = smem_f + (size_t)warp * cols + (size_t)vi * V;
                 float* db = dg + (size_t)kTileRows * cols;
-#pragma unroll
-                for (int h = 0; h < H; h += 2) {
-                    put(dg + 2 * h, accg[v][h], accg[v][h + 1]);
-                    put(db + 2 * h, accb[v][h], accb[v][h + 1]);
+                const f2 z = f2_splat(0.f);
+                if constexpr (H == 4) {
+                    // A lane's 8 columns are two 16-byte halves at a 32-byte lane stride.
+                    // Lanes 4-7 of each group of 8 store their upper half first, so the 8
+                    // lanes of a 128-bit store phase hit 8 distinct groups of 4 banks.
+                    const bool sw = ((lane >> 2) & 1) != 0;
+                    const int o0 = sw ? 4 : 0, o1 = sw ? 0 : 4;
+                    put(dg + o0, sw ? accg[v][2] : accg[v][0], sw ? accg[v][3] : accg[v][1]);
+                    put(db + o0, sw ? accb[v][2] : accb[v][0], sw ? accb[v][3] : accb[v][1]);
+                    put(dg + o1, sw ? accg[v][0] : accg[v][2], sw ? accg[v][1] : accg[v][3]);
+                    put(db + o1, sw ? accb[v][0] : accb[v][2], sw ? accb[v][1] : accb[v][3]);
                     if constexpr (KAHAN) {
-                        const f2 z = f2_splat(0.f);
-                        put(dg + lo_off + 2 * h, f2_sub(z, cmpg[v][h]), f2_sub(z, cmpg[v][h + 1]));
-                        put(db + lo_off + 2 * h, f2_sub(z, cmpb[v][h]), f2_sub(z, cmpb[v][h + 1]));
+                        put(dg + lo_off + o0, f2_sub(z, sw ? cmpg[v][2] : cmpg[v][0]),
+                            f2_sub(z, sw ? cmpg[v][3] : cmpg[v][1]));
+                        put(db + lo_off + o0, f2_sub(z, sw ? cmpb[v][2] : cmpb[v][0]),
+                            f2_sub(z, sw ? cmpb[v][3] : cmpb[v][1]));
+                        put(dg + lo_off + o1, f2_sub(z, sw ? cmpg[v][0] : cmpg[v][2]),
+                            f2_sub(z, sw ? cmpg[v][1] : cmpg[v][3]));
+                        put(db + lo_off + o1, f2_sub(z, sw ? cmpb[v][0] : cmpb[v][2]),
+                            f2_sub(z, sw ? cmpb[v][1] : cmpb[v][3]));
+                    }
+                } else {  // fp32: one 16-byte store per vector, consecutive lanes adjacent
+                    put(dg, accg[v][0], accg[v][1]);
+                    put(db, accb[v][0], accb[v][1]);
+                    if constexpr (KAHAN) {
+                        put(dg + lo_off, f2_sub(z, cmpg[v][0]), f2_sub(z, cmpg[v][1]));
+                        put(db + lo_off, f2_sub(z, cmpb[v][0]), f2_sub(z, cmpb[v][1]));
                     }
                 }
             }
