@@ -96,6 +96,28 @@ int blocks_per_sm(const void* kernel, int threads, size_t smem) {
     return n;
 }
 
+cudaError_t launch_kernel(const void* kern, dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, void** args, bool cooperative) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cooperative) {  // every block co-resident: the driver checks it against occupancy
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 void record_cuda_error(cudaError_t e) { t_last_cuda_error = (int)e; }
 
 bool vector_ok(Dtype dt, int cols, const void* const* ptrs, int nptrs) {

@@ -233,37 +233,50 @@ __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     }
 }
 
+// Called by every thread of every block once the block's partial row is written.  One
+// thread per block publishes the row (block barrier, then a GPU-scope fence and the counter
+// increment).  Blocks that own no unit group of the finish are then done and leave, freeing
+// their SM; the others wait, bounded, until all P blocks have arrived, and finish their
+// groups.  The finishing block that is last past the wait puts the counters back to 0.
 template <typename T>
 __device__ void arrive_and_finish(const KParams& a, float* scratch) {
     __shared__ int s_ok;
-    const unsigned P = gridDim.x;
+    const int P = (int)gridDim.x, f = (int)blockIdx.x;
+    const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
+                            : (a.cols % 2 == 0 ? 2 : 1);  // as finish_units is instantiated
+    const int ng = (2 * (a.cols / U) + kFinUnits - 1) / kFinUnits;
+    const bool finisher = (long long)(f + 1) * ng / P > (long long)f * ng / P;
+    const unsigned F = (unsigned)min(P, ng);  // blocks owning at least one group
     __syncthreads();  // every thread's partial sums are written
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(&a.ctr[0], 1u);
-        const bool ok = wait_counter_geq(&a.ctr[0], P + a.wait_extra, a.limit_ns);
-        __threadfence();
-        s_ok = ok ? 1 : 0;
-        if (!ok) raise_status(a.status, kStatusTimeout);
+        if (finisher) {
+            const bool ok = wait_counter_geq(&a.ctr[0], (unsigned)P + a.wait_extra, a.limit_ns);
+            __threadfence();
+            s_ok = ok ? 1 : 0;
+            if (!ok) raise_status(a.status, kStatusTimeout);
+        }
     }
+    if (!finisher) return;  // the same for every thread of the block
     __syncthreads();
     if (!s_ok) return;
     if (a.compact) {
         if (a.cols % 4 == 0)
-            finish_units<T, 4, true>(a, (int)P, (int)blockIdx.x, scratch);
+            finish_units<T, 4, true>(a, P, f, scratch);
         else if (a.cols % 2 == 0)
-            finish_units<T, 2, true>(a, (int)P, (int)blockIdx.x, scratch);
+            finish_units<T, 2, true>(a, P, f, scratch);
         else
-            finish_units<T, 1, true>(a, (int)P, (int)blockIdx.x, scratch);
+            finish_units<T, 1, true>(a, P, f, scratch);
     } else {
         if (a.cols % 2 == 0)
-            finish_units<T, 2, false>(a, (int)P, (int)blockIdx.x, scratch);
+            finish_units<T, 2, false>(a, P, f, scratch);
         else
-            finish_units<T, 1, false>(a, (int)P, (int)blockIdx.x, scratch);
+            finish_units<T, 1, false>(a, P, f, scratch);
     }
     if (threadIdx.x == 0) {
         const unsigned done = atomicAdd(&a.ctr[1], 1u);
-        if (done == P - 1) {  // every block is past its wait: reset for the next call
+        if (done == F - 1) {  // every finishing block is past its wait: reset for the next call
             atomicExch(&a.ctr[0], 0u);
             atomicExch(&a.ctr[1], 0u);
         }
@@ -291,6 +304,7 @@ template <typename T, int VPL, bool KAHAN>
 __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>())
     bwd_tile_kernel(const KParams a) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -523,6 +537,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 template <typename T, int VPT, bool KAHAN>
 __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const KParams a) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int V = IO::kVec;
     constexpr int MAXW = kBwdBlockMaxThreads / 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -703,6 +718,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
 template <typename T>
 __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KParams a) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int NW = kBwdScalarThreads / 32;
     extern __shared__ __align__(16) float smem_f[];
     __shared__ float red[2][NW];
@@ -967,20 +983,8 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.wait_extra = a.wait_extra;
     k.stages = p.stages;
     void* args[] = {&k};
-    // A cooperative launch (all blocks co-resident, checked by the driver against the
-    // occupancy), issued through cudaLaunchKernelEx so that it can also be captured into a
-    // CUDA graph.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.grid);
-    cfg.blockDim = dim3(p.threads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
+    // A cooperative launch: all blocks co-resident, as the finish's bounded wait needs.
+    cudaError_t e = launch_kernel(kern, dim3(p.grid), dim3(p.threads), p.smem, stream, args, true);
     if (e == cudaSuccess) *launches = 1;
     return e;
 }

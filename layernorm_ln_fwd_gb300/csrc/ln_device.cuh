@@ -421,6 +421,16 @@ struct RingPos {
     }
 };
 
+// Programmatic dependent launch (the kernels are launched with programmatic stream
+// serialization allowed).  At entry a kernel waits until the grid before it in the stream has
+// completed and its memory is visible (a no-op when there is none), then lets the grid after
+// it begin launching: that grid's blocks take SMs as this grid's blocks leave and do their
+// own set-up, but they too wait here before touching memory, so stream order holds.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Default limit of every device-side wait: 2 seconds.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

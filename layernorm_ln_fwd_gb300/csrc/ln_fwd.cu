@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     float* __restrict__ mean, float* __restrict__ rstd, int stages,
                     unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -207,6 +208,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                      float* __restrict__ mean, float* __restrict__ rstd, int stages,
                      unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages];
@@ -357,6 +359,7 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
                       int rows, int cols, T* __restrict__ out, T* __restrict__ res_out,
                       float* __restrict__ mean, float* __restrict__ rstd) {
     using IO = Io<T>;
+    pdl_enter();
     constexpr int NW = kFwdScalarThreads / 32;
     __shared__ float red[4][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -462,7 +465,7 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     uint64_t limit = a.wait_limit_ns;
     void* args[] = {&x,   &res,     &gamma, &beta, &eps,    &rows,   &cols,
                     &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
-    return cudaLaunchKernel(kern, dim3(grid), dim3(kTileThreads), args, smem, stream);
+    return launch_kernel(kern, dim3(grid), dim3(kTileThreads), smem, stream, args, false);
 }
 
 template <typename T>
@@ -535,7 +538,7 @@ cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     uint64_t limit = a.wait_limit_ns;
     void* args[] = {&x,   &res,     &gamma, &beta, &eps,   &rows,   &cols,
                     &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
-    return cudaLaunchKernel(kern, dim3(grid), dim3(threads), args, smem, stream);
+    return launch_kernel(kern, dim3(grid), dim3(threads), smem, stream, args, false);
 }
 
 template <typename T>
@@ -557,7 +560,7 @@ cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     float* mean = a.mean;
     float* rstd = a.rstd;
     void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd};
-    return cudaLaunchKernel(kern, dim3(grid), dim3(kFwdScalarThreads), args, 0, stream);
+    return launch_kernel(kern, dim3(grid), dim3(kFwdScalarThreads), 0, stream, args, false);
 }
 
 template <typename T>

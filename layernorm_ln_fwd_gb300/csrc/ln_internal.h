@@ -75,6 +75,11 @@ struct BwdPlan {
 // multiple of 16 bytes.
 bool vector_ok(Dtype dt, int cols, const void* const* ptrs, int nptrs);
 
+// Launch `kern` with programmatic stream serialization allowed (and cooperatively when
+// `cooperative`): cudaLaunchKernelEx, so that it can also be captured into a CUDA graph.
+cudaError_t launch_kernel(const void* kern, dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, void** args, bool cooperative);
+
 cudaError_t launch_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
                        cudaStream_t stream, int* launches);
 
