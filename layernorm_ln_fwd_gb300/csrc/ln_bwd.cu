@@ -37,6 +37,7 @@
 //  * partial sums are stored as (hi, lo) fp32 pairs and the finishers add them with TwoSum,
 //    so the only rounding left at the end is the final one to the output type.
 #include <algorithm>
+#include <type_traits>
 
 #include "ln_device.cuh"
 #include "ln_internal.h"
@@ -373,45 +374,41 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             const int vi = v * 32 + lane;
             PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
         }
-        // mean and rstd of the warp's row in the next tile are loaded one tile ahead, so
-        // their latency is not on the row's critical path.
-        int row = t0 * kTileRows + warp;
-        float mu_next = row < rows ? a.mean[row] : 0.f;
-        float rs_next = row < rows ? a.rstd[row] : 0.f;
-        RingPos pos;
-        for (int k = 0; k < my_tiles; ++k, row += kTileRows, pos.next(stages)) {
-            const int slot = pos.slot;
-            const float mu = mu_next, rs = rs_next;
-            if (row + kTileRows < rows && k + 1 < my_tiles) {
-                mu_next = a.mean[row + kTileRows];
-                rs_next = a.rstd[row + kTileRows];
-            }
-            const bool ok = mbar_wait(&full_bar[slot], pos.phase, a.limit_ns);
-            if (!__all_sync(kFullMask, ok)) {
-                if (lane == 0) raise_status(a.status, kStatusTimeout);
-                break;
-            }
-            if (row < rows) {
-                const size_t base = (size_t)row * cols;
-                const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
-                                                          (size_t)warp * row_bytes);
-                const T* xs = dys + (size_t)kTileRows * cols;
-                const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
-                // Row sums; the low halves take the even columns, the high halves the odd.
-                f2 sg = f2_splat(0.f), sgx = f2_splat(0.f);
+        // One or two rows through both passes.  With two (the warp's row of tile k and of
+        // tile k + 1), their first passes run together, their four row sums share one
+        // butterfly and their second passes run together; per lane the column sums still add
+        // tile k's terms before tile k + 1's, so the results are those of one row at a time.
+        auto body = [&](auto nr_c, const int (&row_)[2], const int (&slot_)[2],
+                        const float (&mu_)[2], const float (&rs_)[2]) {
+            constexpr int NR = decltype(nr_c)::value;
+            const T* dys[NR];
+            const T* xs[NR];
+            f2 mu2[NR], rs2[NR], sg[NR], sgx[NR];
 #pragma unroll
-                for (int v = 0; v < VPL; ++v) {
-                    const int vi = v * 32 + lane;
-                    if (vi < nvec) {
+            for (int r = 0; r < NR; ++r) {
+                dys[r] = reinterpret_cast<const T*>(smem_raw + (size_t)slot_[r] * slot_bytes +
+                                                    (size_t)warp * row_bytes);
+                xs[r] = dys[r] + (size_t)kTileRows * cols;
+                mu2[r] = f2_splat(mu_[r]);
+                rs2[r] = f2_splat(rs_[r]);
+                // Row sums; the low halves take the even columns, the high halves the odd.
+                sg[r] = sgx[r] = f2_splat(0.f);
+            }
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const int vi = v * 32 + lane;
+                if (vi < nvec) {
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
                         f2 d[H], xx[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
+                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
-                            const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                            const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
                             const f2 g = f2_mul(gm[v][h], d[h]);
-                            sg = f2_add(sg, g);
-                            sgx = f2_fma(g, xh, sgx);
+                            sg[r] = f2_add(sg[r], g);
+                            sgx[r] = f2_fma(g, xh, sgx[r]);
                             if constexpr (KAHAN) {
                                 kahan2(accg[v][h], cmpg[v][h], f2_mul(d[h], xh));
                                 kahan2(accb[v][h], cmpb[v][h], d[h]);
@@ -422,30 +419,101 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                         }
                     }
                 }
-                float tg = f2_lo(sg) + f2_hi(sg), tgx = f2_lo(sgx) + f2_hi(sgx);
-                warp_sum2(tg, tgx);  // the one reduction of the row: both sums together
-                // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
-                // g - mg cancels exactly where it should (a one-column row gives dx = 0).
-                const f2 mg2 = f2_splat(tg / fcols), mgx2 = f2_splat(tgx / fcols);
+            }
+            // The one reduction of each row: both of its sums together (xor butterfly).
+            float t[2 * NR];
 #pragma unroll
-                for (int v = 0; v < VPL; ++v) {
-                    const int vi = v * 32 + lane;
-                    if (vi < nvec) {  // second pass re-reads the row from shared memory
+            for (int r = 0; r < NR; ++r) {
+                t[2 * r] = f2_lo(sg[r]) + f2_hi(sg[r]);
+                t[2 * r + 1] = f2_lo(sgx[r]) + f2_hi(sgx[r]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < 2 * NR; ++i) t[i] += __shfl_xor_sync(kFullMask, t[i], o);
+            // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
+            // g - mg cancels exactly where it should (a one-column row gives dx = 0).
+            f2 mg2[NR], mgx2[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                mg2[r] = f2_splat(t[2 * r] / fcols);
+                mgx2[r] = f2_splat(t[2 * r + 1] / fcols);
+            }
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const int vi = v * 32 + lane;
+                if (vi < nvec) {  // second pass re-reads the rows from shared memory
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
                         f2 d[H], xx[H], o[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
+                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
-                            const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
+                            const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
                             const f2 g = f2_mul(gm[v][h], d[h]);
-                            o[h] = f2_mul(rs2, f2_sub(g, f2_fma(xh, mgx2, mg2)));
+                            o[h] = f2_mul(rs2[r], f2_sub(g, f2_fma(xh, mgx2[r], mg2[r])));
                         }
-                        st_stream(dx + base + (size_t)vi * V, PR::pack(o));
+                        st_stream(dx + (size_t)row_[r] * cols + (size_t)vi * V, PR::pack(o));
                     }
                 }
             }
+        };
+        // Rows go in pairs of consecutive tiles when the ring is deep enough that the pair's
+        // two slots still leave tiles in flight behind them.  The paired form is built for
+        // bf16 rows of 4 or 5 vectors per lane and for fp32 rows, where it measured faster on
+        // GB300 (bf16 8192x1280: 21.8 -> 19.9 us; fp32 262144x1000: 544 -> 507 us, there
+        // even at ring depths that keep it to one row at a time); bf16 rows of 3 or fewer
+        // vectors per lane measured slower with it.
+        constexpr bool kPairRows = (Io<T>::kVec == 8 && VPL >= 4) || Io<T>::kVec == 4;
+        const int pair_max = (kPairRows && stages >= 4) ? 2 : 1;
+        // mean and rstd of the next step's rows are loaded a step ahead, so their latency is
+        // not on the rows' critical path.
+        auto load_stats = [&](int kk, int nr, float (&mu)[2], float (&rs)[2]) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int rr = (t0 + kk + r) * kTileRows + warp;
+                const bool valid = r < nr && kk + r < my_tiles && rr < rows;
+                mu[r] = valid ? a.mean[rr] : 0.f;
+                rs[r] = valid ? a.rstd[rr] : 0.f;
+            }
+        };
+        float mu_n[2], rs_n[2];
+        load_stats(0, min(pair_max, my_tiles), mu_n, rs_n);
+        RingPos pos;
+        for (int k = 0; k < my_tiles;) {
+            const int nr = min(pair_max, my_tiles - k);
+            int slots[2];
+            unsigned phases[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                slots[r] = pos.slot;
+                phases[r] = pos.phase;
+                if (r < nr) pos.next(stages);
+            }
+            const float mu[2] = {mu_n[0], mu_n[1]}, rs[2] = {rs_n[0], rs_n[1]};
+            if (k + nr < my_tiles) load_stats(k + nr, min(pair_max, my_tiles - k - nr), mu_n, rs_n);
+            bool ok = mbar_wait(&full_bar[slots[0]], phases[0], a.limit_ns);
+            if (nr == 2) ok = mbar_wait(&full_bar[slots[1]], phases[1], a.limit_ns) && ok;
+            if (!__all_sync(kFullMask, ok)) {
+                if (lane == 0) raise_status(a.status, kStatusTimeout);
+                break;
+            }
+            const int rws[2] = {(t0 + k) * kTileRows + warp, (t0 + k + 1) * kTileRows + warp};
+            if constexpr (kPairRows) {
+                if (nr == 2 && rws[1] < rows)
+                    body(std::integral_constant<int, 2>{}, rws, slots, mu, rs);
+                else if (rws[0] < rows)
+                    body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
+            } else if (rws[0] < rows) {
+                body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty_bar[slot]);
+            if (lane == 0) {
+                mbar_arrive(&empty_bar[slots[0]]);
+                if (nr == 2) mbar_arrive(&empty_bar[slots[1]]);
+            }
+            k += nr;
         }
     }
     __syncthreads();  // the ring is drained and no warp reads it any more
