@@ -14,28 +14,26 @@
 //  1. Each block owns a FIXED contiguous range of rows.  While it computes dx it
 //     accumulates dy * xhat and dy for the columns its threads own and, at the end, writes
 //     one row of partial sums per statistic to the workspace: part[stat][block][col].
-//  2. Every block then takes a ticket from an integer counter (atomicAdd).  The blocks whose
-//     tickets are among the last F are the finishers: each waits (bounded) until all blocks
-//     have arrived, then sums the partials of ITS slice of columns over blocks in a fixed
-//     order and writes dgamma and dbeta.  The last finisher puts the counters back to 0.
+//  2. Every block then increments an integer arrival counter (atomicAdd).  The blocks that
+//     own a slice of the columns wait (bounded) until all blocks have arrived, sum the
+//     partials of their slice over blocks in a fixed order and write dgamma and dbeta; the
+//     others leave.  The finishing block last past the wait puts the counters back to 0.
 //  This is the last-block-finishes idea of llm.c's layernorm_backward_kernel10 ("llm.c: the
-//  llmc/ CUDA kernel layer", section 3.3), widened from one finishing block to F so that
-//  the finish is spread over many SMs instead of serialising one SM on all partials.  The
-//  grid is launched cooperatively, so every block is resident and the wait always ends.
-//  Which block adds which rows, and in what order, depends only on (rows, cols, device),
-//  so dgamma and dbeta are bitwise reproducible run to run.
+//  llmc/ CUDA kernel layer", section 3.3), widened from one finishing block to many so that
+//  the finish is spread over SMs instead of serialising one SM on all partials.  The grid
+//  is launched cooperatively, so every block is resident and the wait always ends.  Which
+//  block adds which rows, and in what order, depends only on (rows, cols, device), so
+//  dgamma and dbeta are bitwise reproducible run to run.
 //
 // Accuracy of the column sums.  A plain fp32 sum of n terms of size sigma carries an error
 // of about 2^-24 * sigma * sqrt(n * L) for chains of L additions, whatever the order: for
-// 262144 rows that is ~1e-4, far above the 2e-5 that fp32 results are held to.  So:
-//  * the block kernels keep each thread's running sums compensated (Kahan: a second fp32
-//    register holds the rounding error of every addition) whenever a thread owns at most 16
-//    columns (rows up to 8192 columns wide; wider rows keep plain fp32 sums: the registers
-//    for compensation are not there);
-//  * the warp (tile) kernel (bf16, short per-lane chains) keeps plain per-lane sums and
-//    combines its warps with error-free additions (TwoSum);
-//  * partial sums are stored as (hi, lo) fp32 pairs and the finishers add them with TwoSum,
-//    so the only rounding left at the end is the final one to the output type.
+// 262144 rows that is ~1e-4, far above the 2e-5 that fp32 results are held to.  So for fp32
+// I/O (and bf16 rows long enough to make chains long) each thread or lane keeps its running
+// sums compensated (Kahan: a second fp32 register holds the rounding error of every
+// addition), partial sums are stored as (hi, lo) fp32 pairs and every later addition is
+// error-free (TwoSum), so the only rounding left is the final one to the output type.  For
+// bf16 results over short chains plain fp32 sums are far more accurate than the bf16 unit
+// in the last place, and the partials are stored and added plainly.
 #include <algorithm>
 #include <type_traits>
 

@@ -1,8 +1,9 @@
 // ln_device.cuh -- device-side building blocks shared by the forward and backward kernels.
 //
-// 128-bit vectors of the I/O type, warp reductions, mergeable row statistics, bulk-copy
-// (TMA) staging with mbarriers, bounded waits and the per-device status word.  Everything
-// here is sm_100-family code (built for sm_103a); nothing here allocates.
+// 128-bit vectors of the I/O type and their fp32-pair forms, warp reductions, row shifts and
+// mergeable row statistics, bulk-copy (TMA) staging with mbarriers and ring positions, the
+// programmatic-dependent-launch entry, bounded waits and the per-device status word.
+// Everything here is sm_100-family code (built for sm_103a); nothing here allocates.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -184,13 +185,10 @@ struct Pairs<__nv_bfloat16> {
 };
 
 // ---------------------------------------------------------------------------------------
-// Global memory access with cache hints.  Streamed tensors are read and written once per
-// kernel: they use the evict-first ("cs") policy so they do not push gamma/beta or the
-// backward's partial sums out of L2.
+// Global memory access with cache hints.  The row outputs are written once per kernel with
+// the evict-first ("cs") policy so they do not push gamma/beta or the backward's partial sums
+// out of L2 (the row inputs arrive by bulk copies into shared memory).
 // ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
-}
 __device__ __forceinline__ uint4 ld_keep(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
@@ -281,35 +279,6 @@ __device__ __forceinline__ RowStats block_stats(const float (*red)[32], int nw) 
     RowStats r{0.f, 0.f, 0.f, 0.f};
     if (lane < nw) r = RowStats{red[0][lane], red[1][lane], red[2][lane], red[3][lane]};
     warp_stats(r);
-    return r;
-}
-
-// A thread's own summary of the values v[0..count) (already shifted): their sum in four
-// independent partial sums (short chains, so the adds overlap), then M2 about the thread's
-// mean, again in four partial sums.  A thread holds at most 64 values; across threads the
-// sums are combined by stats_merge, which keeps the compensation.
-template <int N>
-__device__ __forceinline__ RowStats thread_stats(const float (&v)[N], int count) {
-    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (i < count) s4[i & 3] += v[i];
-    RowStats r;
-    r.s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    r.c = 0.f;
-    r.n = (float)count;
-    float q4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (count > 0) {
-        const float m = __fdiv_rn(r.s, r.n);
-#pragma unroll
-        for (int i = 0; i < N; ++i) {
-            if (i < count) {
-                const float e = v[i] - m;
-                q4[i & 3] += e * e;
-            }
-        }
-    }
-    r.q = (q4[0] + q4[1]) + (q4[2] + q4[3]);
     return r;
 }
 

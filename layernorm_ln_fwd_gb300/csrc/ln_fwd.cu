@@ -14,7 +14,7 @@
 //    var = sum d^2 / n - (sum d / n)^2 then has both terms of the order of var itself;
 //  * scalar kernel: each thread keeps a Welford summary (count, compensated sum, M2) and the
 //    summaries are combined with the Welford/Chan pairwise merge of the same section;
-//  * xhat = (d - mean(d)) * rstd, which never subtracts two large numbers.
+//  * xhat = d * rstd - mean(d) * rstd (one fma), which never subtracts two large numbers.
 // mean = K + mean(d) and rstd = 1 / sqrt(var + eps) are stored in fp32.
 //
 // Three kernel families compute the same function:
