@@ -60,11 +60,18 @@ def measured_peak():
 
 
 def source_hash() -> str:
+    """Hash of the kernel sources with comments and whitespace removed, so that a committed
+    traffic record stays tied to the code it was measured on and not to its comments."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "layernorm_ln_fwd_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = " ".join(text.split())
+        h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 
