@@ -286,3 +286,16 @@ def test_dependent_launches_in_a_cuda_graph(name):
                                else got[k].view(torch.int32),
                                ref[k].view(torch.uint8) if ref[k].dtype != torch.float32
                                else ref[k].view(torch.int32)), k
+
+
+@pytest.mark.parametrize("dtype,cols", [("bf16", 1280), ("bf16", 1024), ("f32", 1000), ("f32", 768)])
+@pytest.mark.parametrize("rows", [2131, 4099])
+def test_paired_rows_against_oracle(dtype, rows, cols):
+    """Row counts that give blocks several 7-row tiles, an odd number of them and a partial
+    last tile: the backward's warps take rows of consecutive tiles in pairs (bf16 rows of 4-5
+    vectors per lane, fp32 rows) with an unpaired step at the end; every element is compared
+    with the oracle."""
+    inp = synth.make_inputs(rows, cols, dtype, seed=rows + cols)
+    gpu = P.run_gpu(inp, EPS)
+    ref = P.run_oracle(inp, EPS)
+    P.compare_all(gpu, ref, dtype, conditioned=True)
