@@ -518,8 +518,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 
     // Block partial row.  The consumer warps put their sums in shared memory as
     // [stat][warp][cols] floats (the drained ring), followed by the negated compensations in
-    // the same layout when KAHAN; then each thread adds the 7 warps' values of a pair of
-    // columns in warp order (with TwoSum when KAHAN) and stores the (hi, lo) pairs of both.
+    // the same layout when KAHAN; then each thread adds the 7 warps' values of a group of 4
+    // columns in warp order (with TwoSum when KAHAN) and stores the block's partials of them.
     float* smem_f = reinterpret_cast<float*>(smem_raw);
     const size_t lo_off = (size_t)2 * kTileRows * cols;
     auto put = [&](float* dst, f2 a0, f2 a1) {
@@ -566,30 +566,37 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     }
     __syncthreads();
     const int P = gridDim.x;
-    const int half = cols >> 1;  // column pairs per statistic (cols is a multiple of 4)
-    for (int u = tid; u < 2 * half; u += blockDim.x) {
-        const int stat = u >= half ? 1 : 0;
-        const int c = 2 * (u - stat * half);
+    const int quarter = cols >> 2;  // groups of 4 columns per statistic (cols is a multiple of 4)
+    for (int u = tid; u < 2 * quarter; u += blockDim.x) {
+        const int stat = u >= quarter ? 1 : 0;
+        const int c = 4 * (u - stat * quarter);
         const float* src = smem_f + (size_t)stat * kTileRows * cols + c;
-        float S0 = 0.f, C0 = 0.f, S1 = 0.f, C1 = 0.f;
+        if constexpr (KAHAN) {
+            float S[4] = {0.f, 0.f, 0.f, 0.f}, C[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int w = 0; w < kTileRows; ++w) {
-            const float2 t = *reinterpret_cast<const float2*>(src + (size_t)w * cols);
-            if constexpr (KAHAN) {
-                const float2 l = *reinterpret_cast<const float2*>(src + lo_off + (size_t)w * cols);
-                comp_add(S0, C0, t.x, l.x);
-                comp_add(S1, C1, t.y, l.y);
-            } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
-                S0 += t.x;
-                S1 += t.y;
+            for (int w = 0; w < kTileRows; ++w) {
+                const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
+                const float4 l = *reinterpret_cast<const float4*>(src + lo_off + (size_t)w * cols);
+                comp_add(S[0], C[0], t.x, l.x);
+                comp_add(S[1], C[1], t.y, l.y);
+                comp_add(S[2], C[2], t.z, l.z);
+                comp_add(S[3], C[3], t.w, l.w);
             }
+            float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c);
+            dst[0] = make_float4(S[0], C[0], S[1], C[1]);
+            dst[1] = make_float4(S[2], C[2], S[3], C[3]);
+        } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
+            f2 S01 = f2_splat(0.f), S23 = f2_splat(0.f);
+#pragma unroll
+            for (int w = 0; w < kTileRows; ++w) {
+                const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
+                S01 = f2_add(S01, f2_make(t.x, t.y));
+                S23 = f2_add(S23, f2_make(t.z, t.w));
+            }
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.part) +
+                                       ((size_t)stat * P + blockIdx.x) * cols + c) =
+                make_float4(f2_lo(S01), f2_hi(S01), f2_lo(S23), f2_hi(S23));
         }
-        if constexpr (KAHAN)
-            *reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c) =
-                make_float4(S0, C0, S1, C1);
-        else
-            *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.part) +
-                                       ((size_t)stat * P + blockIdx.x) * cols + c) = make_float2(S0, S1);
     }
     arrive_and_finish<T>(a, smem_f);
 }
