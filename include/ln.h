@@ -31,7 +31,7 @@
  *  - Pointers need no particular alignment.  When every pointer is 16-byte aligned and a row
  *    is a multiple of 16 bytes (cols % 4 == 0 for fp32, cols % 8 == 0 for bf16) the 128-bit
  *    vector kernels run; otherwise a scalar kernel computes the same result.
- *  - Limits: 1 <= cols <= LN_MAX_COLS; 0 <= rows < 2^31.  rows == 0 is a no-op for the
+ *  - Limits: 1 <= cols <= LN_MAX_COLS; 0 <= rows <= LN_MAX_ROWS.  rows == 0 is a no-op for the
  *    forward; for the backward it writes dgamma = dbeta = 0.  With rows == 0 the pointers
  *    to [rows, cols] and [rows] arrays may be NULL (empty tensors often have no storage).
  *    eps must be finite and >= 0.
@@ -50,6 +50,8 @@ extern "C" {
 #endif
 
 #define LN_MAX_COLS 16384
+/* Largest row count: row indices, rounded up to whole 7-row tiles, stay within int range. */
+#define LN_MAX_ROWS 2147483583LL
 
 /* The raw bits of one bfloat16 value. */
 typedef uint16_t ln_bf16;
@@ -62,7 +64,7 @@ typedef enum ln_status {
     LN_OK = 0,
     LN_EINVAL = 1,        /* a NULL required pointer, rows < 0, cols <= 0, eps < 0 or not finite */
     LN_EALIGN = 2,        /* a workspace pointer that is not 256-byte aligned */
-    LN_EUNSUPPORTED = 3,  /* cols > LN_MAX_COLS, rows >= 2^31, or not an sm_103 device */
+    LN_EUNSUPPORTED = 3,  /* cols > LN_MAX_COLS, rows > LN_MAX_ROWS, or not an sm_103 device */
     LN_ECUDA = 4,         /* a CUDA runtime call failed; see ln_last_cuda_error() */
     LN_ETIMEOUT = 5,      /* a bounded device-side wait ran out (reported by ln_device_check) */
     LN_ENOSPACE = 6       /* a caller-owned workspace smaller than ln_bwd_workspace_bytes() */

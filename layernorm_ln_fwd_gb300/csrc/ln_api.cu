@@ -133,7 +133,7 @@ namespace {
 // Validation shared by all entry points; touches no CUDA state.
 ln_status check_sizes(int64_t rows, int64_t cols) {
     if (rows < 0 || cols <= 0) return LN_EINVAL;
-    if (cols > LN_MAX_COLS || rows >= (int64_t(1) << 31)) return LN_EUNSUPPORTED;
+    if (cols > LN_MAX_COLS || rows > LN_MAX_ROWS) return LN_EUNSUPPORTED;
     return LN_OK;
 }
 

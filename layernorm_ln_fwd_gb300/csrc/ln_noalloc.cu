@@ -54,7 +54,7 @@ extern "C" ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_
                                          ln_stream_t stream_) {
     using lnk::Dtype;
     if (rows < 0 || cols <= 0) return LN_EINVAL;
-    if (cols > LN_MAX_COLS || rows >= (int64_t(1) << 31)) return LN_EUNSUPPORTED;
+    if (cols > LN_MAX_COLS || rows > LN_MAX_ROWS) return LN_EUNSUPPORTED;
     if (!dgamma || !dbeta) return LN_EINVAL;
     if (rows > 0 && (!dy || !x_or_res_out || !gamma || !mean || !rstd || !dx)) return LN_EINVAL;
     int dev = -1;
