@@ -35,6 +35,9 @@
  *    forward; for the backward it writes dgamma = dbeta = 0.  With rows == 0 the pointers
  *    to [rows, cols] and [rows] arrays may be NULL (empty tensors often have no storage).
  *    eps must be finite and >= 0.
+ *  - Kernels are launched with programmatic dependent launch allowed (and the backward
+ *    cooperatively).  Each kernel still waits for the work before it in the stream to finish
+ *    before it touches memory, so stream order is the usual one, in CUDA graphs too.
  *  - Thread safety: entry points may be called from several host threads.  Two backward
  *    calls that share a workspace (the same stream, or the same caller-owned workspace) must
  *    not overlap on the GPU; stream order takes care of that for one stream.
@@ -111,10 +114,11 @@ ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma
  * The two row sums are taken in one reduction (HW4 form, "Training with LightSeq2",
  * section 2.2).  dgamma and dbeta are reduced in two deterministic stages without float
  * atomics (section 2.4; the last-block-finishes scheme of "llm.c: the llmc/ CUDA kernel
- * layer", section 3.3): each thread block writes compensated fp32 partial column sums over
- * a fixed range of rows to a workspace, an integer counter elects the blocks that arrive
- * last, and they add the partials of every block in block order.  The result is bitwise
- * identical from run to run on the same device and build.
+ * layer", section 3.3): each thread block writes fp32 partial column sums over a fixed range
+ * of rows to a workspace (compensated, as (hi, lo) pairs, for fp32 I/O), then increments an
+ * integer counter; the blocks that own a slice of the columns wait for the counter to reach
+ * the block count and add the partials of every block in a fixed order.  The result is
+ * bitwise identical from run to run on the same device and build.
  *
  * This variant uses a workspace owned by the library, one per (device, stream), allocated
  * with cudaMalloc on first use and grown when a larger problem arrives; ln_release() frees
