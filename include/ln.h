@@ -191,7 +191,9 @@ ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_res_out,
  * faulting.  ln_device_check synchronizes ``stream``, reads and clears that word on the
  * current device, re-zeroes the library-owned workspace of ``stream``, and returns LN_OK or
  * LN_ETIMEOUT (LN_ECUDA if the synchronization itself fails).  Setting the environment
- * variable LN_CHECK=1 makes every entry point do this before returning.
+ * variable LN_CHECK=1 makes every entry point do this before returning
+ * (except for calls made while their stream is being captured into a CUDA graph, which cannot
+ * synchronise).
  */
 ln_status ln_device_check(ln_stream_t stream);
 

@@ -160,7 +160,12 @@ ln_status finish_call(cudaError_t e, int launches, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
-    if (check_mode()) return ln_device_check(reinterpret_cast<ln_stream_t>(stream));
+    if (check_mode()) {
+        // Check mode synchronises, which a stream being captured into a graph cannot do.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+            return ln_device_check(reinterpret_cast<ln_stream_t>(stream));
+    }
     return LN_OK;
 }
 

@@ -4,6 +4,8 @@ Small shapes run the oracle on every element; the five full-size workloads compa
 rows element by element and dgamma/dbeta over all rows, in the launch configuration the
 benchmark uses.  Tolerances are stated in ``lnparity``.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -217,8 +219,14 @@ def test_bounded_wait_reports_timeout_and_recovers():
     try:
         d = P.to_device(inp)
         out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS)
-        ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
-        assert ln.device_check() == 5
+        if os.environ.get("LN_CHECK", "0") not in ("", "0"):
+            # Check mode synchronises after every call, so the call itself reports it.
+            with pytest.raises(ln.LnError) as e:
+                ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
+            assert e.value.status == 5
+        else:
+            ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
+            assert ln.device_check() == 5
     finally:
         L.ln_debug_wait_test(0)
     assert ln.device_check() == 0
