@@ -389,6 +389,33 @@ def run_ours(args):
         us = reps_us[2]
         kern[name] = {"us_per_launch": us, "algorithmic_bytes": nb, "gbs": nb / us / 1e3,
                       "repeats_us": [round(v, 3) for v in reps_us], "launches_per_repeat": nk}
+    # ---- torch elementwise kernels moving the same bytes, for scale at this size: the
+    # forward's 2 reads + 2 writes as two copies, the backward's 2 reads + 1 write as an add
+    # (same buffer rotation, same graph timing; not part of the hot path) ----
+    def ref_fwd(i):
+        S = sets[i % nsets]
+        S["out"].copy_(S["x"])
+        S["dx"].copy_(S["res"])
+
+    def ref_bwd(i):
+        S = sets[(i + nsets // 2) % nsets]
+        torch.add(S["dy"], S["res_out"], out=S["dx"])
+
+    same_bytes = {}
+    for name, fn, nb in (("fwd", ref_fwd, fwd_bytes(R, C, s)), ("bwd", ref_bwd, bwd_bytes(R, C, s))):
+        g = capture(fn, nk, 0)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            ev[0].record(stream)
+            for r in range(5):
+                g.replay()
+                ev[r + 1].record(stream)
+        torch.cuda.synchronize()
+        us = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / nk for r in range(5))[2]
+        same_bytes[name] = {"us": us, "gbs": nb / us / 1e3,
+                            "kernel": "2 x torch copy_" if name == "fwd" else "torch.add"}
     sampler.stop()
 
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
@@ -462,6 +489,7 @@ def run_ours(args):
         "rows_per_s": world * R * args.steps / (ms_total * 1e-3),
         "frac_of_8tbs": value / world / ROOFLINE_NOMINAL_GBS,
         "kernels": kern,
+        "same_bytes_torch": same_bytes,
         "clocks": clocks,
         "e2e": {"value": world * step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
