@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cols = a.cols, nvec = cols / V, stages = a.stages, rows = a.rows;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
     const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
     const unsigned slot_bytes = 2u * tile_bytes;
@@ -434,8 +434,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             f2 mg2[NR], mgx2[NR];
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                mg2[r] = f2_splat(t[2 * r] / fcols);
-                mgx2[r] = f2_splat(t[2 * r + 1] / fcols);
+                mg2[r] = f2_splat(rdiv.div(t[2 * r]));
+                mgx2[r] = f2_splat(rdiv.div(t[2 * r + 1]));
             }
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthreads = blockDim.x, nw = nthreads >> 5;
     const int cols = a.cols, nvec = cols / V, stages = a.stages;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
     const unsigned slot_bytes = 2u * row_bytes;
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
@@ -719,7 +719,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
             tg += red[0][w];
             tgx += red[1][w];
         }
-        const f2 mg2 = f2_splat(tg / fcols), mgx2 = f2_splat(tgx / fcols);
+        const f2 mg2 = f2_splat(rdiv.div(tg)), mgx2 = f2_splat(rdiv.div(tgx));
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
@@ -797,7 +797,7 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
     __shared__ float red[2][NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cols = a.cols, P = gridDim.x;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
     const T* __restrict__ xr = static_cast<const T*>(a.xr);
     const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
@@ -841,7 +841,7 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
             tg += red[0][w];
             tgx += red[1][w];
         }
-        const float mg = tg / fcols, mgx = tgx / fcols;
+        const float mg = rdiv.div(tg), mgx = rdiv.div(tgx);
         for (int j = tid; j < cols; j += kBwdScalarThreads) {
             const float d = IO::to_f(dy[base + j]);
             const float xh = (IO::to_f(xr[base + j]) - mu) * rs;

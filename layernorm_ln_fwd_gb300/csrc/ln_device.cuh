@@ -208,6 +208,21 @@ __device__ __forceinline__ void warp_sum2(float& a, float& b) {
     }
 }
 
+// Division by the row length without a division per row: with inv = 1/n rounded once per
+// kernel, q0 = a * inv rounded, the residual r = a - q0 * n exact in one fma, and one
+// correction q = q0 + r * inv give the correctly rounded a / n (Markstein's correction; see
+// Muller et al., "Handbook of Floating-Point Arithmetic", on Markstein's theorem), i.e. the
+// bits a division would give, in three instructions.
+struct RowDivisor {
+    float n, inv;
+    __device__ explicit RowDivisor(int cols) : n((float)cols), inv(1.0f / (float)cols) {}
+    __device__ __forceinline__ float div(float a) const {
+        const float q = __fmul_rn(a, inv);
+        const float r = __fmaf_rn(-q, n, a);
+        return __fmaf_rn(r, inv, q);
+    }
+};
+
 // The shift of a row for its shifted sums: the mean of the row's first vector (its first 4
 // fp32 or 8 bf16 stored values), rounded to the I/O type.  It lies within about a third of a
 // standard deviation of the row's mean, so sum d^2/n - (sum d/n)^2 with d = s - K loses

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nvec = cols / V;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
     const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
     const unsigned slot_bytes = (HAS_RES ? 2u : 1u) * tile_bytes;
@@ -167,9 +167,9 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
             }
             float sd = f2_lo(a) + f2_hi(a), sd2 = f2_lo(q) + f2_hi(q);
             warp_sum2(sd, sd2);  // the one reduction of the row
-            const float md = sd / fcols;
-            const float var = fmaxf(sd2 / fcols - md * md, 0.f);
-            const float rs = 1.0f / sqrtf(var + eps);
+            const float md = rdiv.div(sd);
+            const float var = fmaxf(rdiv.div(sd2) - md * md, 0.f);
+            const float rs = rsqrtf(var + eps);
             if (lane == 0) {
                 mean[row] = f2_lo(K2) + md;
                 rstd[row] = rs;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
     const unsigned nin = HAS_RES ? 2u : 1u;
     const unsigned slot_bytes = nin * row_bytes;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
 
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) mbar_init(&full_bar[i], 1);
@@ -310,9 +310,9 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
             sd += red[0][w];
             sd2 += red[1][w];
         }
-        const float md = sd / fcols;
-        const float var = fmaxf(sd2 / fcols - md * md, 0.f);
-        const float rs = 1.0f / sqrtf(var + eps);
+        const float md = rdiv.div(sd);
+        const float var = fmaxf(rdiv.div(sd2) - md * md, 0.f);
+        const float rs = rsqrtf(var + eps);
         if (tid == 0) {
             mean[row] = f2_lo(K2) + md;
             rstd[row] = rs;
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
     constexpr int NW = kFwdScalarThreads / 32;
     __shared__ float red[4][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float fcols = (float)cols;
+    const RowDivisor rdiv(cols);
     const bool write_res = res_out != nullptr;
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * cols;
@@ -398,8 +398,8 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
         }
         __syncthreads();
         st = block_stats(red, NW);
-        const float md = __fdiv_rn(__fadd_rn(st.s, st.c), fcols);
-        const float rs = 1.0f / sqrtf(st.q / fcols + eps);
+        const float md = rdiv.div(__fadd_rn(st.s, st.c));
+        const float rs = rsqrtf(rdiv.div(st.q) + eps);
         if (tid == 0) {
             mean[row] = K + md;
             rstd[row] = rs;
