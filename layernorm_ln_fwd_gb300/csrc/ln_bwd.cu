@@ -426,9 +426,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                 t[2 * r + 1] = f2_lo(sgx[r]) + f2_hi(sgx[r]);
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int i = 0; i < 2 * NR; ++i) t[i] += __shfl_xor_sync(kFullMask, t[i], o);
+            for (int r = 0; r < NR; ++r) warp_sum2(t[2 * r], t[2 * r + 1]);
             // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
             // g - mg cancels exactly where it should (a one-column row gives dx = 0).
             f2 mg2[NR], mgx2[NR];

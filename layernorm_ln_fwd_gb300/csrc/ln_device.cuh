@@ -201,11 +201,13 @@ __device__ __forceinline__ void st_stream(void* p, const uint4& v) {
 // lanes of a pair add the same two operands, and fp32 addition is commutative.
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void warp_sum2(float& a, float& b) {
+    f2 v = f2_make(a, b);  // both sums added as one fp32 pair per step
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(kFullMask, a, o);
-        b += __shfl_xor_sync(kFullMask, b, o);
-    }
+    for (int o = 16; o > 0; o >>= 1)
+        v = f2_add(v, f2_make(__shfl_xor_sync(kFullMask, f2_lo(v), o),
+                              __shfl_xor_sync(kFullMask, f2_hi(v), o)));
+    a = f2_lo(v);
+    b = f2_hi(v);
 }
 
 // Division by the row length without a division per row: with inv = 1/n rounded once per
@@ -223,20 +225,17 @@ struct RowDivisor {
     }
 };
 
-// The shift of a row for its shifted sums: the mean of the row's first vector (its first 4
-// fp32 or 8 bf16 stored values), rounded to the I/O type.  It lies within about a third of a
-// standard deviation of the row's mean, so sum d^2/n - (sum d/n)^2 with d = s - K loses
-// almost nothing to cancellation, and for bf16 every d is exact.
+// The shift of a row for its shifted sums: the row's first stored value, K.  Every d = s - K
+// of a bf16 row is exact, and for any row sum d^2 / n = var + (mean - K)^2 with K a draw of
+// the row's own values, so var = sum d^2 / n - (sum d / n)^2 keeps all but about one bit
+// (the cancellation E[x^2] - E[x]^2 suffers is from the mean, not the spread).
 template <typename T>
 __device__ __forceinline__ float row_shift(const uint4& first) {
-    float f[Io<T>::kVec];
-    Io<T>::unpack(first, f);
-    float k = 0.f;
-#pragma unroll
-    for (int i = 0; i < Io<T>::kVec; ++i) k += f[i];
-    return Io<T>::round(k * (1.0f / Io<T>::kVec));
+    if constexpr (Io<T>::kVec == 8)
+        return __uint_as_float(first.x << 16);  // the low bf16 of the first word
+    else
+        return __uint_as_float(first.x);
 }
-
 // Row statistics as a mergeable summary: count n, the sum S + c of the shifted values (S and
 // its compensation c, kept error-free with TwoSum) and M2, the sum of squared deviations from
 // the group's own mean.  Two summaries merge with the pairwise update of Welford/Chan

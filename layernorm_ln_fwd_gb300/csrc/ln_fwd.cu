@@ -7,15 +7,15 @@
 //
 // Statistics in one reduction, without the cancellation of E[s^2] - E[s]^2 that breaks rows
 // whose mean dwarfs their spread ("Accelerating Transformer on GPU (I)", section 4.2):
-//  * vector kernels: shifted sums.  K = the mean of the row's first 16-byte vector, rounded
-//    to the I/O type, so d = s - K is exact for bf16 and K lies within about a third of a
-//    standard deviation of the mean; sum d and sum d^2 are reduced together (one xor
-//    butterfly, plus one cross-warp exchange for a block per row) and
-//    var = sum d^2 / n - (sum d / n)^2 then has both terms of the order of var itself;
+//  * vector kernels: shifted sums.  K = the row's first stored value, so d = s - K is exact
+//    for bf16 and sum d^2 / n exceeds the variance by (mean - K)^2, about one more variance;
+//    sum d and sum d^2 are reduced together (one xor butterfly, plus one cross-warp exchange
+//    for a block per row) and var = sum d^2 / n - (sum d / n)^2 then has both terms of the
+//    order of var itself;
 //  * scalar kernel: each thread keeps a Welford summary (count, compensated sum, M2) and the
 //    summaries are combined with the Welford/Chan pairwise merge of the same section;
 //  * xhat = d * rstd - mean(d) * rstd (one fma), which never subtracts two large numbers.
-// mean = K + mean(d) and rstd = 1 / sqrt(var + eps) are stored in fp32.
+// mean = K + mean(d) and rstd = 1 / sqrt(var + eps) (rsqrtf) are stored in fp32.
 //
 // Three kernel families compute the same function:
 //  * warp per row (rows of at most 256 vectors of 16 bytes): tiles of 7 rows are staged in
@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     sp[v] = make_uint4(0, 0, 0, 0);
                 }
             }
-            // Shifted sums: K = the mean of the row's first vector (lane 0's), rounded.  The
-            // low halves of the pairs sum the even columns, the high halves the odd ones.
+            // Shifted sums: K = the row's first stored value (lane 0's).  The low halves of
+            // the pairs sum the even columns, the high halves the odd ones.
             const f2 K2 = f2_splat(__shfl_sync(kFullMask, row_shift<T>(sp[0]), 0));
             f2 d[VPL][H];
             f2 a = f2_splat(0.f), q = f2_splat(0.f);
@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                 sp[v] = make_uint4(0, 0, 0, 0);
             }
         }
-        // Shifted sums: K = the mean of the row's first vector (every thread reads it from
-        // shared memory and computes the same bits).  The low halves of the pairs sum the
+        // Shifted sums: K = the row's first stored value (every thread reads it from shared
+        // memory).  The low halves of the pairs sum the
         // even columns, the high halves the odd ones.
         const uint4 first = HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
                                                    *reinterpret_cast<const uint4*>(rsm))
