@@ -76,9 +76,13 @@ struct KParams {
     int stages;
 };
 
-__device__ __forceinline__ void row_range(int rows, int& r0, int& r1) {
-    r0 = (int)((long long)blockIdx.x * rows / gridDim.x);
-    r1 = (int)((long long)(blockIdx.x + 1) * rows / gridDim.x);
+// This block's share [r0, r1) of n items split over the grid: the first n % G blocks take
+// one item more (32-bit arithmetic: one division, no 64-bit products).
+__device__ __forceinline__ void row_range(int n, int& r0, int& r1) {
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int q = n / G, rem = n - q * G;
+    r0 = b * q + min(b, rem);
+    r1 = r0 + q + (b < rem ? 1 : 0);
 }
 
 // (S, C) += (h, l), where a compensated value is S + C.
@@ -138,13 +142,12 @@ __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     const int ngroups = cols / U;       // units per statistic
     const int nunits = 2 * ngroups;
     const int ng = (nunits + kFinUnits - 1) / kFinUnits;
-    const int g0 = (int)((long long)f * ng / P);
-    const int g1 = (int)((long long)(f + 1) * ng / P);
+    const int g0 = f * ng / P, g1 = (f + 1) * ng / P;  // f * ng < 2^24: 32-bit is exact
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int RW = a.fin_rw, GW = nw / RW;
     const int gw = warp / RW, rw = warp - gw * RW;
     const int k = lane % kFinUnits, sub = lane / kFinUnits;
-    const int p_lo = (int)((long long)rw * P / RW), p_hi = (int)((long long)(rw + 1) * P / RW);
+    const int p_lo = rw * P / RW, p_hi = (rw + 1) * P / RW;
     const float* part = reinterpret_cast<const float*>(a.part);
     const size_t stat_stride = (size_t)P * cols * E;
     const size_t row_stride = (size_t)cols * E;
@@ -244,7 +247,7 @@ __device__ void arrive_and_finish(const KParams& a, float* scratch) {
     const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
                             : (a.cols % 2 == 0 ? 2 : 1);  // as finish_units is instantiated
     const int ng = (2 * (a.cols / U) + kFinUnits - 1) / kFinUnits;
-    const bool finisher = (long long)(f + 1) * ng / P > (long long)f * ng / P;
+    const bool finisher = (f + 1) * ng / P > f * ng / P;  // as finish_units splits the groups
     const unsigned F = (unsigned)min(P, ng);  // blocks owning at least one group
     __syncthreads();  // every thread's partial sums are written
     if (threadIdx.x == 0) {
@@ -303,7 +306,6 @@ template <typename T, int VPL, bool KAHAN>
 __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>())
     bwd_tile_kernel(const KParams a) {
     using IO = Io<T>;
-    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -329,6 +331,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
         fence_barrier_init();
     }
     __syncthreads();
+    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
+    pdl_enter();
 
     using PR = Pairs<T>;
     constexpr int H = PR::kPairs;
@@ -608,7 +612,6 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 template <typename T, int VPT, bool KAHAN>
 __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const KParams a) {
     using IO = Io<T>;
-    pdl_enter();
     constexpr int V = IO::kVec;
     constexpr int MAXW = kBwdBlockMaxThreads / 32;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -634,6 +637,8 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         fence_barrier_init();
     }
     __syncthreads();
+    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
+    pdl_enter();
     auto issue = [&](int k, int slot) {  // thread 0 only: fetch row r0 + k into `slot`
         const int row = r0 + k;
         if (row >= r1) return;

@@ -405,10 +405,11 @@ struct RingPos {
 };
 
 // Programmatic dependent launch (the kernels are launched with programmatic stream
-// serialization allowed).  At entry a kernel waits until the grid before it in the stream has
-// completed and its memory is visible (a no-op when there is none), then lets the grid after
-// it begin launching: that grid's blocks take SMs as this grid's blocks leave and do their
-// own set-up, but they too wait here before touching memory, so stream order holds.
+// serialization allowed).  Before its first access to global memory (its shared-memory
+// set-up may come first) a kernel waits until the grid before it in the stream has completed
+// and its memory is visible (a no-op when there is none), then lets the grid after it begin
+// launching: that grid's blocks take SMs as this grid's blocks leave and do their own set-up,
+// but they too wait here before touching global memory, so stream order holds.
 __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

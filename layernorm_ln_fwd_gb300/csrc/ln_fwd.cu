@@ -61,7 +61,6 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     float* __restrict__ mean, float* __restrict__ rstd, int stages,
                     unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
-    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
@@ -82,6 +81,8 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
         fence_barrier_init();
     }
     __syncthreads();
+    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
+    pdl_enter();
 
     if (warp == kTileRows) {  // producer
         if (lane == 0) {
@@ -208,7 +209,6 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                      float* __restrict__ mean, float* __restrict__ rstd, int stages,
                      unsigned* status, uint64_t wait_limit_ns) {
     using IO = Io<T>;
-    pdl_enter();
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages];
@@ -229,6 +229,8 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         fence_barrier_init();
     }
     __syncthreads();
+    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
+    pdl_enter();
 
     auto issue = [&](int k, int slot) {  // thread 0 only: fetch the k-th row of this block
         const int row = blockIdx.x + k * gridDim.x;
