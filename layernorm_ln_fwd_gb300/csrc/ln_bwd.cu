@@ -961,14 +961,18 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
             p.kahan = wk;
             const size_t slot = 2ull * kTileRows * cols * esize;  // a tile of dy and of x
             const size_t combine = (wk ? 4ull : 2ull) * kTileRows * cols * 4;
-            // As many tiles in flight as the block's share of the SM's shared memory holds,
-            // at the number of blocks per SM the registers allow.
+            // About four tiles in flight per SM, split over the blocks the registers allow
+            // on an SM, within each block's share of its shared memory.  Measured on GB300:
+            // deeper rings request a block's whole share of rows at once, the DRAM queue then
+            // serves blocks roughly in launch order and the late ones set the kernel's end
+            // (bf16 8192x768, two blocks per SM: 5 stages 14.2 us, 2 stages 13.5 us; bf16
+            // 8192x1280, one block per SM: 6 stages 18.8 us, 4 stages 18.5 us, 2 stages 19.4 us).
             const void* kern = kernel_for(dt, p);
             if (!kern) return cudaErrorInvalidValue;
             const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
             const size_t share = std::min<size_t>(
                 (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
-            int stages = (int)std::min<size_t>(kMaxStages, share / slot);
+            int stages = (int)std::min<size_t>(std::min(kMaxStages, 4 / occ_regs), share / slot);
             stages = std::max(2, stages);
             p.stages = stages;
             // The ring, reused afterwards for the warps' sums.
