@@ -53,8 +53,9 @@ extern "C" {
 #endif
 
 #define LN_MAX_COLS 16384
-/* Largest row count: row indices, rounded up to whole 7-row tiles, stay within int range. */
-#define LN_MAX_ROWS 2147483583LL
+/* Largest row count (2^31 - 2^16): row indices, including a block's look-ahead of a tile
+   step past its last, stay within int range. */
+#define LN_MAX_ROWS 2147418112LL
 
 /* The raw bits of one bfloat16 value. */
 typedef uint16_t ln_bf16;

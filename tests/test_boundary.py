@@ -74,9 +74,9 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.ln_fwd_f32(p, NULL, p, p, float("inf"), 4, 4, p, NULL, p, p, NULL) == 1
     assert lib.ln_fwd_f32(p, NULL, p, p, 1e-5, 4, ln.MAX_COLS + 1, p, NULL, p, p, NULL) == 3
     assert lib.ln_fwd_bf16(p, NULL, p, p, 1e-5, 1 << 31, 8, p, NULL, p, p, NULL) == 3
-    # LN_MAX_ROWS = 2^31 - 65: one more row is refused (tile indices must stay in int range).
-    assert lib.ln_fwd_bf16(p, NULL, p, p, 1e-5, 2**31 - 64, 8, p, NULL, p, p, NULL) == 3
-    assert lib.ln_bwd_bf16(p, p, p, p, p, p, p, p, 2**31 - 64, 8, NULL) == 3
+    # LN_MAX_ROWS = 2^31 - 2^16: one more row is refused (row indices must stay in int range).
+    assert lib.ln_fwd_bf16(p, NULL, p, p, 1e-5, 2**31 - 2**16 + 1, 8, p, NULL, p, p, NULL) == 3
+    assert lib.ln_bwd_bf16(p, p, p, p, p, p, p, p, 2**31 - 2**16 + 1, 8, NULL) == 3
     assert lib.ln_bwd_f32(p, p, p, p, p, p, p, p, 4, ln.MAX_COLS + 1, NULL) == 3
     # rows == 0 is a forward no-op, needs no device, and accepts NULL row arrays.
     assert lib.ln_fwd_f32(p, NULL, p, p, 1e-5, 0, 4, p, NULL, p, p, NULL) == 0
