@@ -11,8 +11,8 @@
 // near-constant values) any difference between them would be amplified into dx.
 //
 // Column sums, deterministic and without float atomics, in two stages:
-//  1. Each block owns a FIXED set of rows (a contiguous range, or every G-th 7-row tile for
-//     the warp-per-row kernel).  While it computes dx it
+//  1. Each block owns a FIXED set of rows (every G-th row or 7-row tile; a contiguous range
+//     in the scalar kernel).  While it computes dx it
 //     accumulates dy * xhat and dy for the columns its threads own and, at the end, writes
 //     one row of partial sums per statistic to the workspace: part[stat][block][col].
 //  2. Every block then increments an integer arrival counter (atomicAdd).  The blocks that
@@ -634,8 +634,9 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     const T* __restrict__ xr = static_cast<const T*>(a.xr);
     const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
     T* __restrict__ dx = static_cast<T*>(a.dx);
-    int r0, r1;
-    row_range(a.rows, r0, r1);
+    // This block's rows: b, b + G, b + 2G, ... (G blocks), interleaved as in the tile kernel.
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int nmy = b < a.rows ? (a.rows - 1 - b) / G + 1 : 0;
 
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) mbar_init(&full_bar[i], 1);
@@ -645,9 +646,9 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     __syncthreads();
     // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
     pdl_enter();
-    auto issue = [&](int k, int slot) {  // thread 0 only: fetch row r0 + k into `slot`
-        const int row = r0 + k;
-        if (row >= r1) return;
+    auto issue = [&](int k, int slot) {  // thread 0 only: fetch the block's k-th row into `slot`
+        if (k >= nmy) return;
+        const int row = b + k * G;
         unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
         mbar_arrive_expect_tx(&full_bar[slot], slot_bytes);
         bulk_g2s(dst, dy + (size_t)row * cols, row_bytes, &full_bar[slot]);
@@ -676,14 +677,14 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
 
     int k = 0;
     // mean and rstd are loaded one row ahead (off the row's critical path).
-    float mu_next = r0 < r1 ? a.mean[r0] : 0.f, rs_next = r0 < r1 ? a.rstd[r0] : 0.f;
+    float mu_next = nmy > 0 ? a.mean[b] : 0.f, rs_next = nmy > 0 ? a.rstd[b] : 0.f;
     RingPos pos;
-    for (int row = r0; row < r1; ++row, ++k, pos.next(stages)) {
+    for (int row = b; k < nmy; row += G, ++k, pos.next(stages)) {
         const int slot = pos.slot;
         const float mu = mu_next, rs = rs_next;
-        if (row + 1 < r1) {
-            mu_next = a.mean[row + 1];
-            rs_next = a.rstd[row + 1];
+        if (k + 1 < nmy) {
+            mu_next = a.mean[row + G];
+            rs_next = a.rstd[row + G];
         }
         if (!mbar_wait(&full_bar[slot], pos.phase, a.limit_ns)) abort_flag = 1;
         const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
@@ -752,7 +753,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
     if (abort_flag) {
         if (tid == 0) {
             raise_status(a.status, kStatusTimeout);
-            for (int j = k; j < k + stages && r0 + j < r1; ++j)
+            for (int j = k; j < k + stages && j < nmy; ++j)
                 (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
         }
         __syncthreads();
