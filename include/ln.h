@@ -115,11 +115,12 @@ ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma
  * The two row sums are taken in one reduction (HW4 form, "Training with LightSeq2",
  * section 2.2).  dgamma and dbeta are reduced in two deterministic stages without float
  * atomics (section 2.4; the last-block-finishes scheme of "llm.c: the llmc/ CUDA kernel
- * layer", section 3.3): each thread block writes fp32 partial column sums over a fixed range
- * of rows to a workspace (compensated, as (hi, lo) pairs, for fp32 I/O), then increments an
- * integer counter; the blocks that own a slice of the columns wait for the counter to reach
- * the block count and add the partials of every block in a fixed order.  The result is
- * bitwise identical from run to run on the same device and build.
+ * layer", section 3.3): each thread block writes fp32 partial column sums over a fixed set
+ * of rows to a workspace (compensated, as (hi, lo) pairs, for fp32 I/O); the blocks that own
+ * a slice of the columns read every block's partials of that slice as they land (a stored
+ * partial is never the all-zero word, and the workspace is all zero between calls, so a zero
+ * word is one not yet written), add them in a fixed order, and zero the words they read.
+ * The result is bitwise identical from run to run on the same device and build.
  *
  * This variant uses a workspace owned by the library, one per (device, stream), allocated
  * with cudaMalloc on first use and grown when a larger problem arrives; ln_release() frees
@@ -145,9 +146,10 @@ size_t ln_bwd_workspace_bytes(int64_t rows, int64_t cols);
 /*
  * Backward with a caller-owned device workspace (256-byte aligned, at least
  * ln_bwd_workspace_bytes(rows, cols) bytes).  The caller must zero the whole workspace once
- * before its first use; every call leaves its counters at zero again, so it can be reused
- * by later calls in stream order without clearing.  After LN_ETIMEOUT it must be zeroed
- * again.  Nothing is allocated.
+ * before its first use; every completed call leaves it all zero again, so it can be reused
+ * by later calls in stream order (of any shape that fits) without clearing.  After
+ * LN_ETIMEOUT it must be zeroed again: a call that gave up may leave partial sums in it.
+ * Nothing is allocated.
  * Errors: as ln_bwd_*, plus LN_EALIGN and LN_ENOSPACE.
  */
 ln_status ln_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
@@ -165,17 +167,18 @@ ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const l
  * point: it exists for callers that cannot call cudaMalloc when they run the backward --
  * a serving process that reserved its whole device-memory budget at start-up, or a plugin
  * whose host framework owns every device allocation -- and cannot hand in a workspace
- * either.  Arguments, results and errors are those of ln_bwd_bf16; the scratch (counters
- * and per-block partial sums) lives in a fixed array of LN_NOALLOC_SCRATCH_BYTES (16 MiB)
+ * either.  Arguments, results and errors are those of ln_bwd_bf16; the scratch (the
+ * per-block partial sums) lives in a fixed array of LN_NOALLOC_SCRATCH_BYTES (16 MiB)
  * compiled into the library, which every GPU that loads the library holds until exit.
  *  - Problems whose scratch would exceed that size are rejected with LN_EUNSUPPORTED
  *    (roughly: 16 * cols * min(rows, 8 * SM count) + 256 bytes must fit; 8192 x 768 and
  *    8192 x 1280 do, 4096 x 8192 does not).
  *  - The first call on each device looks up the array's device address (once, with that
  *    device current); make that first call before any stream capture begins.
- *  - All calls share the one array, and each call first clears its counters on `stream`:
- *    calls whose work overlaps on the GPU (different streams, or different host threads
- *    without ordering) race and corrupt each other's results; order them.
+ *  - All calls share the one array, which every completed call leaves all zero (after
+ *    LN_ETIMEOUT, ln_device_check zeroes it): calls whose work overlaps on the GPU
+ *    (different streams, or different host threads without ordering) race and corrupt each
+ *    other's results; order them.
  *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  */
 #define LN_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -186,8 +189,8 @@ ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_res_out,
                               int64_t cols, ln_stream_t stream);
 
 /*
- * Device-side status.  Every wait inside a kernel (the bulk-copy barrier of the wide-row
- * kernels, the backward's wait for the last blocks) is bounded; when one runs out the
+ * Device-side status.  Every wait inside a kernel (the bulk-copy barriers, the backward's
+ * polls for other blocks' partial sums) is bounded; when one runs out the
  * kernel records LN_ETIMEOUT in a per-device status word and returns early without
  * faulting.  ln_device_check synchronizes ``stream``, reads and clears that word on the
  * current device, re-zeroes the library-owned workspace of ``stream``, and returns LN_OK or
@@ -219,9 +222,10 @@ int ln_version(void);
  * the row does not fit), 2 = block per row with bulk-copy (TMA) staging, 3 = scalar
  * kernels.  Returns the previous setting.
  *
- * ln_debug_wait_test makes the next backward launches wait for one block more than exists,
- * with a wait limit of ``limit_us`` microseconds, so that the bounded wait runs out and
- * LN_ETIMEOUT is reported by ln_device_check; 0 turns it off.  Used by the test of the
+ * ln_debug_wait_test makes the finishing blocks of the next backward launches also wait for
+ * a workspace word that nothing writes, with a wait limit of ``limit_us`` microseconds, so
+ * that the bounded wait runs out and LN_ETIMEOUT is reported by ln_device_check; 0 turns it
+ * off.  Used by the test of the
  * timeout path; it never faults the device.
  */
 int ln_debug_force_path(int path);

@@ -228,7 +228,7 @@ ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const flo
     BwdPlan plan;
     cudaError_t e = plan_bwd(dt, (int)rows, (int)cols, aligned, g_force_path.load(), &plan);
     if (e != cudaSuccess) return cuda_fail(e);
-    const size_t need = bwd_workspace_bytes(plan.grid, (int)cols);
+    const size_t need = bwd_workspace_bytes(plan.grid, (int)cols, bwd_plan_acc_region(plan));
     if (own_ws) {
         const int dev = current_device();
         std::lock_guard<std::mutex> lk(g_mu);
@@ -247,7 +247,7 @@ ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const flo
                 return cuda_fail(e);
             }
             w.bytes = need;
-            e = cudaMemsetAsync(w.ptr, 0, kWorkspaceHeader, stream);
+            e = cudaMemsetAsync(w.ptr, 0, need, stream);  // zero between calls, from the start
             if (e != cudaSuccess) return cuda_fail(e);
         }
         ws = w.ptr;
@@ -325,7 +325,8 @@ size_t ln_bwd_workspace_bytes(int64_t rows, int64_t cols) {
     const lnk::DeviceInfo& di = lnk::device_info(dev);
     if (di.sms <= 0) return 0;
     return lnk::bwd_workspace_bytes(lnk::bwd_max_grid((int)std::max<int64_t>(rows, 1), di.sms),
-                                    (int)cols);
+                                    (int)cols,
+                                    !lnk::bwd_scalar_acc_in_smem((int)cols, (size_t)di.smem_optin));
 }
 
 ln_status ln_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
@@ -361,16 +362,20 @@ ln_status ln_device_check(ln_stream_t stream_) {
     const unsigned zero = 0;
     e = cudaMemcpy(sw, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return lnk::cuda_fail(e);
-    // A backward that gave up may have left its counters non-zero: clear this stream's one.
+    // A backward that gave up may have left partial sums in its workspace, where the next
+    // call would take them for its own: clear this stream's workspace and the fixed scratch
+    // of the allocation-free entry point.
     {
         const int dev = lnk::current_device();
         std::lock_guard<std::mutex> lk(lnk::g_mu);
         auto it = lnk::g_workspaces.find(std::make_pair(dev, stream));
         if (it != lnk::g_workspaces.end() && it->second.ptr) {
-            e = cudaMemset(it->second.ptr, 0, lnk::kWorkspaceHeader);
+            e = cudaMemset(it->second.ptr, 0, it->second.bytes);
             if (e != cudaSuccess) return lnk::cuda_fail(e);
         }
     }
+    e = lnk::noalloc_scratch_clear();
+    if (e != cudaSuccess) return lnk::cuda_fail(e);
     return (word & lnk::kStatusTimeout) ? LN_ETIMEOUT : LN_OK;
 }
 

@@ -15,14 +15,16 @@
 //     in the scalar kernel).  While it computes dx it
 //     accumulates dy * xhat and dy for the columns its threads own and, at the end, writes
 //     one row of partial sums per statistic to the workspace: part[stat][block][col].
-//  2. Every block then increments an integer arrival counter (atomicAdd).  The blocks that
-//     own a slice of the columns wait (bounded) until all blocks have arrived, sum the
-//     partials of their slice over blocks in a fixed order and write dgamma and dbeta; the
-//     others leave.  The finishing block last past the wait puts the counters back to 0.
+//  2. The blocks that own a slice of the columns then read every block's partials of their
+//     slice, add them over blocks in a fixed order and write dgamma and dbeta; the others
+//     leave.  A partial announces itself: the workspace words are zero between calls and a
+//     stored partial never is (see part_enc), so a reader polls, bounded, only the words it
+//     is still missing -- no fence, arrival counter or grid-wide wait -- and zeroes what it
+//     has read for the next call.
 //  This is the last-block-finishes idea of llm.c's layernorm_backward_kernel10 ("llm.c: the
 //  llmc/ CUDA kernel layer", section 3.3), widened from one finishing block to many so that
 //  the finish is spread over SMs instead of serialising one SM on all partials.  The grid
-//  is launched cooperatively, so every block is resident and the wait always ends.  Which
+//  is launched cooperatively, so every block is resident and the polls always end.  Which
 //  block adds which rows, and in what order, depends only on (rows, cols, device), so
 //  dgamma and dbeta are bitwise reproducible run to run.
 //
@@ -36,6 +38,7 @@
 // bf16 results over short chains plain fp32 sums are far more accurate than the bf16 unit
 // in the last place, and the partials are stored and added plainly.
 #include <algorithm>
+#include <climits>
 #include <type_traits>
 
 #include "ln_device.cuh"
@@ -68,9 +71,10 @@ struct KParams {
     int rows;
     int cols;
     float2* part;  // [2][gridDim.x][cols] (hi, lo) pairs, or plain fp32 sums when compact
+    float2* acc;   // scalar kernel, rows too wide for shared memory: its running (hi, lo) sums
     int compact;   // partials without the lo half (kernels whose column sums are plain)
     int fin_rw;    // warps per unit group in the finish (divides the block's warp count)
-    unsigned* ctr;
+    unsigned* ctr;  // a zero word nothing writes (the bounded-wait test polls it)
     unsigned* status;
     uint64_t limit_ns;
     unsigned wait_extra;
@@ -124,6 +128,10 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 // touches kFinSub lines); the kFinSub lane totals are folded by a fixed shuffle tree, and
 // the RW warp totals are added in warp order through shared memory.  The order depends
 // only on P, RW and the unit.
+// A loaded unit with a zero word belongs to a block that has not written its partials yet:
+// one lane of the warp watches a single word of the earliest such row, the lanes then reload
+// what they miss, until nothing is missing or the time limit passes; then each lane zeroes
+// the units it read and adds them.
 // Compensated partials are added with TwoSum; COMPACT partials (plain fp32 sums from
 // kernels with bf16 results) with plain fp32 additions: their error, about 2^-24 * sqrt(P)
 // times the partials' size, is far below a bf16 unit in the last place.
@@ -131,14 +139,34 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 // ---------------------------------------------------------------------------------------
 constexpr int kFinUnits = 8;
 constexpr int kFinSub = 32 / kFinUnits;
-constexpr int kFinBatch = 48;  // floats of partials a lane loads per batch
+constexpr int kFinBatch = 48;  // at most this many words of partials per lane and batch,
+constexpr int kFinMaxRows = 12;  // from at most this many partial rows
+__host__ __device__ constexpr int fin_rows_per_lane(int words_per_unit) {
+    return kFinBatch / words_per_unit < kFinMaxRows ? kFinBatch / words_per_unit : kFinMaxRows;
+}
+
+// The same pointer, opaque to the compiler (so values derived from it are recomputed, not
+// kept live from an earlier computation).
+template <typename P>
+__device__ __forceinline__ P* opaque(P* p) {
+    asm volatile("" : "+l"(p));
+    return p;
+}
+
+template <int N>
+__device__ __forceinline__ bool has_zero(const uint32_t (&w)[N]) {
+    bool z = false;
+#pragma unroll
+    for (int i = 0; i < N; ++i) z |= w[i] == 0u;
+    return z;
+}
 
 template <typename T, int U, bool COMPACT>
 __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     using IO = Io<T>;
     constexpr int E = COMPACT ? 1 : 2;  // floats per column of a partial
-    constexpr int W = E * U;            // floats per unit of a partial row: 1, 2 or 4
-    constexpr int L = kFinBatch / W;    // partial rows one lane loads per batch
+    constexpr int W = E * U;            // words per unit of a partial row: 1, 2 or 4
+    constexpr int L = fin_rows_per_lane(W);  // partial rows one lane loads per batch
     const int cols = a.cols;
     const int ngroups = cols / U;       // units per statistic
     const int nunits = 2 * ngroups;
@@ -149,45 +177,88 @@ __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
     const int gw = warp / RW, rw = warp - gw * RW;
     const int k = lane % kFinUnits, sub = lane / kFinUnits;
     const int p_lo = rw * P / RW, p_hi = (rw + 1) * P / RW;
-    const float* part = reinterpret_cast<const float*>(a.part);
+    uint32_t* part = reinterpret_cast<uint32_t*>(a.part);
     const size_t stat_stride = (size_t)P * cols * E;
     const size_t row_stride = (size_t)cols * E;
+    bool late = false;  // a partial did not arrive within the time limit
     for (int gb = g0; gb < g1; gb += GW) {  // block-uniform
         const int gi = gb + gw;
         const int u = gi * kFinUnits + k;
-        const bool act = gi < g1 && u < nunits;
+        const bool grp_ok = gi < g1;  // the same in the whole warp
+        const bool act = grp_ok && u < nunits;
         const int stat = u >= ngroups ? 1 : 0, grp = u - stat * ngroups;
         float S[U], C[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-        if (act) {
-            const float* src = part + stat * stat_stride + (size_t)grp * W;
-            for (int p0 = p_lo + sub; p0 < p_hi; p0 += kFinSub * L) {
-                float v[L][W];
+        if (grp_ok) {
+            uint32_t* src = part + stat * stat_stride + (size_t)grp * W;
+            const size_t step = (size_t)kFinSub * row_stride;  // between a lane's rows
+            for (int pb = p_lo; pb < p_hi; pb += kFinSub * L) {  // the same trips in the warp
+                const int p0 = pb + sub;
+                const int nj = act && p0 < p_hi ? (p_hi - p0 + kFinSub - 1) / kFinSub : 0;
+                uint32_t* q0 = src + (size_t)p0 * row_stride;
+                uint32_t v[L][W];
 #pragma unroll
                 for (int j = 0; j < L; ++j) {
-                    const int p = p0 + j * kFinSub;
-                    const float* q = src + (size_t)p * row_stride;
-                    if constexpr (W == 4) {
-                        const float4 w = p < p_hi ? __ldcg(reinterpret_cast<const float4*>(q))
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                        v[j][0] = w.x; v[j][1] = w.y; v[j][2] = w.z; v[j][3] = w.w;
-                    } else if constexpr (W == 2) {
-                        const float2 w = p < p_hi ? __ldcg(reinterpret_cast<const float2*>(q))
-                                                  : make_float2(0.f, 0.f);
-                        v[j][0] = w.x; v[j][1] = w.y;
+                    if (j < nj) {
+                        ld_part<W>(q0 + j * step, v[j]);
                     } else {
-                        v[j][0] = p < p_hi ? __ldcg(q) : 0.f;
+#pragma unroll
+                        for (int i = 0; i < W; ++i) v[j][i] = ~0u;  // reads as +0
                     }
                 }
+                unsigned miss = 0;  // bit j: row j of this lane's batch is not all there
+#pragma unroll
+                for (int j = 0; j < L; ++j) miss |= has_zero<W>(v[j]) ? 1u << j : 0u;
+                if (__any_sync(kFullMask, miss != 0)) {
+                    // Blocks still writing.  Lane 0 watches one word (its unit) of the warp's
+                    // earliest missing row until it is written -- one load per warp and
+                    // round, not one per missing unit -- then the lanes reload what they
+                    // miss, until nothing is missing or the time limit passes.
+                    const uint64_t t0 = global_ns();
+                    while (true) {
+                        const int mine = miss ? p0 + (__ffs((int)miss) - 1) * kFinSub : INT_MAX;
+                        const int pw = __reduce_min_sync(kFullMask, mine);
+                        if (pw == INT_MAX) break;
+                        int gave_up = 0;
+                        if (lane == 0) {  // lane 0 owns unit 0 of the group, which exists
+                            const uint32_t* wq = opaque(src) + (size_t)pw * row_stride;
+                            uint32_t w1[1];
+                            ld_part<1>(wq, w1);
+                            while (w1[0] == 0u) {
+                                if (global_ns() - t0 > a.limit_ns) {
+                                    gave_up = 1;
+                                    break;
+                                }
+                                __nanosleep(128);
+                                ld_part<1>(wq, w1);
+                            }
+                        }
+                        if (__shfl_sync(kFullMask, gave_up, 0)) {
+                            late = true;
+                            break;
+                        }
+                        const uint32_t* q = opaque(q0);  // addresses recomputed, not kept live
+#pragma unroll
+                        for (int j = 0; j < L; ++j)
+                            if (miss & (1u << j)) ld_part<W>(q + j * step, v[j]);
+                        miss = 0;
+#pragma unroll
+                        for (int j = 0; j < L; ++j) miss |= has_zero<W>(v[j]) ? 1u << j : 0u;
+                    }
+                }
+                uint32_t* qz = opaque(q0);
+#pragma unroll
+                for (int j = 0; j < L; ++j)  // read: cleared for the next call
+                    if (j < nj) st_zero<W>(qz + j * step);
 #pragma unroll
                 for (int j = 0; j < L; ++j)
 #pragma unroll
                     for (int i = 0; i < U; ++i) {
                         if constexpr (COMPACT)
-                            S[i] += v[j][i];
+                            S[i] += part_dec(v[j][i]);
                         else
-                            comp_add(S[i], C[i], v[j][2 * i], v[j][2 * i + 1]);
+                            comp_add(S[i], C[i], part_dec(v[j][2 * i]), part_dec(v[j][2 * i + 1]));
                     }
             }
         }
@@ -234,36 +305,25 @@ __device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
         }
         __syncthreads();  // scratch is reused by the next group
     }
+    if (late) raise_status(a.status, kStatusTimeout);
 }
 
-// Called by every thread of every block once the block's partial row is written.  One
-// thread per block publishes the row (block barrier, then a GPU-scope fence and the counter
-// increment).  Blocks that own no unit group of the finish are then done and leave, freeing
-// their SM; the others wait, bounded, until all P blocks have arrived, and finish their
-// groups.  The finishing block that is last past the wait puts the counters back to 0.
+// Called by every thread of every block once the block's partial row is stored.  Blocks that
+// own no unit group of the finish are done and leave, freeing their SM; the others finish
+// their groups, picking up each block's partials as they land.
 template <typename T>
-__device__ void arrive_and_finish(const KParams& a, float* scratch) {
-    __shared__ int s_ok;
+__device__ void finish_if_owner(const KParams& a, float* scratch) {
     const int P = (int)gridDim.x, f = (int)blockIdx.x;
     const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
                             : (a.cols % 2 == 0 ? 2 : 1);  // as finish_units is instantiated
     const int ng = (2 * (a.cols / U) + kFinUnits - 1) / kFinUnits;
     const bool finisher = (f + 1) * ng / P > f * ng / P;  // as finish_units splits the groups
-    const unsigned F = (unsigned)min(P, ng);  // blocks owning at least one group
-    __syncthreads();  // every thread's partial sums are written
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(&a.ctr[0], 1u);
-        if (finisher) {
-            const bool ok = wait_counter_geq(&a.ctr[0], (unsigned)P + a.wait_extra, a.limit_ns);
-            __threadfence();
-            s_ok = ok ? 1 : 0;
-            if (!ok) raise_status(a.status, kStatusTimeout);
-        }
-    }
     if (!finisher) return;  // the same for every thread of the block
-    __syncthreads();
-    if (!s_ok) return;
+    __syncthreads();        // shared memory becomes the finish's scratch
+    if (a.wait_extra && threadIdx.x == 0) {
+        // Test hook: also wait for a word that nothing writes, so the limit runs out.
+        if (!wait_counter_geq(a.ctr, 1u, a.limit_ns)) raise_status(a.status, kStatusTimeout);
+    }
     if (a.compact) {
         if (a.cols % 4 == 0)
             finish_units<T, 4, true>(a, P, f, scratch);
@@ -276,13 +336,6 @@ __device__ void arrive_and_finish(const KParams& a, float* scratch) {
             finish_units<T, 2, false>(a, P, f, scratch);
         else
             finish_units<T, 1, false>(a, P, f, scratch);
-    }
-    if (threadIdx.x == 0) {
-        const unsigned done = atomicAdd(&a.ctr[1], 1u);
-        if (done == F - 1) {  // every finishing block is past its wait: reset for the next call
-            atomicExch(&a.ctr[0], 0u);
-            atomicExch(&a.ctr[1], 0u);
-        }
     }
 }
 
@@ -591,8 +644,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                 comp_add(S[3], C[3], t.w, l.w);
             }
             float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c);
-            dst[0] = make_float4(S[0], C[0], S[1], C[1]);
-            dst[1] = make_float4(S[2], C[2], S[3], C[3]);
+            st_part4(dst, S[0], C[0], S[1], C[1]);
+            st_part4(dst + 1, S[2], C[2], S[3], C[3]);
         } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
             f2 S01 = f2_splat(0.f), S23 = f2_splat(0.f);
 #pragma unroll
@@ -601,12 +654,11 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                 S01 = f2_add(S01, f2_make(t.x, t.y));
                 S23 = f2_add(S23, f2_make(t.z, t.w));
             }
-            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.part) +
-                                       ((size_t)stat * P + blockIdx.x) * cols + c) =
-                make_float4(f2_lo(S01), f2_hi(S01), f2_lo(S23), f2_hi(S23));
+            st_part4(reinterpret_cast<float*>(a.part) + ((size_t)stat * P + blockIdx.x) * cols + c,
+                     f2_lo(S01), f2_hi(S01), f2_lo(S23), f2_hi(S23));
         }
     }
-    arrive_and_finish<T>(a, smem_f);
+    finish_if_owner<T>(a, smem_f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -772,34 +824,31 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
                 float2* pb = a.part + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
-                    *reinterpret_cast<float4*>(pg + 2 * h) =
-                        make_float4(f2_lo(sg[v][h]), -f2_lo(cg[v][h]), f2_hi(sg[v][h]), -f2_hi(cg[v][h]));
-                    *reinterpret_cast<float4*>(pb + 2 * h) =
-                        make_float4(f2_lo(sb[v][h]), -f2_lo(cb[v][h]), f2_hi(sb[v][h]), -f2_hi(cb[v][h]));
+                    st_part4(pg + 2 * h, f2_lo(sg[v][h]), -f2_lo(cg[v][h]), f2_hi(sg[v][h]), -f2_hi(cg[v][h]));
+                    st_part4(pb + 2 * h, f2_lo(sb[v][h]), -f2_lo(cb[v][h]), f2_hi(sb[v][h]), -f2_hi(cb[v][h]));
                 }
             } else {
                 float* pg = reinterpret_cast<float*>(a.part) + (size_t)blockIdx.x * cols + (size_t)vi * V;
                 float* pb = reinterpret_cast<float*>(a.part) + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
 #pragma unroll
                 for (int h = 0; h < H; h += 2) {
-                    *reinterpret_cast<float4*>(pg + 2 * h) =
-                        make_float4(f2_lo(sg[v][h]), f2_hi(sg[v][h]), f2_lo(sg[v][h + 1]), f2_hi(sg[v][h + 1]));
-                    *reinterpret_cast<float4*>(pb + 2 * h) =
-                        make_float4(f2_lo(sb[v][h]), f2_hi(sb[v][h]), f2_lo(sb[v][h + 1]), f2_hi(sb[v][h + 1]));
+                    st_part4(pg + 2 * h, f2_lo(sg[v][h]), f2_hi(sg[v][h]), f2_lo(sg[v][h + 1]), f2_hi(sg[v][h + 1]));
+                    st_part4(pb + 2 * h, f2_lo(sb[v][h]), f2_hi(sb[v][h]), f2_lo(sb[v][h + 1]), f2_hi(sb[v][h + 1]));
                 }
             }
         }
     }
-    arrive_and_finish<T>(a, reinterpret_cast<float*>(smem_raw));
+    finish_if_owner<T>(a, reinterpret_cast<float*>(smem_raw));
 }
 
 // ---------------------------------------------------------------------------------------
 // Scalar kernel (any alignment, any width).  Each column is owned by one thread of the
 // block; its compensated running sums live in shared memory when 16 bytes per column fit,
-// else directly in the block's partial row of the workspace (L2-resident).
+// else in a region of the workspace behind the partial rows (L2-resident), so that the
+// partial rows themselves are written only once, when they are final.
 // ---------------------------------------------------------------------------------------
 template <typename T>
-__global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KParams a) {
+__global__ void __launch_bounds__(kBwdScalarThreads, 1) bwd_scalar_kernel(const KParams a) {
     using IO = Io<T>;
     pdl_enter();
     constexpr int NW = kBwdScalarThreads / 32;
@@ -817,9 +866,9 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
     // acc_g[c] = (s, c) Kahan pair of dgamma, acc_b[c] the one of dbeta.
     const bool in_smem = a.stages != 0;  // the host sets it when 16 * cols bytes fit
     float2* acc_g = in_smem ? reinterpret_cast<float2*>(smem_f)
-                            : a.part + (size_t)blockIdx.x * cols;
+                            : a.acc + (size_t)blockIdx.x * cols;
     float2* acc_b = in_smem ? reinterpret_cast<float2*>(smem_f) + cols
-                            : a.part + ((size_t)P + blockIdx.x) * cols;
+                            : a.acc + ((size_t)P + blockIdx.x) * cols;
     for (int j = tid; j < cols; j += kBwdScalarThreads)
         acc_g[j] = acc_b[j] = make_float2(0.f, 0.f);
 
@@ -862,11 +911,12 @@ __global__ void __launch_bounds__(kBwdScalarThreads) bwd_scalar_kernel(const KPa
     // Partial row as (hi, lo): Kahan's value is s - c.
     for (int j = tid; j < cols; j += kBwdScalarThreads) {
         const float2 pg = acc_g[j], pb = acc_b[j];
-        a.part[(size_t)blockIdx.x * cols + j] = make_float2(pg.x, -pg.y);
-        a.part[((size_t)P + blockIdx.x) * cols + j] = make_float2(pb.x, -pb.y);
+        st_part2(a.part + (size_t)blockIdx.x * cols + j, pg.x, -pg.y);
+        st_part2(a.part + ((size_t)P + blockIdx.x) * cols + j, pb.x, -pb.y);
+        if (!in_smem) acc_g[j] = acc_b[j] = make_float2(0.f, 0.f);  // the workspace is left zero
     }
     __syncthreads();  // the shared accumulators become the finish scratch
-    arrive_and_finish<T>(a, smem_f);
+    finish_if_owner<T>(a, smem_f);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1012,7 +1062,7 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
         p.path = kPathScalar;
         p.threads = kBwdScalarThreads;
         const size_t acc = 16ull * cols;  // (hi, lo) pairs for both statistics
-        const bool fits = acc <= (size_t)di.smem_optin / 2;
+        const bool fits = bwd_scalar_acc_in_smem(cols, (size_t)di.smem_optin);
         p.smem = std::max<size_t>(fits ? acc : 0, (size_t)kBwdScalarThreads * 16);
         p.stages = fits ? 1 : 0;  // tells the kernel where its accumulators live
     }
@@ -1047,6 +1097,7 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.rows = a.rows;
     k.cols = a.cols;
     k.part = reinterpret_cast<float2*>(a.partials);
+    k.acc = bwd_plan_acc_region(p) ? k.part + 2ull * (size_t)p.grid * (size_t)a.cols : nullptr;
     k.compact = (p.path == kPathScalar || p.kahan) ? 0 : 1;
     {
         // Warps per unit group in the finish: the fewest (a divisor of the warp count) for
@@ -1054,7 +1105,7 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
         const int nw = p.threads / 32;
         const int U = k.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
                                 : (a.cols % 2 == 0 ? 2 : 1);
-        const int rows_per_warp_batch = kFinSub * (kFinBatch / ((k.compact ? 1 : 2) * U));
+        const int rows_per_warp_batch = kFinSub * fin_rows_per_lane((k.compact ? 1 : 2) * U);
         const int need = (p.grid + rows_per_warp_batch - 1) / rows_per_warp_batch;
         int rw = nw;
         for (int d = 1; d <= nw; ++d)
@@ -1070,7 +1121,7 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_
     k.wait_extra = a.wait_extra;
     k.stages = p.stages;
     void* args[] = {&k};
-    // A cooperative launch: all blocks co-resident, as the finish's bounded wait needs.
+    // A cooperative launch: all blocks co-resident, as the finish's polls need.
     cudaError_t e = launch_kernel(kern, dim3(p.grid), dim3(p.threads), p.smem, stream, args, true);
     if (e == cudaSuccess) *launches = 1;
     return e;

@@ -315,6 +315,59 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     return v;
 }
 
+// ---------------------------------------------------------------------------------------
+// Partial sums that announce themselves.  The backward's per-block partial sums go to a
+// workspace whose words are all zero between calls.  A partial is stored as the complement
+// of its fp32 bits, the one pattern whose complement is zero (0xffffffff, a NaN) first
+// replaced by its neighbour 0xfffffffe (also a NaN), so a stored partial is never the zero
+// word and a zero word is one not written yet.  Readers poll with strong (relaxed, GPU-scope)
+// loads until none of the words they need is zero, then put zeros back for the next call.
+// Every word is written once per call and read whole (aligned 32-bit accesses are
+// single-copy atomic), so neither a fence nor a counter is needed to publish the partials.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t part_enc(float x) {
+    return ~min(__float_as_uint(x), 0xfffffffeu);
+}
+__device__ __forceinline__ float part_dec(uint32_t w) { return __uint_as_float(~w); }
+
+__device__ __forceinline__ void st_part4(void* p, float a, float b, float c, float d) {
+    asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p),
+                 "r"(part_enc(a)), "r"(part_enc(b)), "r"(part_enc(c)), "r"(part_enc(d))
+                 : "memory");
+}
+__device__ __forceinline__ void st_part2(void* p, float a, float b) {
+    asm volatile("st.relaxed.gpu.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(part_enc(a)),
+                 "r"(part_enc(b))
+                 : "memory");
+}
+
+// Strong loads of N = 4, 2 or 1 consecutive words (16-, 8- or 4-byte aligned).
+template <int N>
+__device__ __forceinline__ void ld_part(const void* p, uint32_t (&w)[N]) {
+    if constexpr (N == 4)
+        asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "l"(p)
+                     : "memory");
+    else if constexpr (N == 2)
+        asm volatile("ld.relaxed.gpu.global.v2.b32 {%0, %1}, [%2];"
+                     : "=r"(w[0]), "=r"(w[1])
+                     : "l"(p)
+                     : "memory");
+    else
+        asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(w[0]) : "l"(p) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void st_zero(void* p) {
+    if constexpr (N == 4)
+        *reinterpret_cast<uint4*>(p) = make_uint4(0u, 0u, 0u, 0u);
+    else if constexpr (N == 2)
+        *reinterpret_cast<uint2*>(p) = make_uint2(0u, 0u);
+    else
+        *reinterpret_cast<uint32_t*>(p) = 0u;
+}
+
 // Wait until *ctr >= target or `limit_ns` has passed.  Returns whether the target was seen.
 __device__ __forceinline__ bool wait_counter_geq(const unsigned* ctr, unsigned target,
                                                  uint64_t limit_ns) {

@@ -54,10 +54,10 @@ struct BwdArgs {
     int rows;
     int cols;
     float* partials;      // [2][grid][cols] (hi, lo) fp32 pairs: dgamma, then dbeta
-    unsigned* counters;   // [2]: blocks arrived, blocks finished
+    unsigned* counters;   // the workspace header: zero words that no kernel writes
     unsigned* status;
     uint64_t wait_limit_ns;
-    unsigned wait_extra;  // test hook: wait for this many more arrivals than exist
+    unsigned wait_extra;  // test hook: the finish also waits for a word nothing writes
 };
 
 // A launch plan for the backward: which kernel, how many blocks (= rows of partials).
@@ -89,15 +89,32 @@ cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_overri
 // Largest grid any backward plan can use for `rows` rows on a device with `sms` SMs.
 int bwd_max_grid(int rows, int sms);
 
-constexpr size_t kWorkspaceHeader = 256;  // counters live in the first 256 bytes
+constexpr size_t kWorkspaceHeader = 256;  // a header of zero words, kept for alignment
 
-// Partial sums: [2 statistics][grid][cols] (hi, lo) fp32 pairs.
-inline size_t bwd_workspace_bytes(int grid, int cols) {
-    return kWorkspaceHeader + 2ull * (size_t)grid * (size_t)cols * 2 * sizeof(float);
+// Whether the scalar kernel's running (hi, lo) column sums fit its shared memory.
+inline bool bwd_scalar_acc_in_smem(int cols, size_t smem_optin) {
+    return 16ull * (size_t)cols <= smem_optin / 2;
+}
+
+// The workspace: the header, the partial sums [2 statistics][grid][cols] as (hi, lo) fp32
+// pairs, and -- when `acc_region` (the scalar kernel on rows too wide for its shared memory)
+// -- as much again for that kernel's running sums.  Every byte is zero between calls.
+inline size_t bwd_workspace_bytes(int grid, int cols, bool acc_region) {
+    return kWorkspaceHeader + 2ull * (size_t)grid * (size_t)cols * 2 * sizeof(float) *
+                                  (acc_region ? 2 : 1);
+}
+
+// Whether a plan's kernel keeps running sums in the workspace.
+inline bool bwd_plan_acc_region(const BwdPlan& p) {
+    return p.path == kPathScalar && p.stages == 0;
 }
 
 cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStream_t stream,
                        int* launches);
+
+// Zeroes the allocation-free entry point's fixed scratch on the current device, if a call
+// there has used it (synchronous; after a backward gave up).
+cudaError_t noalloc_scratch_clear();
 
 // Occupancy (resident blocks per SM) of a kernel, cached per (device, kernel, threads, smem).
 int blocks_per_sm(const void* kernel, int threads, size_t smem);

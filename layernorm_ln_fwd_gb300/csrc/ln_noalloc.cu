@@ -4,8 +4,10 @@
 // that reserved its whole device-memory budget at start-up, or a plugin whose host framework
 // owns every device allocation through its own allocator, would fail or fragment memory by
 // allocating mid-run.  ln_bwd_bf16_noalloc runs the same backward kernels as ln_bwd_bf16 but
-// keeps their scratch (the counters and the per-block partial sums) in a fixed array that is
-// part of the library's device image, so the call allocates nothing.
+// keeps their scratch (the per-block partial sums) in a fixed array that is part of the
+// library's device image, so the call allocates nothing.  The array starts zeroed (static
+// device storage) and every completed backward leaves the words it used at zero again, as
+// the kernels' finish requires; ln_device_check re-zeroes it after a backward gave up.
 #include <map>
 #include <mutex>
 
@@ -47,6 +49,22 @@ ln_status fail(cudaError_t e) {
 
 }  // namespace
 
+namespace lnk {
+cudaError_t noalloc_scratch_clear() {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    void* p = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_scratch_addr.find(dev);
+        if (it == g_scratch_addr.end()) return cudaSuccess;  // never used on this device
+        p = it->second;
+    }
+    return cudaMemset(p, 0, LN_NOALLOC_SCRATCH_BYTES);
+}
+}  // namespace lnk
+
 extern "C" ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_res_out,
                                          const ln_bf16* gamma, const float* mean,
                                          const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
@@ -73,13 +91,11 @@ extern "C" ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_
     lnk::BwdPlan plan;
     e = lnk::plan_bwd(Dtype::BF16, (int)rows, (int)cols, aligned, lnk::kPathAuto, &plan);
     if (e != cudaSuccess) return fail(e);
-    if (lnk::bwd_workspace_bytes(plan.grid, (int)cols) > (size_t)LN_NOALLOC_SCRATCH_BYTES)
+    if (lnk::bwd_workspace_bytes(plan.grid, (int)cols, lnk::bwd_plan_acc_region(plan)) >
+        (size_t)LN_NOALLOC_SCRATCH_BYTES)
         return LN_EUNSUPPORTED;  // the problem's partial sums do not fit the fixed scratch
     void* ws = nullptr;
     e = scratch_address(&ws);
-    if (e != cudaSuccess) return fail(e);
-    // The array keeps whatever the previous call left; the counters must start at zero.
-    e = cudaMemsetAsync(ws, 0, lnk::kWorkspaceHeader, stream);
     if (e != cudaSuccess) return fail(e);
     lnk::BwdArgs a;
     a.dy = dy;

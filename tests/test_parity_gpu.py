@@ -125,12 +125,31 @@ def test_caller_owned_workspace(dtype):
     ws = torch.zeros(ln.workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
     assert ws.data_ptr() % 256 == 0
     ref = P.run_oracle(inp, EPS)
-    for _ in range(2):  # the counters are left at zero, so the workspace can be reused
+    for _ in range(2):  # each call leaves the workspace zeroed, so it can be reused
         P.compare_all(P.run_gpu(inp, EPS, workspace=ws), ref, dtype)
     small = torch.zeros(64, dtype=torch.uint8, device="cuda")
     with pytest.raises(ln.LnError) as e:
         P.run_gpu(inp, EPS, workspace=small)
     assert e.value.status == 6
+
+
+def test_workspace_is_left_zero_and_serves_every_shape():
+    """One caller-owned workspace, backwards of several shapes and kernel families in turn:
+    each result matches the oracle and each call leaves every workspace byte at zero (the
+    finish reads the partial sums as they land, taking a zero word for one not yet written,
+    so a stale partial left behind would be taken for the next call's)."""
+    cases = [("f32", 300, 1024, ln.PATH_AUTO), ("bf16", 37, 768, ln.PATH_AUTO),
+             ("bf16", 9, 4104, ln.PATH_BLOCK), ("f32", 5, 8191, ln.PATH_AUTO),
+             ("bf16", 7, 1001, ln.PATH_SCALAR), ("f32", 300, 1024, ln.PATH_AUTO)]
+    nbytes = max(ln.workspace_bytes(r, c) for _, r, c, _ in cases)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for i, (dtype, rows, cols, path) in enumerate(cases):
+        ln.force_path(path)
+        inp = synth.make_inputs(rows, cols, dtype, seed=40 + i)
+        P.compare_all(P.run_gpu(inp, EPS, workspace=ws), P.run_oracle(inp, EPS), dtype,
+                      conditioned=True)
+        torch.cuda.synchronize()
+        assert int(torch.count_nonzero(ws)) == 0, (dtype, rows, cols, path)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
