@@ -140,7 +140,7 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
 constexpr int kFinUnits = 8;
 constexpr int kFinSub = 32 / kFinUnits;
 constexpr int kFinBatch = 48;  // at most this many words of partials per lane and batch,
-constexpr int kFinMaxRows = 12;  // from at most this many partial rows
+constexpr int kFinMaxRows = 10;  // from at most this many partial rows
 __host__ __device__ constexpr int fin_rows_per_lane(int words_per_unit) {
     return kFinBatch / words_per_unit < kFinMaxRows ? kFinBatch / words_per_unit : kFinMaxRows;
 }
@@ -413,6 +413,13 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             RingPos pos;
             for (; k < my_tiles; ++k, pos.next(stages)) {
                 const int slot = pos.slot;
+                // With a 2-slot ring (two blocks per SM) the second tile is requested once the
+                // first has landed, so every block's first tile is ahead of all second tiles
+                // in the DRAM queue and the late blocks start sooner (measured on GB300: bf16
+                // 8192x768 backward 12.6 -> 12.2 us; with a 4-slot ring, one block per SM,
+                // holding back the rest of the first fill was slower: bf16 8192x1280
+                // 16.3 -> 17.2 us).  A timeout here shows again in the consumers' wait.
+                if (k == 1 && stages == 2) (void)mbar_wait(&full_bar[0], 0u, a.limit_ns);
                 // A slot's second and later fills wait for the consumers of the previous pass.
                 if (k >= stages && !mbar_wait(&empty_bar[slot], pos.phase ^ 1u, a.limit_ns)) {
                     raise_status(a.status, kStatusTimeout);
