@@ -152,6 +152,40 @@ def test_workspace_is_left_zero_and_serves_every_shape():
         assert int(torch.count_nonzero(ws)) == 0, (dtype, rows, cols, path)
 
 
+@pytest.mark.parametrize("dtype,rows,cols,path", [
+    ("f32", 300, 1024, ln.PATH_AUTO),    # warp per row, compensated (hi, lo) partials
+    ("bf16", 300, 768, ln.PATH_AUTO),    # warp per row, plain partials
+    ("bf16", 9, 4104, ln.PATH_BLOCK),
+    ("f32", 64, 4104, ln.PATH_BLOCK),
+    ("f32", 37, 1001, ln.PATH_AUTO),     # scalar (unaligned rows)
+])
+def test_nan_in_dy_propagates_and_the_finish_completes(dtype, rows, cols, path):
+    """A NaN in dy makes its row of dx and its column of dgamma and dbeta NaN, as in the
+    oracle, and everything else still matches.  The NaN also reaches the stored partial sums
+    -- as the negated compensation of a Kahan sum its bits can be 0xffffffff, the one pattern
+    the partial encoding must move off the zero word -- and the finish must still see every
+    partial as written (no timeout)."""
+    ln.force_path(path)
+    inp = synth.make_inputs(rows, cols, dtype, seed=77)
+    dy = inp["dy"].clone()
+    dy[rows // 2, 3] = float("nan")
+    inp["dy"] = dy
+    gpu = P.run_gpu(inp, EPS)
+    assert ln.device_check() == 0
+    ref = P.run_oracle(inp, EPS)
+    io = dtype
+    for name in ("dx", "dgamma", "dbeta"):
+        g, r = P.to64(gpu[name]), ref[name]
+        assert np.array_equal(np.isnan(g), np.isnan(r)), name
+        assert np.isnan(r).any(), name
+        ok = ~np.isnan(r)
+        extra = None
+        for part in (ref["_conditioning"].get(name), ref["_colsum"].get(name)):
+            if part is not None:
+                extra = part if extra is None else extra + part
+        P.compare(name, g[ok], r[ok], io, extra=None if extra is None else extra[ok])
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zero_rows(dtype):
     td = synth.torch_dtype(dtype)
