@@ -816,7 +816,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
                 (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
         }
         __syncthreads();
-        return;  // no partial row: every other block's bounded wait runs out as well
+        return;  // no partial row: the finishing blocks' bounded polls run out as well
     }
 
     // Partial row: (hi, lo) for each column, two columns per 16-byte store; plain sums four
