@@ -27,7 +27,7 @@ def lib():
     return ln.lib()
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_forward_and_backward_calls():
     names = _declared_functions()
     for n in ("ln_fwd_f32", "ln_fwd_bf16", "ln_bwd_f32", "ln_bwd_bf16"):
         assert n in names
