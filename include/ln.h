@@ -167,18 +167,21 @@ ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const l
  * point: it exists for callers that cannot call cudaMalloc when they run the backward --
  * a serving process that reserved its whole device-memory budget at start-up, or a plugin
  * whose host framework owns every device allocation -- and cannot hand in a workspace
- * either.  Arguments, results and errors are those of ln_bwd_bf16; the scratch (the
+ * either.  Arguments, results and errors are those of ln_bwd_bf16, and so are the kernels,
+ * the LN_CHECK handling, ln_last_launch_count and the test hooks; the scratch (the
  * per-block partial sums) lives in a fixed array of LN_NOALLOC_SCRATCH_BYTES (16 MiB)
  * compiled into the library, which every GPU that loads the library holds until exit.
- *  - Problems whose scratch would exceed that size are rejected with LN_EUNSUPPORTED
- *    (roughly: 16 * cols * min(rows, 8 * SM count) + 256 bytes must fit; 8192 x 768 and
- *    8192 x 1280 do, 4096 x 8192 does not).
+ *  - Size limit: every problem with ln_bwd_workspace_bytes(rows, cols) <=
+ *    LN_NOALLOC_SCRATCH_BYTES is accepted (that bound covers every kernel choice, so a
+ *    caller can check it in advance); some larger ones fit too, and those that do not are
+ *    rejected with LN_EUNSUPPORTED before anything is launched.  8192 x 768 fits by
+ *    that rule, 8192 x 1280 fits as well, 4096 x 8192 does not.
  *  - The first call on each device looks up the array's device address (once, with that
  *    device current); make that first call before any stream capture begins.
  *  - All calls share the one array, which every completed call leaves all zero (after
- *    LN_ETIMEOUT, ln_device_check zeroes it): calls whose work overlaps on the GPU
- *    (different streams, or different host threads without ordering) race and corrupt each
- *    other's results; order them.
+ *    LN_ETIMEOUT, ln_device_check zeroes it on the stream it is given): calls whose work
+ *    overlaps on the GPU (different streams, or different host threads without ordering)
+ *    race and corrupt each other's results; order them.
  *  - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  */
 #define LN_NOALLOC_SCRATCH_BYTES (16u << 20)
@@ -193,8 +196,10 @@ ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_res_out,
  * polls for other blocks' partial sums) is bounded; when one runs out the
  * kernel records LN_ETIMEOUT in a per-device status word and returns early without
  * faulting.  ln_device_check synchronizes ``stream``, reads and clears that word on the
- * current device, re-zeroes the library-owned workspace of ``stream``, and returns LN_OK or
- * LN_ETIMEOUT (LN_ECUDA if the synchronization itself fails).  Setting the environment
+ * current device and, if it was set, re-zeroes the library-owned workspace of ``stream`` and
+ * the allocation-free entry point's array with copies enqueued on ``stream`` (so they are
+ * ordered before later work on it) and waits for them; it returns LN_OK or LN_ETIMEOUT
+ * (LN_ECUDA if a CUDA call fails).  Setting the environment
  * variable LN_CHECK=1 makes every entry point do this before returning
  * (except for calls made while their stream is being captured into a CUDA graph, which cannot
  * synchronise).

@@ -203,6 +203,8 @@ ln_status fwd_impl(Dtype dt, const T* x, const T* res, const T* gamma, const T* 
     return finish_call(e, launches, stream);
 }
 
+}  // namespace
+
 template <typename T>
 ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const float* mean,
                    const float* rstd, T* dx, T* dgamma, T* dbeta, int64_t rows, int64_t cols,
@@ -275,7 +277,14 @@ ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const flo
     return finish_call(e, launches, stream);
 }
 
-}  // namespace
+template ln_status bwd_impl<float>(Dtype, const float*, const float*, const float*,
+                                   const float*, const float*, float*, float*, float*, int64_t,
+                                   int64_t, void*, size_t, bool, ln_stream_t);
+template ln_status bwd_impl<__nv_bfloat16>(Dtype, const __nv_bfloat16*, const __nv_bfloat16*,
+                                           const __nv_bfloat16*, const float*, const float*,
+                                           __nv_bfloat16*, __nv_bfloat16*, __nv_bfloat16*,
+                                           int64_t, int64_t, void*, size_t, bool, ln_stream_t);
+
 }  // namespace lnk
 
 using lnk::Dtype;
@@ -364,17 +373,19 @@ ln_status ln_device_check(ln_stream_t stream_) {
     if (e != cudaSuccess) return lnk::cuda_fail(e);
     // A backward that gave up may have left partial sums in its workspace, where the next
     // call would take them for its own: clear this stream's workspace and the fixed scratch
-    // of the allocation-free entry point.
+    // of the allocation-free entry point, on this stream (so that the clearing is ordered
+    // before any later work on it, whatever kind of stream it is), and wait for it.
     {
         const int dev = lnk::current_device();
         std::lock_guard<std::mutex> lk(lnk::g_mu);
         auto it = lnk::g_workspaces.find(std::make_pair(dev, stream));
         if (it != lnk::g_workspaces.end() && it->second.ptr) {
-            e = cudaMemset(it->second.ptr, 0, it->second.bytes);
+            e = cudaMemsetAsync(it->second.ptr, 0, it->second.bytes, stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
             if (e != cudaSuccess) return lnk::cuda_fail(e);
         }
     }
-    e = lnk::noalloc_scratch_clear();
+    e = lnk::noalloc_scratch_clear(stream);
     if (e != cudaSuccess) return lnk::cuda_fail(e);
     return (word & lnk::kStatusTimeout) ? LN_ETIMEOUT : LN_OK;
 }

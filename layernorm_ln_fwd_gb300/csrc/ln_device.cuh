@@ -225,75 +225,105 @@ struct RowDivisor {
     }
 };
 
-// The shift of a row for its shifted sums: the row's first stored value, K.  Every d = s - K
-// of a bf16 row is exact, and for any row sum d^2 / n = var + (mean - K)^2 with K a draw of
-// the row's own values, so var = sum d^2 / n - (sum d / n)^2 keeps all but about one bit
-// (the cancellation E[x^2] - E[x]^2 suffers is from the mean, not the spread).
-template <typename T>
-__device__ __forceinline__ float row_shift(const uint4& first) {
-    if constexpr (Io<T>::kVec == 8)
-        return __uint_as_float(first.x << 16);  // the low bf16 of the first word
-    else
-        return __uint_as_float(first.x);
+// Row statistics without E[x^2] - E[x]^2 ("Accelerating Transformer on GPU (I)", section 4.2:
+// the pairwise update of Welford and Chan).  Each lane (or thread) summarises its own values
+// of a row as a count n, the mean m of d = s - K and the sum M2 of squared deviations of d
+// from m, where K is one value of the row shared by all lanes (so the lane means are small
+// numbers whenever K is a typical value; M2 does not depend on K at all).  The summaries are
+// merged pairwise with
+//   n = na + nb,  m = (na ma + nb mb) / n,  M2 = M2a + M2b + (mb - ma)^2 na nb / n,
+// a sum of non-negative terms: nothing cancels, whichever value K is.  The merge is written
+// in a form symmetric in (a, b) -- separate products, commutative sums, delta^2 -- so both
+// lanes of an xor-butterfly pair end with the same bits and, after the butterfly, every lane
+// of the warp holds the same summary.  (The section prints the mean update as
+// ma + delta nb / n; the weighted form computes the same number and is symmetric.)
+//
+// The plain sum S of the unshifted values travels with the summary: the stored mean is S / n,
+// which carries only the rounding of sums of the row's own values (K + m would carry K's
+// distance to the mean times the unit roundoff, large when K is an outlier).
+//
+// One level of the merge with partner offset o and weights wa = na / n, wb = nb / n,
+// w = na nb / n (this lane holds the na-value summary).
+__device__ __forceinline__ void chan_step(int o, float wa, float wb, float w, float& S,
+                                          float& m, float& M2) {
+    const float Sb = __shfl_xor_sync(kFullMask, S, o);
+    const float mb = __shfl_xor_sync(kFullMask, m, o);
+    const float qb = __shfl_xor_sync(kFullMask, M2, o);
+    const float delta = __fsub_rn(mb, m);
+    S = __fadd_rn(S, Sb);
+    M2 = __fmaf_rn(__fmul_rn(delta, delta), w, __fadd_rn(M2, qb));
+    m = __fadd_rn(__fmul_rn(wa, m), __fmul_rn(wb, mb));
 }
-// Row statistics as a mergeable summary: count n, the sum S + c of the shifted values (S and
-// its compensation c, kept error-free with TwoSum) and M2, the sum of squared deviations from
-// the group's own mean.  Two summaries merge with the pairwise update of Welford/Chan
-// ("Accelerating Transformer on GPU (I)", section 4.2):
-//   n = na + nb,  S = Sa + Sb,  M2 = M2a + M2b + delta^2 na nb / n,  delta = Sb/nb - Sa/na,
-// where delta^2 na nb / n is computed as (na Sb - nb Sa)^2 / (na nb n).  Every operation is
-// rounded separately (never fused) and is symmetric in (a, b), so both lanes of an xor-
-// butterfly pair end with the same bits.  M2 is a sum of non-negative terms: no cancellation.
-struct RowStats {
-    float n, s, c, q;
-};
+
+// Butterfly over xor offsets `first`, first / 2, ..., 1 when every lane's summary covers the
+// same count n: each level merges two equal halves (wa = wb = 1/2, w = n / 2, n doubling).
+__device__ __forceinline__ void chan_reduce_equal(int first, float n, float& S, float& m,
+                                                  float& M2) {
+    for (int o = first; o > 0; o >>= 1) {
+        chan_step(o, 0.5f, 0.5f, __fmul_rn(n, 0.5f), S, m, M2);
+        n = __fadd_rn(n, n);
+    }
+}
+
+// Butterfly over all 32 lanes for any counts (n = this lane's; 0 for a lane with no values).
+__device__ __forceinline__ void chan_reduce_any(float n, float& S, float& m, float& M2) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float nb = __shfl_xor_sync(kFullMask, n, o);
+        float wa = 1.f, wb = 0.f, w = 0.f;
+        if (n == 0.f) {
+            wa = 0.f;
+            wb = 1.f;
+        } else if (nb != 0.f) {
+            const float inv = __frcp_rn(__fadd_rn(n, nb));  // counts are small integers
+            wa = __fmul_rn(n, inv);
+            wb = __fmul_rn(nb, inv);
+            w = __fmul_rn(__fmul_rn(n, nb), inv);
+        }
+        chan_step(o, wa, wb, w, S, m, M2);
+        n = __fadd_rn(n, nb);
+    }
+}
+
+// The row's shift K: the median of five of its stored values (in the block and scalar
+// kernels those at columns 0, C/4, C/2, 3C/4 and C - 1; in the warp kernel the first values
+// of five lanes spread over the row).  Any K gives the same M2; K only sets the size of the shifted values d, whose
+// rounding (when |d| is large next to s) and whose mean's rounding reach xhat as about the
+// unit roundoff times |K - mean| * rstd.  The median of a spread sample stays within the
+// body of the row whatever a few values (an outlier in the first column, say) are.
+__device__ __forceinline__ float median5(float a, float b, float c, float d, float e) {
+    const float f = fmaxf(fminf(a, b), fminf(c, d));
+    const float g = fminf(fmaxf(a, b), fmaxf(c, d));
+    return fmaxf(fminf(e, f), fminf(fmaxf(e, f), g));  // the median of (e, f, g)
+}
+
+// A vector's first value (the low bf16 of its first word for bf16).
+template <typename T>
+__device__ __forceinline__ float first_value(const uint4& v) {
+    if constexpr (Io<T>::kVec == 8)
+        return __uint_as_float(v.x << 16);
+    else
+        return __uint_as_float(v.x);
+}
+
+__device__ __forceinline__ int sample_col(int j, int cols) { return (int)(((long long)j * (cols - 1)) / 4); }
+
+// K from a row held in shared or global memory: s = x + res rounded to the I/O type (or x).
+template <typename T, bool HAS_RES>
+__device__ __forceinline__ float row_shift(const T* xs, const T* rs, int cols) {
+    float v[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+        const int c = sample_col(j, cols);
+        v[j] = HAS_RES ? Io<T>::round(Io<T>::to_f(xs[c]) + Io<T>::to_f(rs[c])) : Io<T>::to_f(xs[c]);
+    }
+    return median5(v[0], v[1], v[2], v[3], v[4]);
+}
 
 __device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
     s = __fadd_rn(a, b);
     const float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-}
-
-__device__ __forceinline__ void stats_merge(RowStats& a, const RowStats& b) {
-    const float nn = __fadd_rn(a.n, b.n);  // exact: small integers
-    if (a.n > 0.f && b.n > 0.f) {
-        const float sa = __fadd_rn(a.s, a.c), sb = __fadd_rn(b.s, b.c);
-        const float t = __fsub_rn(__fmul_rn(a.n, sb), __fmul_rn(b.n, sa));
-        const float den = __fmul_rn(__fmul_rn(a.n, b.n), nn);
-        // A correction term: the fast division's ~2 ulp error is immaterial, and both lanes
-        // of a pair divide the same operands.
-        a.q = __fadd_rn(__fadd_rn(a.q, b.q), __fdividef(__fmul_rn(t, t), den));
-    } else {
-        a.q = __fadd_rn(a.q, b.q);
-    }
-    float s, e;
-    two_sum_f(a.s, b.s, s, e);
-    a.c = __fadd_rn(__fadd_rn(a.c, b.c), e);
-    a.s = s;
-    a.n = nn;
-}
-
-__device__ __forceinline__ void warp_stats(RowStats& r) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        RowStats b;
-        b.n = __shfl_xor_sync(kFullMask, r.n, o);
-        b.s = __shfl_xor_sync(kFullMask, r.s, o);
-        b.c = __shfl_xor_sync(kFullMask, r.c, o);
-        b.q = __shfl_xor_sync(kFullMask, r.q, o);
-        stats_merge(r, b);
-    }
-}
-
-// Merge the summaries of a block's warps (red[0..3][w], w < nw) the same way in every warp:
-// lane w holds warp w's summary and one butterfly combines them, so every thread of the block
-// ends with the same bits without a per-thread sequential merge.
-__device__ __forceinline__ RowStats block_stats(const float (*red)[32], int nw) {
-    const int lane = threadIdx.x & 31;
-    RowStats r{0.f, 0.f, 0.f, 0.f};
-    if (lane < nw) r = RowStats{red[0][lane], red[1][lane], red[2][lane], red[3][lane]};
-    warp_stats(r);
-    return r;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -6,16 +6,17 @@
 // fusion as in "llm.c: the llmc/ CUDA kernel layer", section 3.2.)
 //
 // Statistics in one reduction, without the cancellation of E[s^2] - E[s]^2 that breaks rows
-// whose mean dwarfs their spread ("Accelerating Transformer on GPU (I)", section 4.2):
-//  * vector kernels: shifted sums.  K = the row's first stored value, so d = s - K is exact
-//    for bf16 and sum d^2 / n exceeds the variance by (mean - K)^2, about one more variance;
-//    sum d and sum d^2 are reduced together (one xor butterfly, plus one cross-warp exchange
-//    for a block per row) and var = sum d^2 / n - (sum d / n)^2 then has both terms of the
-//    order of var itself;
-//  * scalar kernel: each thread keeps a Welford summary (count, compensated sum, M2) and the
-//    summaries are combined with the Welford/Chan pairwise merge of the same section;
-//  * xhat = d * rstd - mean(d) * rstd (one fma), which never subtracts two large numbers.
-// mean = K + mean(d) and rstd = 1 / sqrt(var + eps) (rsqrtf) are stored in fp32.
+// whose mean dwarfs their spread ("Accelerating Transformer on GPU (I)", section 4.2): every
+// lane (thread) summarises its own values as (count, mean of d = s - K, M2 of d) -- K is a
+// value from the body of the row, so the means are small numbers -- and the summaries
+// are merged pairwise with the Welford/Chan update of the same section: one xor butterfly per
+// warp, plus one cross-warp exchange and a second butterfly for a block per row.  K is the
+// median of five values spread over the row, so it stays in the body of the row whatever a
+// few values are.  The merged
+// M2 is a sum of non-negative terms, so the variance keeps full precision whichever value K
+// is (an outlier in the first column included).  The plain sum of the unshifted values rides
+// along in the same butterfly and gives the stored mean; out = gamma * ((d - mean_d) * rstd)
+// + beta, and rstd = 1 / sqrt(M2 / n + eps) (rsqrtf), mean and rstd stored in fp32.
 //
 // Three kernel families compute the same function:
 //  * warp per row (rows of at most 256 vectors of 16 bytes): tiles of 7 rows are staged in
@@ -119,6 +120,21 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
         PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
         PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
+    // This lane's count of values in a row (the same for every row); when the row is a
+    // multiple of 32 vectors every lane holds the same count and the butterfly merges equal
+    // halves.
+    int nv_lane = 0;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) nv_lane += v * 32 + lane < nvec ? 1 : 0;
+    const float n_lane = (float)(nv_lane * V);
+    const float inv_lane = nv_lane ? 1.0f / n_lane : 0.f;
+    const bool equal = nvec % 32 == 0;
+    // The lanes whose first values make the row's five-value sample for its shift K: spread
+    // over the lanes that hold part of the row.
+    const int nlanes = min(nvec, 32);
+    int sample_lane[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) sample_lane[j] = j * (nlanes - 1) / 4;
     const bool write_res = res_out != nullptr;
     RingPos pos;
     for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
@@ -149,41 +165,66 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     sp[v] = make_uint4(0, 0, 0, 0);
                 }
             }
-            // Shifted sums: K = the row's first stored value (lane 0's).  The low halves of
-            // the pairs sum the even columns, the high halves the odd ones.
-            const f2 K2 = f2_splat(__shfl_sync(kFullMask, row_shift<T>(sp[0]), 0));
+            // This lane's summary: the plain sum of s, then d = s - K (K = the median of five
+            // of the row's values: the first values of five lanes spread over the row), the
+            // mean of d and M2 about it, from registers.  The low halves of the pairs take the
+            // even columns, the high halves the odd ones; two accumulators each (even and odd
+            // pairs) halve the chains of dependent additions.
+            const float f0 = first_value<T>(sp[0]);
+            float kv[5];
+#pragma unroll
+            for (int j = 0; j < 5; ++j) kv[j] = __shfl_sync(kFullMask, f0, sample_lane[j]);
+            const f2 K2 = f2_splat(median5(kv[0], kv[1], kv[2], kv[3], kv[4]));
             f2 d[VPL][H];
-            f2 a = f2_splat(0.f), q = f2_splat(0.f);
+            f2 as[2] = {f2_splat(0.f), f2_splat(0.f)}, ad[2] = {f2_splat(0.f), f2_splat(0.f)};
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 PR::unpack(sp[v], d[v]);
                 if (v * 32 + lane < nvec) {
 #pragma unroll
                     for (int h = 0; h < H; ++h) {
+                        as[h & 1] = f2_add(as[h & 1], d[v][h]);
                         d[v][h] = f2_sub(d[v][h], K2);
-                        a = f2_add(a, d[v][h]);
-                        q = f2_fma(d[v][h], d[v][h], q);
+                        ad[h & 1] = f2_add(ad[h & 1], d[v][h]);
                     }
                 }
             }
-            float sd = f2_lo(a) + f2_hi(a), sd2 = f2_lo(q) + f2_hi(q);
-            warp_sum2(sd, sd2);  // the one reduction of the row
-            const float md = rdiv.div(sd);
-            const float var = fmaxf(rdiv.div(sd2) - md * md, 0.f);
-            const float rs = rsqrtf(var + eps);
+            const f2 as2 = f2_add(as[0], as[1]), ad2 = f2_add(ad[0], ad[1]);
+            float S = f2_lo(as2) + f2_hi(as2);
+            float md = (f2_lo(ad2) + f2_hi(ad2)) * inv_lane;
+            const f2 ml2 = f2_splat(md);
+            f2 q[2] = {f2_splat(0.f), f2_splat(0.f)};
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                if (v * 32 + lane < nvec) {
+#pragma unroll
+                    for (int h = 0; h < H; ++h) {
+                        const f2 t = f2_sub(d[v][h], ml2);
+                        q[h & 1] = f2_fma(t, t, q[h & 1]);
+                    }
+                }
+            }
+            const f2 q2 = f2_add(q[0], q[1]);
+            float M2 = f2_lo(q2) + f2_hi(q2);
+            if (equal)  // the one reduction of the row
+                chan_reduce_equal(16, n_lane, S, md, M2);
+            else
+                chan_reduce_any(n_lane, S, md, M2);
+            const float rs = rsqrtf(rdiv.div(M2) + eps);
             if (lane == 0) {
-                mean[row] = f2_lo(K2) + md;
+                mean[row] = rdiv.div(S);
                 rstd[row] = rs;
             }
-            // out = gamma * ((s - K) * rs - md * rs) + beta
-            const f2 rs2 = f2_splat(rs), nmr2 = f2_splat(-md * rs);
+            // out = gamma * ((s - K - mean_d) * rs) + beta
+            const f2 rs2 = f2_splat(rs), md2 = f2_splat(md);
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 const int vi = v * 32 + lane;
                 if (vi < nvec) {
                     f2 o[H];
 #pragma unroll
-                    for (int h = 0; h < H; ++h) o[h] = f2_fma(gp[v][h], f2_fma(d[v][h], rs2, nmr2), bp[v][h]);
+                    for (int h = 0; h < H; ++h)
+                        o[h] = f2_fma(gp[v][h], f2_mul(f2_sub(d[v][h], md2), rs2), bp[v][h]);
                     st_stream(out + base + (size_t)vi * V, PR::pack(o));
                 }
             }
@@ -212,7 +253,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages];
-    __shared__ float red[2][32];
+    __shared__ float red[3][32];
     __shared__ int abort_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -223,6 +264,23 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     const unsigned slot_bytes = nin * row_bytes;
     const RowDivisor rdiv(cols);
 
+    // Counts of values in a row (the same for every row): this thread's, and in lane w the
+    // count of warp w, whose summary lane w takes in the cross-warp butterfly.  When every
+    // thread holds VPT vectors (and the warp count is a power of two) the butterflies merge
+    // equal halves.
+    auto vecs_of = [&](int t) {
+        int n = 0;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) n += v * nthreads + t < nvec ? 1 : 0;
+        return n;
+    };
+    const float n_thr = (float)(vecs_of(tid) * V);
+    const float inv_thr = n_thr > 0.f ? 1.0f / n_thr : 0.f;
+    int nv_warp = 0;
+    for (int j = 0; j < 32 && lane < nw; ++j) nv_warp += vecs_of(lane * 32 + j);
+    const float n_warp = (float)(nv_warp * V);
+    const bool equal_thr = nvec == nthreads * VPT;
+    const bool equal_warps = equal_thr && (nw & (nw - 1)) == 0;
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) mbar_init(&full_bar[i], 1);
         abort_flag = 0;
@@ -263,6 +321,9 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
+        // The row's shift K: the median of five of its values, which every thread reads from
+        // shared memory (first, so that these loads overlap the vector loads below).
+        const f2 K2 = f2_splat(row_shift<T, HAS_RES>(xs, rsm, cols));
 
         uint4 sp[VPT];
 #pragma unroll
@@ -277,57 +338,77 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                 sp[v] = make_uint4(0, 0, 0, 0);
             }
         }
-        // Shifted sums: K = the row's first stored value (every thread reads it from shared
-        // memory).  The low halves of the pairs sum the
-        // even columns, the high halves the odd ones.
-        const uint4 first = HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
-                                                   *reinterpret_cast<const uint4*>(rsm))
-                                    : *reinterpret_cast<const uint4*>(xs);
-        const f2 K2 = f2_splat(row_shift<T>(first));
+        // This thread's summary: the plain sum of s, then d = s - K, the mean of d and M2
+        // about it.  The low halves of the pairs take the even columns, the high halves the
+        // odd ones.
         f2 d[VPT][H];
-        f2 a2 = f2_splat(0.f), q2 = f2_splat(0.f);
+        f2 as = f2_splat(0.f), ad = f2_splat(0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             PR::unpack(sp[v], d[v]);
             if (v * nthreads + tid < nvec) {
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
+                    as = f2_add(as, d[v][h]);
                     d[v][h] = f2_sub(d[v][h], K2);
-                    a2 = f2_add(a2, d[v][h]);
-                    q2 = f2_fma(d[v][h], d[v][h], q2);
+                    ad = f2_add(ad, d[v][h]);
                 }
             }
         }
-        float sd = f2_lo(a2) + f2_hi(a2), sd2 = f2_lo(q2) + f2_hi(q2);
-        warp_sum2(sd, sd2);
+        float S = f2_lo(as) + f2_hi(as);
+        float md = (f2_lo(ad) + f2_hi(ad)) * inv_thr;
+        const f2 ml2 = f2_splat(md);
+        f2 q = f2_splat(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            if (v * nthreads + tid < nvec) {
+#pragma unroll
+                for (int h = 0; h < H; ++h) {
+                    const f2 t = f2_sub(d[v][h], ml2);
+                    q = f2_fma(t, t, q);
+                }
+            }
+        }
+        float M2 = f2_lo(q) + f2_hi(q);
+        if (equal_thr)
+            chan_reduce_equal(16, n_thr, S, md, M2);
+        else
+            chan_reduce_any(n_thr, S, md, M2);
         if (lane == 0) {
-            red[0][warp] = sd;
-            red[1][warp] = sd2;
+            red[0][warp] = S;
+            red[1][warp] = md;
+            red[2][warp] = M2;
         }
         __syncthreads();  // the one cross-warp exchange of the row
         if (abort_flag) break;
-        sd = 0.f;
-        sd2 = 0.f;
-        for (int w = 0; w < nw; ++w) {  // same order in every thread: same bits everywhere
-            sd += red[0][w];
-            sd2 += red[1][w];
+        // Every warp merges the warps' summaries the same way: the same bits everywhere.
+        if (equal_warps) {  // lane l takes warp l mod nw; groups of nw lanes merge alike
+            const int w = lane & (nw - 1);
+            S = red[0][w];
+            md = red[1][w];
+            M2 = red[2][w];
+            chan_reduce_equal(nw >> 1, 32.f * n_thr, S, md, M2);
+        } else {
+            S = lane < nw ? red[0][lane] : 0.f;
+            md = lane < nw ? red[1][lane] : 0.f;
+            M2 = lane < nw ? red[2][lane] : 0.f;
+            chan_reduce_any(n_warp, S, md, M2);
         }
-        const float md = rdiv.div(sd);
-        const float var = fmaxf(rdiv.div(sd2) - md * md, 0.f);
-        const float rs = rsqrtf(var + eps);
+        const float rs = rsqrtf(rdiv.div(M2) + eps);
         if (tid == 0) {
-            mean[row] = f2_lo(K2) + md;
+            mean[row] = rdiv.div(S);
             rstd[row] = rs;
         }
-        // out = gamma * ((s - K) * rs - md * rs) + beta
-        const f2 rs2 = f2_splat(rs), nmr2 = f2_splat(-md * rs);
+        // out = gamma * ((s - K - mean_d) * rs) + beta
+        const f2 rs2 = f2_splat(rs), md2 = f2_splat(md);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
                 f2 o[H];
 #pragma unroll
-                for (int h = 0; h < H; ++h) o[h] = f2_fma(gp[v][h], f2_fma(d[v][h], rs2, nmr2), bp[v][h]);
+                for (int h = 0; h < H; ++h)
+                    o[h] = f2_fma(gp[v][h], f2_mul(f2_sub(d[v][h], md2), rs2), bp[v][h]);
                 st_stream(out + base + (size_t)vi * V, PR::pack(o));
             }
         }
@@ -363,10 +444,20 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
     using IO = Io<T>;
     pdl_enter();
     constexpr int NW = kFwdScalarThreads / 32;
-    __shared__ float red[4][32];
+    __shared__ float red[3][NW];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const RowDivisor rdiv(cols);
     const bool write_res = res_out != nullptr;
+    // This thread's count of values in a row (columns tid, tid + 256, ...) and the weights of
+    // the warp's and of the cross-warp butterflies; every warp's count follows from cols.
+    // Counts of values in a row: this thread's (columns tid, tid + 256, ...) and, in lane w,
+    // warp w's.  Equal everywhere when cols is a multiple of the block size.
+    auto count_of = [&](int t) { return t < cols ? (cols - 1 - t) / kFwdScalarThreads + 1 : 0; };
+    const float n_thr = (float)count_of(tid);
+    int nw_total = 0;
+    for (int j = 0; j < 32 && lane < NW; ++j) nw_total += count_of(lane * 32 + j);
+    const float n_warp = (float)nw_total;
+    const bool equal = cols % kFwdScalarThreads == 0;
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * cols;
         auto load_s = [&](int j) -> float {
@@ -374,42 +465,49 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
             if (HAS_RES) v = IO::round(v + IO::to_f(res[base + j]));
             return v;
         };
-        const float K = load_s(0);
-        // This thread's summary of d = s - K: compensated sum plus Welford's running M2.
-        RowStats st{0.f, 0.f, 0.f, 0.f};
-        float wm = 0.f;  // Welford's running mean
+        const float K = row_shift<T, HAS_RES>(x + base, HAS_RES ? res + base : nullptr, cols);
+        // This thread's summary of its values: their plain sum S, and Welford's running mean
+        // and M2 of d = s - K.
+        float S = 0.f, md = 0.f, M2 = 0.f, n = 0.f;
         for (int j = tid; j < cols; j += kFwdScalarThreads) {
             const float sv = load_s(j);
             if (write_res) res_out[base + j] = IO::from_f(sv);
-            const float d = sv - K;
-            st.n += 1.f;
-            float sum, e;
-            two_sum_f(st.s, d, sum, e);
-            st.s = sum;
-            st.c = __fadd_rn(st.c, e);
-            const float delta = d - wm;
-            wm += delta / st.n;
-            st.q += delta * (d - wm);
+            S = __fadd_rn(S, sv);
+            const float d = __fsub_rn(sv, K);
+            n = __fadd_rn(n, 1.f);
+            const float delta = __fsub_rn(d, md);
+            md = __fadd_rn(md, __fdiv_rn(delta, n));
+            M2 = __fmaf_rn(delta, __fsub_rn(d, md), M2);
         }
-        warp_stats(st);
+        if (equal)
+            chan_reduce_equal(16, n_thr, S, md, M2);
+        else
+            chan_reduce_any(n_thr, S, md, M2);
         if (lane == 0) {
-            red[0][warp] = st.n;
-            red[1][warp] = st.s;
-            red[2][warp] = st.c;
-            red[3][warp] = st.q;
+            red[0][warp] = S;
+            red[1][warp] = md;
+            red[2][warp] = M2;
         }
         __syncthreads();
-        st = block_stats(red, NW);
-        const float md = rdiv.div(__fadd_rn(st.s, st.c));
-        const float rs = rsqrtf(rdiv.div(st.q) + eps);
+        if (equal) {  // NW = 8 warps of equal counts: lane l takes warp l mod 8
+            S = red[0][lane & (NW - 1)];
+            md = red[1][lane & (NW - 1)];
+            M2 = red[2][lane & (NW - 1)];
+            chan_reduce_equal(NW / 2, 32.f * n_thr, S, md, M2);
+        } else {
+            S = lane < NW ? red[0][lane] : 0.f;
+            md = lane < NW ? red[1][lane] : 0.f;
+            M2 = lane < NW ? red[2][lane] : 0.f;
+            chan_reduce_any(n_warp, S, md, M2);
+        }
+        const float rs = rsqrtf(rdiv.div(M2) + eps);
         if (tid == 0) {
-            mean[row] = K + md;
+            mean[row] = rdiv.div(S);
             rstd[row] = rs;
         }
         for (int j = tid; j < cols; j += kFwdScalarThreads) {
             const float sv = load_s(j);
-            out[base + j] =
-                IO::from_f(IO::to_f(gamma[j]) * ((sv - K - md) * rs) + IO::to_f(beta[j]));
+            out[base + j] = IO::from_f(IO::to_f(gamma[j]) * ((sv - K - md) * rs) + IO::to_f(beta[j]));
         }
         __syncthreads();  // `red` is reused by the next row
     }

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "ln.h"
+
 namespace lnk {
 
 enum class Dtype { F32, BF16 };
@@ -113,8 +115,17 @@ cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStre
                        int* launches);
 
 // Zeroes the allocation-free entry point's fixed scratch on the current device, if a call
-// there has used it (synchronous; after a backward gave up).
-cudaError_t noalloc_scratch_clear();
+// there has used it: on `stream`, which is then synchronised (after a backward gave up).
+cudaError_t noalloc_scratch_clear(cudaStream_t stream);
+
+// The backward behind every ln_bwd_* entry point: argument checks, the launch plan, the
+// workspace (the library's own per-stream one when `own_ws`, else `ws` of `ws_bytes` bytes,
+// zero between calls), the launch, and the LN_CHECK handling.  Instantiated for float and
+// __nv_bfloat16.
+template <typename T>
+ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const float* mean,
+                   const float* rstd, T* dx, T* dgamma, T* dbeta, int64_t rows, int64_t cols,
+                   void* ws, size_t ws_bytes, bool own_ws, ln_stream_t stream);
 
 // Occupancy (resident blocks per SM) of a kernel, cached per (device, kernel, threads, smem).
 int blocks_per_sm(const void* kernel, int threads, size_t smem);

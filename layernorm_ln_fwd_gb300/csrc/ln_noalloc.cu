@@ -42,15 +42,10 @@ cudaError_t scratch_address(void** out) {
     return cudaSuccess;
 }
 
-ln_status fail(cudaError_t e) {
-    lnk::record_cuda_error(e);
-    return LN_ECUDA;
-}
-
 }  // namespace
 
 namespace lnk {
-cudaError_t noalloc_scratch_clear() {
+cudaError_t noalloc_scratch_clear(cudaStream_t stream) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -61,7 +56,8 @@ cudaError_t noalloc_scratch_clear() {
         if (it == g_scratch_addr.end()) return cudaSuccess;  // never used on this device
         p = it->second;
     }
-    return cudaMemset(p, 0, LN_NOALLOC_SCRATCH_BYTES);
+    e = cudaMemsetAsync(p, 0, LN_NOALLOC_SCRATCH_BYTES, stream);
+    return e == cudaSuccess ? cudaStreamSynchronize(stream) : e;
 }
 }  // namespace lnk
 
@@ -69,52 +65,24 @@ extern "C" ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_
                                          const ln_bf16* gamma, const float* mean,
                                          const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
                                          ln_bf16* dbeta, int64_t rows, int64_t cols,
-                                         ln_stream_t stream_) {
-    using lnk::Dtype;
+                                         ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    // Sizes are checked before the address lookup, so invalid calls touch no CUDA state.
     if (rows < 0 || cols <= 0) return LN_EINVAL;
     if (cols > LN_MAX_COLS || rows > LN_MAX_ROWS) return LN_EUNSUPPORTED;
-    if (!dgamma || !dbeta) return LN_EINVAL;
-    if (rows > 0 && (!dy || !x_or_res_out || !gamma || !mean || !rstd || !dx)) return LN_EINVAL;
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(e);
-    const lnk::DeviceInfo& di = lnk::device_info(dev);
-    if (di.cc_major != 10 || di.cc_minor != 3) return LN_EUNSUPPORTED;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (rows == 0) {  // sums over no rows
-        e = cudaMemsetAsync(dgamma, 0, (size_t)cols * sizeof(ln_bf16), stream);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, (size_t)cols * sizeof(ln_bf16), stream);
-        return e == cudaSuccess ? LN_OK : fail(e);
-    }
-    const void* ptrs[] = {dy, x_or_res_out, gamma, dx};
-    const bool aligned = lnk::vector_ok(Dtype::BF16, (int)cols, ptrs, 4);
-    lnk::BwdPlan plan;
-    e = lnk::plan_bwd(Dtype::BF16, (int)rows, (int)cols, aligned, lnk::kPathAuto, &plan);
-    if (e != cudaSuccess) return fail(e);
-    if (lnk::bwd_workspace_bytes(plan.grid, (int)cols, lnk::bwd_plan_acc_region(plan)) >
-        (size_t)LN_NOALLOC_SCRATCH_BYTES)
-        return LN_EUNSUPPORTED;  // the problem's partial sums do not fit the fixed scratch
     void* ws = nullptr;
-    e = scratch_address(&ws);
-    if (e != cudaSuccess) return fail(e);
-    lnk::BwdArgs a;
-    a.dy = dy;
-    a.xr = x_or_res_out;
-    a.gamma = gamma;
-    a.mean = mean;
-    a.rstd = rstd;
-    a.dx = dx;
-    a.dgamma = dgamma;
-    a.dbeta = dbeta;
-    a.rows = (int)rows;
-    a.cols = (int)cols;
-    a.counters = static_cast<unsigned*>(ws);
-    a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + lnk::kWorkspaceHeader);
-    a.status = lnk::status_word();
-    a.wait_limit_ns = lnk::kWaitLimitNs;
-    a.wait_extra = 0;
-    int launches = 0;
-    e = lnk::launch_bwd(Dtype::BF16, a, plan, stream, &launches);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    return e == cudaSuccess ? LN_OK : fail(e);
+    const cudaError_t e = scratch_address(&ws);
+    if (e != cudaSuccess) {
+        lnk::record_cuda_error(e);
+        return LN_ECUDA;
+    }
+    // The regular backward with the fixed array as a caller-owned workspace: the same plan,
+    // kernels, checks and test hooks as ln_bwd_bf16.
+    const ln_status st = lnk::bwd_impl<B>(
+        lnk::Dtype::BF16, reinterpret_cast<const B*>(dy), reinterpret_cast<const B*>(x_or_res_out),
+        reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
+        reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols, ws,
+        LN_NOALLOC_SCRATCH_BYTES, false, stream);
+    // A problem whose partial sums do not fit the array is an unsupported size here.
+    return st == LN_ENOSPACE ? LN_EUNSUPPORTED : st;
 }

@@ -3,9 +3,13 @@ float64 oracle on the same seeded inputs, and compare them element by element.
 
 Tolerances (the ones the tests assert):
 
-* fp32 I/O: out, res_out and dx within 2e-5 absolute; mean, rstd, dgamma and dbeta within
-  2e-5 * max(1, |oracle|) (column sums over 262144 rows reach ~1e3, where the fp32 spacing
-  alone is ~1e-4, so a fixed 2e-5 absolute bound would ask for more than fp32 can hold).
+* fp32 I/O: out, res_out and dx within 2e-5 absolute, or 4 fp32 ulps of the oracle value
+  where that is larger (|value| >= 64: at 256 the fp32 spacing alone is 3e-5, so no fp32
+  computation of more than one rounding can promise 2e-5 there; dx of a constant row is
+  rstd * (g - mean g) with rstd = eps^-1/2 ~ 316, hundreds in size); mean, rstd, dgamma and
+  dbeta within 2e-5 * max(1, |oracle|) (column sums over 262144 rows reach ~1e3, where the
+  fp32 spacing alone is ~1e-4, so a fixed 2e-5 absolute bound would ask for more than fp32
+  can hold).
 * bf16 I/O: every bf16 output within 2 bf16 ulps of the oracle value, the ulp taken at
   max(|oracle|, 2^-14) (a plain "2 ulps of the value" cannot be met for values that round
   to almost 0 after an fp32 computation: the fp32 arithmetic itself is ~1e-7 absolute);
@@ -69,11 +73,18 @@ def io_of(dtype) -> str:
     return {torch.float32: "f32", torch.bfloat16: "bf16"}[dtype]
 
 
+def ulp_f32(v) -> np.ndarray:
+    a = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 23)
+
+
 def tolerance(name: str, ref: np.ndarray, io: str) -> np.ndarray:
     if name in ("mean", "rstd") or (io == "f32" and name in ("dgamma", "dbeta")):
         return F32_ABS * np.maximum(1.0, np.abs(ref))
     if io == "f32":
-        return np.full_like(ref, F32_ABS)
+        # 2e-5 absolute; from |value| >= 64 on, where fp32 values are more than 5e-6 apart,
+        # 4 fp32 ulps of the oracle value (a few roundings of a value that size).
+        return np.maximum(F32_ABS, 4.0 * ulp_f32(ref))
     return 2.0 * ulp_bf16(ref)
 
 

@@ -1,8 +1,8 @@
 """Parity of the CUDA path (called through the C ABI) with the float64 oracle.
 
-Small shapes run the oracle on every element; the five full-size workloads compare sampled
-rows element by element and dgamma/dbeta over all rows, in the launch configuration the
-benchmark uses.  Tolerances are stated in ``lnparity``.
+Small shapes run the oracle on every element; the five full-size workloads compare every
+row (a sample of the 262144-row one) element by element and dgamma/dbeta over all rows, in
+the launch configuration the benchmark uses.  Tolerances are stated in ``lnparity``.
 """
 import os
 
@@ -219,28 +219,52 @@ def test_integer_dy_gives_exact_dbeta(dtype, rows, cols):
     np.testing.assert_array_equal(P.to64(gpu["dbeta"]), ref["dbeta"])
 
 
+# The full-size workloads compared on every row (the oracle finishes them in seconds); the
+# 262144-row fp32 workload on a sample of rows (dgamma and dbeta always over all rows).
+SAMPLED_WORKLOADS = {"f32_262144x1000"}
+
+
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
 def test_workload_full_size(name):
-    """The five workloads at full size, in the benchmark's launch configuration: sampled
-    rows element by element, dgamma/dbeta over all rows, and bitwise-repeatable results."""
+    """The five workloads at full size, in the benchmark's launch configuration: every
+    output element by element (all rows; a 256-row sample of the largest), dgamma/dbeta over
+    all rows, and bitwise-repeatable results.  Every output meets the bare stated tolerance
+    (no element needs the column-sum allowance), except dgamma/dbeta of the 262144-row
+    fp32 workload, whose sums over 262144 rows the allowance covers."""
     w = synth.WORKLOADS[name]
     inp = synth.workload_inputs(name, seed=0)
     gpu = P.run_gpu(inp, w.eps)
-    rng = np.random.default_rng(1)
-    sample = rng.choice(w.rows, min(254, w.rows), replace=False)
-    rows_idx = np.unique(np.concatenate([[0, w.rows - 1], sample]))
-    ref = P.run_oracle(inp, w.eps, rows_idx=rows_idx)
-    P.compare_all(gpu, ref, w.dtype, rows_idx=rows_idx)
-    ref_p = P.oracle_dparams(inp, w.eps)
+    rows_idx = None
+    if name in SAMPLED_WORKLOADS:
+        rng = np.random.default_rng(1)
+        sample = rng.choice(w.rows, min(254, w.rows), replace=False)
+        rows_idx = np.unique(np.concatenate([[0, w.rows - 1], sample]))
+        ref = P.run_oracle(inp, w.eps, rows_idx=rows_idx)
+        ref_p = P.oracle_dparams(inp, w.eps)
+    else:
+        ref = P.run_oracle(inp, w.eps)
+        ref_p = {"dgamma": ref.pop("dgamma"), "dbeta": ref.pop("dbeta"),
+                 "_colsum": ref["_colsum"]}
+    infos = P.compare_all(gpu, ref, w.dtype, rows_idx=rows_idx)
     for k in ("dgamma", "dbeta"):
-        P.compare(k, P.to64(gpu[k]), ref_p[k], w.dtype, extra=ref_p["_colsum"][k])
+        infos.append(P.compare(k, P.to64(gpu[k]), ref_p[k], w.dtype, extra=ref_p["_colsum"][k]))
+    over = {i["name"]: i["n_over_stated"] for i in infos if i["n_over_stated"]}
+    allowed = {"dgamma", "dbeta"} if name in SAMPLED_WORKLOADS else set()
+    assert set(over) <= allowed, over
     # Run to run: the backward gives the same bits (dgamma, dbeta and dx).
     d = P.to_device(inp)
+    stable = True
     for _ in range(2):
         dx2, dg2, db2 = ln.bwd(d["dy"], gpu["res_out"], d["gamma"], gpu["mean"], gpu["rstd"])
         torch.cuda.synchronize()
-        assert torch.equal(dg2, gpu["dgamma"]) and torch.equal(db2, gpu["dbeta"])
-        assert torch.equal(dx2, gpu["dx"])
+        stable &= bool(torch.equal(dg2, gpu["dgamma"]) and torch.equal(db2, gpu["dbeta"])
+                       and torch.equal(dx2, gpu["dx"]))
+    P.report({"workload": name, "rows_compared": w.rows if rows_idx is None else len(rows_idx),
+              "max_abs": {i["name"]: i["max_abs"] for i in infos},
+              "worst_ratio": {i["name"]: i["worst_ratio"] for i in infos},
+              "n_over_stated": {i["name"]: i["n_over_stated"] for i in infos},
+              "bitwise_stable": stable})
+    assert stable
 
 
 def test_normalised_rows_property_at_full_size():
@@ -262,28 +286,34 @@ def test_normalised_rows_property_at_full_size():
                                rtol=2e-7, atol=0)
 
 
-def test_bounded_wait_reports_timeout_and_recovers():
+@pytest.mark.parametrize("own_stream", [False, True])
+def test_bounded_wait_reports_timeout_and_recovers(own_stream):
     """The backward's finishers wait for one block more than exists, with a 2 ms limit: the
-    wait runs out, the kernel returns, and ln_device_check reports LN_ETIMEOUT.  Afterwards
-    the same stream computes correct results again."""
+    wait runs out, the kernel returns, and ln_device_check reports LN_ETIMEOUT and re-zeroes
+    the stream's workspace with work ordered on that stream.  Afterwards the same stream --
+    the default one, or a non-blocking torch stream -- computes correct results again."""
     inp = synth.make_inputs(512, 768, "bf16", seed=9)
     L = ln.lib()
+    st = torch.cuda.Stream() if own_stream else torch.cuda.current_stream()
     L.ln_debug_wait_test(2000)
     try:
-        d = P.to_device(inp)
-        out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS)
-        if os.environ.get("LN_CHECK", "0") not in ("", "0"):
-            # Check mode synchronises after every call, so the call itself reports it.
-            with pytest.raises(ln.LnError) as e:
+        with torch.cuda.stream(st):
+            d = P.to_device(inp)
+            out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], EPS)
+            if os.environ.get("LN_CHECK", "0") not in ("", "0"):
+                # Check mode synchronises after every call, so the call itself reports it.
+                with pytest.raises(ln.LnError) as e:
+                    ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
+                assert e.value.status == 5
+            else:
                 ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
-            assert e.value.status == 5
-        else:
-            ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
-            assert ln.device_check() == 5
+                assert ln.device_check(st) == 5
     finally:
         L.ln_debug_wait_test(0)
-    assert ln.device_check() == 0
-    P.compare_all(P.run_gpu(inp, EPS), P.run_oracle(inp, EPS), "bf16")
+    with torch.cuda.stream(st):
+        assert ln.device_check(st) == 0
+        gpu = P.run_gpu(inp, EPS)
+    P.compare_all(gpu, P.run_oracle(inp, EPS), "bf16")
 
 
 def test_launch_count_and_native_library_loaded():
