@@ -2,20 +2,24 @@
 """Benchmark of the fused residual-add + LayerNorm forward + backward on GB300.
 
 One step = one pass of the whole hot path over one batch: the forward (residual add, row
-statistics, normalisation) and the backward (dx, dgamma, dbeta) of the GPT-2-small-shaped
-bf16 workload, 8 x 1024 = 8192 rows of 768 columns, on synthetic seeded inputs.
+statistics, normalisation) and the backward (dx, dgamma, dbeta).  The headline line times
+the largest workload, fp32 262144 x 1000 (the metric names no configuration); the same line
+carries every workload's forward, backward and step times under ``workloads`` (fp32 64x768,
+the GPT-2-shaped bf16 8192x768 and 8192x1280, the wide bf16 4096x8192 with mean 100, and
+the headline), all on seeded synthetic inputs.
 
 Metric: achieved HBM GB/s of the algorithmic bytes (and rows/s), next to the 8 TB/s HBM
 roofline and the measured copy bandwidth.  Algorithmic bytes per step:
   forward  = 4 R C s + 2 C s + 8 R   (read x, res; write out, res_out; gamma, beta; mean, rstd)
   backward = 3 R C s + 3 C s + 8 R   (read dy, res_out; write dx; gamma, dgamma, dbeta; stats)
-with s = 2 bytes for bf16.
+with s = 4 bytes for fp32 and 2 for bf16.
 
 Timing: inputs are resident in HBM; W warm-up steps, then exactly K steps replayed from a
-CUDA graph (captured in chunks of steps), bracketed by a barrier and a synchronize.  Between
-steps nothing is L2-hot: the step cycles through S buffer sets whose total footprint is more
-than three times the L2 cache, and the backward of a step consumes the forward outputs of
-the set half a cycle back.  The graph launches our kernels only (2 per step).
+CUDA graph (captured in chunks of steps), bracketed by a barrier and a synchronize.  Nothing
+is L2-hot between steps: the step cycles through S buffer sets whose total footprint is more
+than three times the L2 cache (for the headline each step alone moves 7.3 GB, far more than
+L2), and the backward of a step consumes the forward outputs of the set half a cycle back.
+The graph launches our kernels only (2 per step).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Under torchrun each rank runs its own replica (replicas only: no data-path collective);
@@ -49,6 +53,14 @@ def bwd_bytes(R, C, s):
     return 3 * R * C * s + 3 * C * s + 8 * R
 
 
+def rms_fwd_bytes(R, C, s):  # read x, res; write out, res_out; gamma; rrms
+    return 4 * R * C * s + C * s + 4 * R
+
+
+def rms_bwd_bytes(R, C, s):  # read dy, res_out; write dx; gamma, dgamma; rrms
+    return 3 * R * C * s + 2 * C * s + 4 * R
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -78,19 +90,23 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def profiled_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu summary, if it
+    was taken on the current kernel sources (else None).  A capture of a row slice of the
+    workload (same width, fewer rows) is scaled to the full row count: a kernel's traffic
+    grows in proportion to the rows it processes."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
         return None
-    ent = d.get(kernel)
+    ent = d.get(f"{kernel}:{workload}")
     if not ent or ent.get("source_hash") != source_hash():
         return None
-    return ent.get("dram_bytes_per_launch")
+    from layernorm_ln_fwd_gb300 import synth
+    rows = synth.WORKLOADS[workload].rows
+    return ent["dram_bytes_per_launch"] * rows / ent.get("rows_captured", rows)
 
 
 class ClockSampler:
@@ -200,51 +216,78 @@ def max_over_ranks(world, v: float) -> float:
 
 
 # ------------------------------------------------------------------------------------------
+# The workload's description, identical in both arms' lines.
+# ------------------------------------------------------------------------------------------
+def workload_config(name: str, world: int) -> dict:
+    from layernorm_ln_fwd_gb300 import synth
+    w = synth.WORKLOADS[name]
+    s = 4 if w.dtype == "f32" else 2
+    step = fwd_bytes(w.rows, w.cols, s) + bwd_bytes(w.rows, w.cols, s)
+    return {"workload": name, "rows": w.rows, "cols": w.cols, "io_dtype": w.dtype,
+            "accumulate": "fp32", "eps": w.eps, "global_batch_rows": w.rows * world,
+            "l2": (f"inputs larger than L2: one step moves {step / 1e9:.2f} GB"
+                   if step > 1e9 else "buffer sets rotated, more than 3x L2 between reuses"),
+            "parallelism": f"replicas x{world}"}
+
+
+# ------------------------------------------------------------------------------------------
 # The reference arm: the float64 oracle on the host cores (the pages ship no runnable code).
 # ------------------------------------------------------------------------------------------
 def time_oracle(workload: str, steps: int, warmup: int, budget_s: float, target_s: float = 0.0,
                 threads: int = 0):
     """Time the oracle's fwd+bwd on the workload.  Each step covers all rows unless that
-    would overrun `budget_s`; with `target_s` > 0 the number of steps is instead chosen to
-    take about that long (the CPU-baseline sample)."""
+    would overrun `budget_s` for warm-up plus timed steps, in which case every step covers
+    the same leading slice of rows; with `target_s` > 0 the steps and the slice are instead
+    chosen so that the timed steps take about that long (the CPU-baseline sample)."""
     import numpy as np
 
     import oracle
     from layernorm_ln_fwd_gb300 import synth
     w = synth.WORKLOADS[workload]
     s = 4 if w.dtype == "f32" else 2
-    inp = synth.workload_inputs(workload, seed=0)
-    f64 = {k: v.float().numpy().astype(np.float64) for k, v in inp.items()}
     cores = threads or len(os.sched_getaffinity(0))
     oracle.build()
+    # Seeded inputs; only the rows a step can use are drawn and converted.
+    pilot = min(w.rows, 2048)
 
-    def step(rows):
+    def inputs(rows):
+        inp = synth.make_inputs(rows, w.cols, w.dtype, seed=0, x=w.x, res=w.res, dy=w.dy,
+                                gamma=w.gamma, beta=w.beta)
+        return {k: v.float().numpy().astype(np.float64) for k, v in inp.items()}
+
+    def step(f64, rows):
         f = oracle.ln_fwd(f64["x"][:rows], f64["res"][:rows], f64["gamma"], f64["beta"], w.eps,
                           io=w.dtype, threads=cores)
         oracle.ln_bwd(f64["dy"][:rows], f["res_out"], f64["gamma"], f["mean"], f["rstd"],
                       io=w.dtype, threads=cores)
 
+    f64 = inputs(pilot)
+    step(f64, pilot)
     t = time.perf_counter()
-    step(w.rows)
-    t_full = time.perf_counter() - t
-    # Size each step so that warm-up plus timed steps stay within the budget.
+    step(f64, pilot)
+    t_row = (time.perf_counter() - t) / pilot
     rows = w.rows
     if target_s > 0:
-        steps = max(1, min(100, int(target_s / max(t_full, 1e-3))))
-    elif t_full * (steps + warmup) > budget_s:
-        rows = max(64, int(w.rows * budget_s / ((steps + warmup) * t_full)))
+        rows = max(pilot, min(w.rows, int(target_s / 3 / t_row)))
+        steps = max(1, min(100, int(target_s / (t_row * rows))))
+    elif t_row * w.rows * (steps + warmup) > budget_s:
+        rows = max(pilot, int(budget_s / ((steps + warmup) * t_row)))
+    rows = min(rows, w.rows)
+    if rows > pilot:
+        f64 = inputs(rows)
     for _ in range(warmup):
-        step(rows)
+        step(f64, rows)
     t0 = time.perf_counter()
     for _ in range(steps):
-        step(rows)
+        step(f64, rows)
     dt = time.perf_counter() - t0
     nbytes = fwd_bytes(rows, w.cols, s) + bwd_bytes(rows, w.cols, s)
     gbs = nbytes * steps / dt / 1e9
     return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "rows_per_s": rows * steps / dt, "ms_per_step": dt / steps * 1e3,
-            "sample": f"{steps} step(s) of {rows} of the {w.rows} rows x {w.cols} columns "
-                      f"({w.dtype}), float64 C oracle fwd+bwd, OpenMP on {cores} threads"}
+            "sample": f"{steps} step(s) of the first {rows} of the {w.rows} rows x {w.cols} "
+                      f"columns ({w.dtype}), float64 C oracle fwd+bwd, OpenMP on {cores} "
+                      f"threads; GB/s counts the algorithmic bytes of the rows processed"}
 
 
 def run_reference(args):
@@ -252,17 +295,14 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    from layernorm_ln_fwd_gb300 import synth
-    w = synth.WORKLOADS[args.workload]
-    r = time_oracle(args.workload, args.steps, args.warmup, budget_s=120.0)
+    r = time_oracle(args.workload, args.steps, args.warmup, budget_s=150.0)
     line = {
         "impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "rows": w.rows, "cols": w.cols,
-                   "io_dtype": w.dtype, "note": "the float64 CPU oracle: the pages ship no "
-                   "runnable reference code"},
+        "config": workload_config(args.workload, world),
+        "note": "the float64 CPU oracle: the pages ship no runnable reference code",
         "rows_per_s": r["rows_per_s"],
         "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"],
                          "kind": "oracle", "sample": r["sample"]},
@@ -277,6 +317,105 @@ def run_reference(args):
 # ------------------------------------------------------------------------------------------
 # Our arm.
 # ------------------------------------------------------------------------------------------
+class Workbench:
+    """Device buffer sets of one workload and graph timing of its kernels on one stream."""
+
+    def __init__(self, name: str, rank: int, stream):
+        import torch
+
+        import layernorm_ln_fwd_gb300 as ln
+        from layernorm_ln_fwd_gb300 import synth
+        self.ln = ln
+        self.w = w = synth.WORKLOADS[name]
+        self.name = name
+        self.R, self.C, td = w.rows, w.cols, synth.torch_dtype(w.dtype)
+        self.s = 4 if w.dtype == "f32" else 2
+        self.stream = stream
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        R, C, s = self.R, self.C, self.s
+        self.set_bytes = 6 * R * C * s + 8 * R + 5 * C * s
+        nsets = max(2, -(-3 * l2 // self.set_bytes) + 1)
+        self.nsets = nsets + nsets % 2
+        self.sets = []
+        for i in range(self.nsets):  # set i draws with seed 1000 * rank + i, on the device
+            d = synth.workload_inputs(name, seed=1000 * rank + i, device="cuda")
+            d.update(out=torch.empty_like(d["x"]), res_out=torch.empty_like(d["x"]),
+                     dx=torch.empty_like(d["x"]),
+                     mean=torch.empty(R, dtype=torch.float32, device="cuda"),
+                     rstd=torch.empty(R, dtype=torch.float32, device="cuda"),
+                     dgamma=torch.empty(C, dtype=td, device="cuda"),
+                     dbeta=torch.empty(C, dtype=td, device="cuda"))
+            self.sets.append(d)
+        self.ws = torch.zeros(ln.workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+        self.fwd_b = fwd_bytes(R, C, s)
+        self.bwd_b = bwd_bytes(R, C, s)
+        with torch.cuda.stream(stream):
+            for i in range(self.nsets):
+                self.fwd(i)
+        torch.cuda.synchronize()
+
+    def fwd(self, i):
+        S = self.sets[i % self.nsets]
+        self.ln.fwd(S["x"], S["res"], S["gamma"], S["beta"], self.w.eps, out=S["out"],
+                    res_out=S["res_out"], mean=S["mean"], rstd=S["rstd"], stream=self.stream)
+
+    def bwd(self, i):
+        S = self.sets[i % self.nsets]
+        self.ln.bwd(S["dy"], S["res_out"], S["gamma"], S["mean"], S["rstd"], dx=S["dx"],
+                    dgamma=S["dgamma"], dbeta=S["dbeta"], workspace=self.ws, stream=self.stream)
+
+    def step(self, k):  # one pass of the hot path; the backward reads set k + S/2's forward
+        self.fwd(k)
+        self.bwd(k + self.nsets // 2)
+
+    def capture(self, fn, n, start=0):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for k in range(n):
+                fn(start + k)
+        return g
+
+    def time_graph(self, fn, n, repeats=5):
+        """Median over `repeats` replays of a graph of n calls of fn: us per call."""
+        import torch
+        g = self.capture(fn, n)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(repeats + 1)]
+        with torch.cuda.stream(self.stream):
+            g.replay()
+            torch.cuda.synchronize()
+            ev[0].record(self.stream)
+            for r in range(repeats):
+                g.replay()
+                ev[r + 1].record(self.stream)
+        torch.cuda.synchronize()
+        reps = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / n for r in range(repeats))
+        return reps[len(reps) // 2], reps
+
+    def kernels(self, n, peak):
+        """Forward, backward and step times of this workload (graphs of n launches)."""
+        out = {}
+        for name, fn, nb in (("fwd", self.fwd, self.fwd_b),
+                             ("bwd", lambda k: self.bwd(k + self.nsets // 2), self.bwd_b),
+                             ("step", self.step, self.fwd_b + self.bwd_b)):
+            us, reps = self.time_graph(fn, n)
+            gbs = nb / us / 1e3
+            out[name] = {"us": us, "algorithmic_bytes": nb, "gbs": gbs,
+                         "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / ROOFLINE_NOMINAL_GBS,
+                         "repeats_us": [round(v, 3) for v in reps], "launches_per_repeat": n}
+        out["rows_per_s"] = self.R / (out["step"]["us"] * 1e-6)
+        out["dominant"] = "ln_fwd" if out["fwd"]["us"] >= out["bwd"]["us"] else "ln_bwd"
+        out["buffer_sets"] = self.nsets
+        return out
+
+    def free(self):
+        import torch
+        self.sets = []
+        self.ws = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
 def run_ours(args):
     import torch
 
@@ -286,74 +425,34 @@ def run_ours(args):
 
     lnbuild.build()
     world, rank, local = dist_setup()
-    w = synth.WORKLOADS[args.workload]
-    R, C, td = w.rows, w.cols, synth.torch_dtype(w.dtype)
-    s = 4 if w.dtype == "f32" else 2
-    props = torch.cuda.get_device_properties(local)
-    l2 = props.L2_cache_size
-    step_bytes = fwd_bytes(R, C, s) + bwd_bytes(R, C, s)
-    set_bytes = 6 * R * C * s + 8 * R + 5 * C * s
-    nsets = max(4, -(-3 * l2 // set_bytes) + 1)
-    nsets += nsets % 2
-
-    # Seeded inputs (set i uses seed i, rank-offset so replicas differ), resident in HBM.
-    sets = []
-    for i in range(nsets):
-        inp = synth.workload_inputs(args.workload, seed=1000 * rank + i)
-        d = {k: v.cuda() for k, v in inp.items()}
-        d.update(out=torch.empty_like(d["x"]), res_out=torch.empty_like(d["x"]),
-                 dx=torch.empty_like(d["x"]),
-                 mean=torch.empty(R, dtype=torch.float32, device="cuda"),
-                 rstd=torch.empty(R, dtype=torch.float32, device="cuda"),
-                 dgamma=torch.empty(C, dtype=td, device="cuda"),
-                 dbeta=torch.empty(C, dtype=td, device="cuda"))
-        sets.append(d)
-    ws = torch.zeros(ln.workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+    peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream()
-
-    def fwd(i):
-        S = sets[i % nsets]
-        ln.fwd(S["x"], S["res"], S["gamma"], S["beta"], w.eps, out=S["out"],
-               res_out=S["res_out"], mean=S["mean"], rstd=S["rstd"], stream=stream)
-
-    def bwd(i):
-        S = sets[i % nsets]
-        ln.bwd(S["dy"], S["res_out"], S["gamma"], S["mean"], S["rstd"], dx=S["dx"],
-               dgamma=S["dgamma"], dbeta=S["dbeta"], workspace=ws, stream=stream)
-
-    def step(k):  # one pass of the hot path; the backward reads set k + S/2's forward
-        fwd(k)
-        bwd(k + nsets // 2)
+    wb = Workbench(args.workload, rank, stream)
+    R, C = wb.R, wb.C
+    step_bytes = wb.fwd_b + wb.bwd_b
 
     with torch.cuda.stream(stream):
-        for i in range(nsets):
-            fwd(i)
         for k in range(max(args.warmup, 3)):
-            step(k)
+            wb.step(k)
     torch.cuda.synchronize()
-
-    def capture(fn, n, start):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(n):
-                fn(start + k)
-        return g
-
     chunk = min(args.steps, 500)
     while args.steps % chunk:
         chunk -= 1
-    g_step = capture(step, chunk, 0)
+    g_step = wb.capture(wb.step, chunk, 0)
     with torch.cuda.stream(stream):  # replay() launches on the current stream
         for _ in range(2):
             g_step.replay()
     torch.cuda.synchronize()
 
+    props = torch.cuda.get_device_properties(local)
     uuid = getattr(props, "uuid", None)
     sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-")
                            else (str(uuid) if uuid is not None else local))
     if rank == 0:
         sampler.start()
-    # ---- timed region: exactly K steps ----
+    # ---- warm-up, then the timed region: exactly K steps ----
+    with torch.cuda.stream(stream):
+        g_step.replay()  # untimed: brings the clocks up right before the timed steps
     barrier(world)
     torch.cuda.synchronize()
     sampler.begin()
@@ -370,58 +469,18 @@ def run_ours(args):
     ms_total = max_over_ranks(world, e0.elapsed_time(e1))
     ms_step = ms_total / args.steps
 
-    # ---- per-kernel launch durations (same stream, same rotation, separate loops): the
-    # median of 5 repeats of a graph of nk launches ----
-    nk = min(args.steps, 400)
-    kern = {}
-    for name, fn, nb in (("fwd", fwd, fwd_bytes(R, C, s)), ("bwd", lambda k: bwd(k + nsets // 2), bwd_bytes(R, C, s))):
-        g = capture(fn, nk, 0)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        with torch.cuda.stream(stream):
-            g.replay()
-            torch.cuda.synchronize()
-            ev[0].record(stream)
-            for r in range(5):
-                g.replay()
-                ev[r + 1].record(stream)
-        torch.cuda.synchronize()
-        reps_us = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / nk for r in range(5))
-        us = reps_us[2]
-        kern[name] = {"us_per_launch": us, "algorithmic_bytes": nb, "gbs": nb / us / 1e3,
-                      "repeats_us": [round(v, 3) for v in reps_us], "launches_per_repeat": nk}
-    # ---- torch elementwise kernels moving the same bytes, for scale at this size: the
-    # forward's 2 reads + 2 writes as two copies, the backward's 2 reads + 1 write as an add
-    # (same buffer rotation, same graph timing; not part of the hot path) ----
-    def ref_fwd(i):
-        S = sets[i % nsets]
-        S["out"].copy_(S["x"])
-        S["dx"].copy_(S["res"])
-
-    def ref_bwd(i):
-        S = sets[(i + nsets // 2) % nsets]
-        torch.add(S["dy"], S["res_out"], out=S["dx"])
-
-    same_bytes = {}
-    for name, fn, nb in (("fwd", ref_fwd, fwd_bytes(R, C, s)), ("bwd", ref_bwd, bwd_bytes(R, C, s))):
-        g = capture(fn, nk, 0)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        with torch.cuda.stream(stream):
-            g.replay()
-            torch.cuda.synchronize()
-            ev[0].record(stream)
-            for r in range(5):
-                g.replay()
-                ev[r + 1].record(stream)
-        torch.cuda.synchronize()
-        us = sorted(ev[r].elapsed_time(ev[r + 1]) * 1e3 / nk for r in range(5))[2]
-        same_bytes[name] = {"us": us, "gbs": nb / us / 1e3,
-                            "kernel": "2 x torch copy_" if name == "fwd" else "torch.add"}
+    # ---- per-kernel launch durations of the headline (same stream, same rotation) ----
+    nk = max(min(args.steps, 400), 10)
+    head = wb.kernels(nk, peak)
+    kern = {k: {"us_per_launch": head[k]["us"], "algorithmic_bytes": head[k]["algorithmic_bytes"],
+                "gbs": head[k]["gbs"], "repeats_us": head[k]["repeats_us"],
+                "launches_per_repeat": nk} for k in ("fwd", "bwd")}
     sampler.stop()
 
     # ---- end to end through the public API, host buffers, copies inside the timed region ----
-    e2e_steps = min(args.steps, 200)
-    host = {k: sets[0][k].cpu().pin_memory() for k in ("x", "res", "dy", "gamma", "beta")}
-    outs_h = {k: torch.empty(sets[0][k].shape, dtype=sets[0][k].dtype).pin_memory()
+    e2e_steps = max(2, min(args.steps, 200 if step_bytes < 1e9 else 10))
+    host = {k: wb.sets[0][k].cpu().pin_memory() for k in ("x", "res", "dy", "gamma", "beta")}
+    outs_h = {k: torch.empty(wb.sets[0][k].shape, dtype=wb.sets[0][k].dtype).pin_memory()
               for k in ("out", "res_out", "dx", "mean", "rstd", "dgamma", "dbeta")}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
@@ -435,7 +494,7 @@ def run_ours(args):
 
     def e2e_step(k):
         b = k % 2
-        dev = sets[b]
+        dev = wb.sets[b]
         with torch.cuda.stream(up):
             if k >= 2:
                 up.wait_event(ev_free[b])
@@ -443,9 +502,9 @@ def run_ours(args):
                 dev[name].copy_(t, non_blocking=True)
             ev_in[b].record(up)
         stream.wait_event(ev_in[b])
-        fwd(b)
+        wb.fwd(b)
         ln.bwd(dev["dy"], dev["res_out"], dev["gamma"], dev["mean"], dev["rstd"],
-               dx=dev["dx"], dgamma=dev["dgamma"], dbeta=dev["dbeta"], workspace=ws,
+               dx=dev["dx"], dgamma=dev["dgamma"], dbeta=dev["dbeta"], workspace=wb.ws,
                stream=stream)
         ev_done[b].record(stream)
         with torch.cuda.stream(down):
@@ -454,7 +513,7 @@ def run_ours(args):
                 t.copy_(dev[name], non_blocking=True)
             ev_free[b].record(down)
 
-    for k in range(4):  # warm-up
+    for k in range(2):  # warm-up
         e2e_step(k)
     torch.cuda.synchronize()
     barrier(world)
@@ -464,32 +523,41 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(world, time.perf_counter() - t0)
     barrier(world)
+    del host, outs_h
+    wb.free()
+
+    # ---- every workload: forward, backward and step times, same method ----
+    workloads = {}
+    for name in synth.WORKLOADS:
+        if name == args.workload:
+            workloads[name] = head
+            continue
+        other = Workbench(name, rank, stream)
+        workloads[name] = other.kernels(200, peak)
+        other.free()
 
     if rank != 0:
         return 0
-    peak, peak_kind = measured_peak()
     value = world * step_bytes * args.steps / (ms_total * 1e-3) / 1e9
     dom = max(kern, key=lambda k: kern[k]["us_per_launch"])
     kname = {"fwd": "ln_fwd", "bwd": "ln_bwd"}[dom]
     achieved = kern[dom]["gbs"]
-    cpu = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=10.0)
+    cpu = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=12.0)
     cpu1 = time_oracle(args.workload, steps=1, warmup=0, budget_s=60.0, target_s=4.0, threads=1)
     clocks = sampler.summary()
+    config = workload_config(args.workload, world)
+    config["timing"] = f"CUDA graph of {chunk} steps replayed {args.steps // chunk} times"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",  # fp32 arithmetic (io_dtype: storage)
-        "config": {"workload": args.workload, "rows": R, "cols": C, "io_dtype": w.dtype,
-                   "accumulate": "fp32", "global_batch_rows": R * world,
-                   "l2": f"rotating {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB > "
-                         f"3x L2 ({l2 / 1e6:.0f} MB); backward reads the set half a cycle back",
-                   "timing": f"CUDA graph of {chunk} steps replayed {args.steps // chunk} times",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(args.workload, world),
+        "timing": config["timing"],
         "rows_per_s": world * R * args.steps / (ms_total * 1e-3),
         "frac_of_8tbs": value / world / ROOFLINE_NOMINAL_GBS,
         "kernels": kern,
-        "same_bytes_torch": same_bytes,
+        "workloads": workloads,
         "clocks": clocks,
         "e2e": {"value": world * step_bytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -497,8 +565,9 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": profiled_traffic(kname)},
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst figure: kernel timed in "
+                                  f"graphs of {nk} launches)",
+                     "traffic": profiled_traffic(kname, args.workload)},
         "cpu_baseline": {"value": cpu["value"], "unit": "GB/s", "cores": cpu["cores"],
                          "kind": "oracle", "sample": cpu["sample"],
                          "rows_per_s": cpu["rows_per_s"],
@@ -511,12 +580,13 @@ def run_ours(args):
 
 
 def main():
+    from layernorm_ln_fwd_gb300 import synth
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="bf16_8192x768")
+    ap.add_argument("--workload", default=synth.BENCH_WORKLOAD, choices=list(synth.WORKLOADS))
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
