@@ -4,7 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl
 legs of ``bench.py`` may import this package.  The CUDA library never calls it and shares no
 code with it.
 
-Two independent implementations of the same definitions live here:
+It covers the fused residual-add + LayerNorm (``ln_fwd``, ``ln_bwd``) and the fused
+residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``).  Two independent implementations of the
+same definitions live here:
 
 * ``ln_oracle.c`` (float64 C, OpenMP over rows; built into ``libln_oracle.so`` by
   :func:`build`) -- the oracle proper, fast enough for the full-size configurations;
@@ -73,6 +75,12 @@ def _load():
             lib.oracle_ln_bwd.restype = None
             lib.oracle_ln_bwd_dx_slides.argtypes = [d, d, d, d, d, i64, i64, d, ctypes.c_int]
             lib.oracle_ln_bwd_dx_slides.restype = None
+            lib.oracle_rms_fwd.argtypes = [d, d, d, ctypes.c_double, i64, i64, ctypes.c_int,
+                                           d, d, d, ctypes.c_int]
+            lib.oracle_rms_fwd.restype = None
+            lib.oracle_rms_bwd.argtypes = [d, d, d, d, i64, i64, ctypes.c_int, d, d,
+                                           ctypes.c_int]
+            lib.oracle_rms_bwd.restype = None
             lib.oracle_round_io.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_round_io.restype = ctypes.c_double
             lib.oracle_max_threads.argtypes = []
@@ -168,3 +176,42 @@ def ln_bwd_dx_slides(dy, xr, gamma, mean, rstd, threads: int = 0):
     _load().oracle_ln_bwd_dx_slides(_ptr(dy), _ptr(xr), _ptr(gamma), _ptr(mean), _ptr(rstd),
                                     rows, cols, _ptr(dx), int(threads))
     return dx
+
+
+def rms_fwd(x, res, gamma, eps: float, io: str = "f64", threads: int = 0, want_out: bool = True,
+            want_res_out: bool = True):
+    """Forward of the fused residual-add + RMSNorm ("GPU Performance from First Principles",
+    section 6.1): s = x + res (rounded to ``io``), r = 1/sqrt(mean(s^2) + eps),
+    out = gamma * s * r.  Returns ``out``, ``res_out`` (rounded to ``io``) and ``rrms`` (r,
+    float64, unrounded)."""
+    x = _f64(x)
+    rows, cols = x.shape
+    res = _f64(res)
+    gamma = _f64(gamma)
+    assert gamma.shape == (cols,)
+    if res is not None:
+        assert res.shape == x.shape
+    out = np.empty((rows, cols)) if want_out else None
+    res_out = np.empty((rows, cols)) if want_res_out else None
+    rrms = np.empty(rows)
+    _load().oracle_rms_fwd(_ptr(x), _ptr(res), _ptr(gamma), float(eps), rows, cols,
+                           IO_CODES[io], _ptr(out), _ptr(res_out), _ptr(rrms), int(threads))
+    return {"out": out, "res_out": res_out, "rrms": rrms}
+
+
+def rms_bwd(dy, xr, gamma, rrms, io: str = "f64", threads: int = 0, want_dx: bool = True,
+            want_dgamma: bool = True):
+    """Backward of the fused residual-add + RMSNorm: ``dx`` = r (g - shat sum(g shat)/m) with
+    shat = xr * r, g = gamma * dy, and ``dgamma`` = sum over rows of dy * shat, rounded to
+    ``io``.  ``xr`` is the tensor the forward normalised."""
+    dy = _f64(dy)
+    rows, cols = dy.shape
+    xr = _f64(xr)
+    gamma = _f64(gamma)
+    rrms = _f64(rrms)
+    assert xr.shape == dy.shape and gamma.shape == (cols,) and rrms.shape == (rows,)
+    dx = np.empty((rows, cols)) if want_dx else None
+    dgamma = np.empty(cols) if want_dgamma else None
+    _load().oracle_rms_bwd(_ptr(dy), _ptr(xr), _ptr(gamma), _ptr(rrms), rows, cols,
+                           IO_CODES[io], _ptr(dx), _ptr(dgamma), int(threads))
+    return {"dx": dx, "dgamma": dgamma}

@@ -2,8 +2,9 @@
  * ln_oracle.c -- TEST INFRASTRUCTURE ONLY.
  *
  * A plain, slow, float64 CPU oracle for the fused residual-add + LayerNorm forward and
- * backward.  Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
- * load it; the CUDA library never links or calls it, and it shares no code with it.
+ * backward (and, at the end of the file, the fused residual-add + RMSNorm ones).  Only the
+ * test suite, the smoke check and the benchmark's CPU-baseline leg may load it; the CUDA
+ * library never links or calls it, and it shares no code with it.
  *
  * Sources (page titles and sections; the pages are course notes and blog posts):
  *  - Forward definition, per row of length m:
@@ -237,6 +238,102 @@ void oracle_ln_bwd_dx_slides(const double* dy, const double* xr, const double* g
             double alpha = ((x[j] - mu) * mu - sigma * sigma) / s3;
             double beta = (mu - x[j]) / s3;
             dx[r * cols + j] = g / sigma + alpha * sum_g + beta * sum_gx;
+        }
+    }
+}
+
+/*
+ * Fused residual-add + RMSNorm, forward.  "GPU Performance from First Principles", section
+ * 6.1 (operator fusion, the "fused add + RMSNorm" item) and exercise 4 of the same page: one
+ * kernel reads x and the residual and writes the new residual stream and the normalised
+ * result.  The page names the operation without printing its formula; the plainest reading,
+ * taken here, is the usual RMSNorm: no mean is subtracted, no shift is added, eps is added to
+ * the mean square inside the square root, and a per-column gain gamma scales the result.
+ * Per row of length m:
+ *    s = x + res (rounded to the stored precision, as for LayerNorm above; it is written
+ *    out and it is what gets normalised),  ms = mean(s^2),  r = 1 / sqrt(ms + eps),
+ *    out_i = gamma_i * s_i * r.
+ * Outputs: out, res_out [rows, cols] (either may be NULL), rrms [rows] (r, unrounded).
+ */
+void oracle_rms_fwd(const double* x, const double* res, const double* gamma, double eps,
+                    int64_t rows, int64_t cols, int io, double* out, double* res_out,
+                    double* rrms, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * cols;
+        const double* rr = res ? res + r * cols : NULL;
+        double sq = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double s = round_io(rr ? xr[j] + rr[j] : xr[j], io);
+            if (res_out) res_out[r * cols + j] = s;
+            sq += s * s;
+        }
+        double rs = 1.0 / sqrt(sq / (double)cols + eps);
+        rrms[r] = rs;
+        if (out) {
+            for (int64_t j = 0; j < cols; ++j) {
+                double s = round_io(rr ? xr[j] + rr[j] : xr[j], io);
+                out[r * cols + j] = round_io(gamma[j] * (s * rs), io);
+            }
+        }
+    }
+}
+
+/*
+ * Fused residual-add + RMSNorm, backward, from the forward above by the chain rule
+ * (d r / d s_j = -r^3 s_j / m).  With shat = s * r and g = gamma * dy:
+ *    dx_j = r * (g_j - shat_j * sum_i g_i shat_i / m)   (the gradient of s, hence of x and res)
+ *    dgamma_j = sum over rows of dy_j * shat_j.
+ * xr is the tensor the forward normalised (its res_out, or x without a residual).  Outputs:
+ * dx [rows, cols] (may be NULL), dgamma [cols] (may be NULL), rounded to `io`.
+ */
+void oracle_rms_bwd(const double* dy, const double* xr, const double* gamma, const double* rrms,
+                    int64_t rows, int64_t cols, int io, double* dx, double* dgamma,
+                    int nthreads) {
+    set_threads(nthreads);
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            const double* d = dy + r * cols;
+            const double* s = xr + r * cols;
+            double rs = rrms[r];
+            double sum_gs = 0.0;
+            for (int64_t j = 0; j < cols; ++j) sum_gs += gamma[j] * d[j] * (s[j] * rs);
+            for (int64_t j = 0; j < cols; ++j) {
+                double shat = s[j] * rs;
+                double v = rs * (gamma[j] * d[j] - shat * sum_gs / (double)cols);
+                dx[r * cols + j] = round_io(v, io);
+            }
+        }
+    }
+    if (dgamma) {
+        /* Each thread owns a contiguous slice of columns and walks the rows in order. */
+#pragma omp parallel
+        {
+            int t = 0, nt = 1;
+#ifdef _OPENMP
+            t = omp_get_thread_num();
+            nt = omp_get_num_threads();
+#endif
+            int64_t j0 = cols * t / nt, j1 = cols * (t + 1) / nt;
+            int64_t w = j1 - j0;
+            /* Running sums of the slice, every column summed over rows 0, 1, ... in order. */
+            double* acc = w > 0 ? (double*)calloc((size_t)w, sizeof(double)) : NULL;
+            if (acc) {
+                for (int64_t r = 0; r < rows; ++r)
+                    for (int64_t j = j0; j < j1; ++j)
+                        acc[j - j0] += dy[r * cols + j] * (xr[r * cols + j] * rrms[r]);
+                for (int64_t j = j0; j < j1; ++j) dgamma[j] = round_io(acc[j - j0], io);
+            } else {
+                for (int64_t j = j0; j < j1; ++j) {
+                    double a = 0.0;
+                    for (int64_t r = 0; r < rows; ++r)
+                        a += dy[r * cols + j] * (xr[r * cols + j] * rrms[r]);
+                    dgamma[j] = round_io(a, io);
+                }
+            }
+            free(acc);
         }
     }
 }

@@ -5,7 +5,9 @@ independent code so that the two can be compared:
 
 * forward ("Accelerating Transformer on GPU (II): Training with LightSeq2", section 2.1;
   residual sum stored then normalised, "llm.c: the llmc/ CUDA kernel layer", section 3.2);
-* backward, HW4 form, and dgamma/dbeta as column sums (same lecture, sections 2.1, 2.4).
+* backward, HW4 form, and dgamma/dbeta as column sums (same lecture, sections 2.1, 2.4);
+* the fused residual-add + RMSNorm forward and backward ("GPU Performance from First
+  Principles", section 6.1).
 """
 from __future__ import annotations
 
@@ -64,3 +66,27 @@ def ln_bwd(dy, xr, gamma, mean, rstd, io: str = "f64"):
     dgamma = (dy * xhat).sum(axis=0)
     dbeta = dy.sum(axis=0)
     return {"dx": round_io(dx, io), "dgamma": round_io(dgamma, io), "dbeta": round_io(dbeta, io)}
+
+
+def rms_fwd(x, res, gamma, eps: float, io: str = "f64"):
+    """Fused residual-add + RMSNorm forward ("GPU Performance from First Principles", section
+    6.1): s = x + res rounded to ``io``; out = gamma * s / sqrt(mean(s^2) + eps)."""
+    x = np.asarray(x, dtype=np.float64)
+    s = x if res is None else x + np.asarray(res, dtype=np.float64)
+    s = round_io(s, io)
+    rrms = 1.0 / np.sqrt((s * s).mean(axis=1) + eps)
+    out = round_io(np.asarray(gamma, np.float64)[None, :] * (s * rrms[:, None]), io)
+    return {"out": out, "res_out": s, "rrms": rrms}
+
+
+def rms_bwd(dy, xr, gamma, rrms, io: str = "f64"):
+    dy = np.asarray(dy, dtype=np.float64)
+    xr = np.asarray(xr, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    rrms = np.asarray(rrms, dtype=np.float64)
+    m = dy.shape[1]
+    shat = xr * rrms[:, None]
+    g = gamma[None, :] * dy
+    dx = rrms[:, None] * (g - shat * (g * shat).sum(axis=1, keepdims=True) / m)
+    dgamma = (dy * shat).sum(axis=0)
+    return {"dx": round_io(dx, io), "dgamma": round_io(dgamma, io)}
