@@ -4,8 +4,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / ``--impl
 legs of ``bench.py`` may import this package.  The CUDA library never calls it and shares no
 code with it.
 
-It covers the fused residual-add + LayerNorm (``ln_fwd``, ``ln_bwd``) and the fused
-residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``).  Two independent implementations of the
+It covers the fused residual-add + LayerNorm (``ln_fwd``, ``ln_bwd``), the fused
+residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``) and the fused softmax (``softmax_fwd``,
+``softmax_bwd``).  Two independent implementations of the
 same definitions live here:
 
 * ``ln_oracle.c`` (float64 C, OpenMP over rows; built into ``libln_oracle.so`` by
@@ -81,6 +82,12 @@ def _load():
             lib.oracle_rms_bwd.argtypes = [d, d, d, d, i64, i64, ctypes.c_int, d, d,
                                            ctypes.c_int]
             lib.oracle_rms_bwd.restype = None
+            lib.oracle_softmax_fwd.argtypes = [d, d, i64, ctypes.c_double, i64, i64,
+                                               ctypes.c_int, d, ctypes.c_int]
+            lib.oracle_softmax_fwd.restype = None
+            lib.oracle_softmax_bwd.argtypes = [d, d, ctypes.c_double, i64, i64, ctypes.c_int, d,
+                                               ctypes.c_int]
+            lib.oracle_softmax_bwd.restype = None
             lib.oracle_round_io.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_round_io.restype = ctypes.c_double
             lib.oracle_max_threads.argtypes = []
@@ -215,3 +222,33 @@ def rms_bwd(dy, xr, gamma, rrms, io: str = "f64", threads: int = 0, want_dx: boo
     _load().oracle_rms_bwd(_ptr(dy), _ptr(xr), _ptr(gamma), _ptr(rrms), rows, cols,
                            IO_CODES[io], _ptr(dx), _ptr(dgamma), int(threads))
     return {"dx": dx, "dgamma": dgamma}
+
+
+def softmax_fwd(x, mask=None, scale: float = 1.0, io: str = "f64", threads: int = 0):
+    """Fused softmax forward ("Accelerating Transformer on GPU (I)", section 4.1): per row,
+    y = softmax(scale * x + mask), the additive mask's rows repeating every mask.shape[0]
+    rows.  Returns y rounded to ``io``."""
+    x = _f64(x)
+    rows, cols = x.shape
+    mask = _f64(mask)
+    mask_rows = 1
+    if mask is not None:
+        assert mask.ndim == 2 and mask.shape[1] == cols
+        mask_rows = mask.shape[0]
+    y = np.empty((rows, cols))
+    _load().oracle_softmax_fwd(_ptr(x), _ptr(mask), mask_rows, float(scale), rows, cols,
+                               IO_CODES[io], _ptr(y), int(threads))
+    return y
+
+
+def softmax_bwd(dy, y, scale: float = 1.0, io: str = "f64", threads: int = 0):
+    """Fused softmax backward ("Accelerating Transformer on GPU (II)", section 3.1):
+    dx = scale * y * (dy - sum(dy * y)), rounded to ``io``."""
+    dy = _f64(dy)
+    rows, cols = dy.shape
+    y = _f64(y)
+    assert y.shape == dy.shape
+    dx = np.empty((rows, cols))
+    _load().oracle_softmax_bwd(_ptr(dy), _ptr(y), float(scale), rows, cols, IO_CODES[io],
+                               _ptr(dx), int(threads))
+    return dx

@@ -337,3 +337,52 @@ void oracle_rms_bwd(const double* dy, const double* xr, const double* gamma, con
         }
     }
 }
+
+/*
+ * Fused softmax, forward ("Accelerating Transformer on GPU (I)", section 4.1: scale, add the
+ * mask, row maximum, exponentiate the difference, row sum, divide -- one kernel).  Per row r
+ * of length m:
+ *    z_j = scale * x_j + mask[(r % mask_rows) * m + j]   (no mask term when mask is NULL)
+ *    y_j = exp(z_j - max z) / sum_i exp(z_i - max z).
+ * The mask is additive (0 keeps an entry, -inf removes it) and its rows repeat every
+ * mask_rows rows (an attention mask of [L, L] over rows batch x heads x L).  A row whose
+ * entries are all -inf has no defined softmax; the definition gives NaN (0 / 0) there.
+ * Output y [rows, cols], rounded to `io`.
+ */
+void oracle_softmax_fwd(const double* x, const double* mask, int64_t mask_rows, double scale,
+                        int64_t rows, int64_t cols, int io, double* y, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * cols;
+        const double* mr = mask ? mask + (r % mask_rows) * cols : NULL;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j) {
+            double z = scale * xr[j] + (mr ? mr[j] : 0.0);
+            if (z > mx) mx = z;
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j) sum += exp(scale * xr[j] + (mr ? mr[j] : 0.0) - mx);
+        for (int64_t j = 0; j < cols; ++j)
+            y[r * cols + j] = round_io(exp(scale * xr[j] + (mr ? mr[j] : 0.0) - mx) / sum, io);
+    }
+}
+
+/*
+ * Fused softmax, backward ("Accelerating Transformer on GPU (II)", section 3.1: only y is
+ * needed, and one row reduction): with s = sum_i dy_i y_i,
+ *    dx_j = scale * y_j * (dy_j - s)
+ * (scale: the forward's factor on x; the mask has no gradient).  Output dx, rounded to `io`.
+ */
+void oracle_softmax_bwd(const double* dy, const double* y, double scale, int64_t rows,
+                        int64_t cols, int io, double* dx, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* d = dy + r * cols;
+        const double* yr = y + r * cols;
+        double s = 0.0;
+        for (int64_t j = 0; j < cols; ++j) s += d[j] * yr[j];
+        for (int64_t j = 0; j < cols; ++j) dx[r * cols + j] = round_io(scale * yr[j] * (d[j] - s), io);
+    }
+}

@@ -7,7 +7,9 @@ independent code so that the two can be compared:
   residual sum stored then normalised, "llm.c: the llmc/ CUDA kernel layer", section 3.2);
 * backward, HW4 form, and dgamma/dbeta as column sums (same lecture, sections 2.1, 2.4);
 * the fused residual-add + RMSNorm forward and backward ("GPU Performance from First
-  Principles", section 6.1).
+  Principles", section 6.1);
+* the fused softmax forward ("Accelerating Transformer on GPU (I)", section 4.1) and backward
+  ("... (II)", section 3.1).
 """
 from __future__ import annotations
 
@@ -90,3 +92,21 @@ def rms_bwd(dy, xr, gamma, rrms, io: str = "f64"):
     dx = rrms[:, None] * (g - shat * (g * shat).sum(axis=1, keepdims=True) / m)
     dgamma = (dy * shat).sum(axis=0)
     return {"dx": round_io(dx, io), "dgamma": round_io(dgamma, io)}
+
+
+def softmax_fwd(x, mask=None, scale: float = 1.0, io: str = "f64"):
+    """Fused softmax forward ("Accelerating Transformer on GPU (I)", section 4.1)."""
+    z = scale * np.asarray(x, dtype=np.float64)
+    if mask is not None:
+        mask = np.asarray(mask, dtype=np.float64)
+        z = z + np.tile(mask, (-(-z.shape[0] // mask.shape[0]), 1))[: z.shape[0]]
+    with np.errstate(invalid="ignore"):
+        e = np.exp(z - z.max(axis=1, keepdims=True))
+        return round_io(e / e.sum(axis=1, keepdims=True), io)
+
+
+def softmax_bwd(dy, y, scale: float = 1.0, io: str = "f64"):
+    """Fused softmax backward ("Accelerating Transformer on GPU (II)", section 3.1)."""
+    dy = np.asarray(dy, dtype=np.float64)
+    y = np.asarray(y, dtype=np.float64)
+    return round_io(scale * y * (dy - (dy * y).sum(axis=1, keepdims=True)), io)
