@@ -6,7 +6,8 @@ statistics, normalisation) and the backward (dx, dgamma, dbeta).  The headline l
 the largest workload, fp32 262144 x 1000 (the metric names no configuration); the same line
 carries every workload's forward, backward and step times under ``workloads`` (fp32 64x768,
 the GPT-2-shaped bf16 8192x768 and 8192x1280, the wide bf16 4096x8192 with mean 100, and
-the headline), all on seeded synthetic inputs.
+the headline), and those of the other fused row operations (the fused add + RMSNorm at the
+GPT-2 shapes, the fused softmax of causal attention scores), all on seeded synthetic inputs.
 
 Metric: achieved HBM GB/s of the algorithmic bytes (and rows/s), next to the 8 TB/s HBM
 roofline and the measured copy bandwidth.  Algorithmic bytes per step:
@@ -80,7 +81,8 @@ def source_hash() -> str:
     csrc = os.path.join(ROOT, "layernorm_ln_fwd_gb300", "csrc")
     # The kernels and their launch planning; the API layer (argument checks, workspaces,
     # status handling) does not change what a kernel moves.
-    for name in ("ln_bwd.cu", "ln_device.cuh", "ln_fwd.cu", "ln_internal.h"):
+    for name in ("ln_bwd.cu", "ln_bwd_kernels.cuh", "ln_device.cuh", "ln_fwd.cu",
+                 "ln_fwd_kernels.cuh", "ln_internal.h", "rms_bwd.cu", "rms_fwd.cu"):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -416,6 +418,76 @@ class Workbench:
         torch.cuda.empty_cache()
 
 
+def softmax_fwd_bytes(R, C, L, s):  # read x, the mask once; write y
+    return 2 * R * C * s + L * C * s
+
+
+def softmax_bwd_bytes(R, C, s):  # read dy, y; write dx
+    return 3 * R * C * s
+
+
+class OpBench(Workbench):
+    """Buffer sets and graph timing of one of the other fused row operations (the fused add +
+    RMSNorm, the fused softmax): forward and backward launches on rotating sets."""
+
+    def __init__(self, name: str, rank: int, stream):  # noqa: D401  (no super().__init__)
+        import torch
+
+        import layernorm_ln_fwd_gb300 as ln
+        from layernorm_ln_fwd_gb300 import synth
+        self.ln = ln
+        self.name = name
+        self.op = op = synth.OP_WORKLOADS[name]
+        self.R, self.C = R, C = op["rows"], op["cols"]
+        td = synth.torch_dtype(op["dtype"])
+        self.s = s = 4 if op["dtype"] == "f32" else 2
+        self.stream = stream
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        if op["kind"] == "rms":
+            self.set_bytes = 6 * R * C * s
+            self.fwd_b, self.bwd_b = rms_fwd_bytes(R, C, s), rms_bwd_bytes(R, C, s)
+        else:
+            self.set_bytes = 4 * R * C * s
+            self.fwd_b = softmax_fwd_bytes(R, C, op["mask_rows"], s)
+            self.bwd_b = softmax_bwd_bytes(R, C, s)
+        nsets = max(2, -(-3 * l2 // self.set_bytes) + 1)
+        self.nsets = nsets + nsets % 2
+        self.sets = []
+        for i in range(self.nsets):
+            d = synth.make_inputs(R, C, op["dtype"], seed=1000 * rank + i, device="cuda",
+                                  x=("normal", 0.0, 3.0 if op["kind"] == "softmax" else 1.0))
+            if op["kind"] == "rms":
+                d.update(out=torch.empty_like(d["x"]), res_out=torch.empty_like(d["x"]),
+                         dx=torch.empty_like(d["x"]),
+                         rrms=torch.empty(R, dtype=torch.float32, device="cuda"),
+                         dgamma=torch.empty(C, dtype=td, device="cuda"))
+            else:
+                d.update(y=torch.empty_like(d["x"]), dx=torch.empty_like(d["x"]),
+                         mask=synth.causal_mask(op["mask_rows"], C, op["dtype"], device="cuda"))
+            self.sets.append(d)
+        self.ws = torch.zeros(ln.workspace_bytes(R, C), dtype=torch.uint8, device="cuda")
+        with torch.cuda.stream(stream):
+            for i in range(self.nsets):
+                self.fwd(i)
+        torch.cuda.synchronize()
+
+    def fwd(self, i):
+        S = self.sets[i % self.nsets]
+        if self.op["kind"] == "rms":
+            self.ln.rms_fwd(S["x"], S["res"], S["gamma"], 1e-5, out=S["out"],
+                            res_out=S["res_out"], rrms=S["rrms"], stream=self.stream)
+        else:
+            self.ln.softmax_fwd(S["x"], S["mask"], self.op["scale"], y=S["y"], stream=self.stream)
+
+    def bwd(self, i):
+        S = self.sets[i % self.nsets]
+        if self.op["kind"] == "rms":
+            self.ln.rms_bwd(S["dy"], S["res_out"], S["gamma"], S["rrms"], dx=S["dx"],
+                            dgamma=S["dgamma"], workspace=self.ws, stream=self.stream)
+        else:
+            self.ln.softmax_bwd(S["dy"], S["y"], self.op["scale"], dx=S["dx"], stream=self.stream)
+
+
 def run_ours(args):
     import torch
 
@@ -533,6 +605,10 @@ def run_ours(args):
             workloads[name] = head
             continue
         other = Workbench(name, rank, stream)
+        workloads[name] = other.kernels(200, peak)
+        other.free()
+    for name in synth.OP_WORKLOADS:  # the other fused row operations
+        other = OpBench(name, rank, stream)
         workloads[name] = other.kernels(200, peak)
         other.free()
 

@@ -1,5 +1,7 @@
 /*
- * ln.h -- C ABI of the GB300 (sm_103a) fused residual-add + LayerNorm library (libln.so).
+ * ln.h -- C ABI of the GB300 (sm_103a) fused residual-add + LayerNorm library (libln.so),
+ * with the fused residual-add + RMSNorm (ln_rms_*) and the fused row softmax (ln_softmax_*)
+ * alongside.
  *
  * The library computes, for a row-major [rows, cols] problem:
  *
@@ -161,6 +163,106 @@ ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const l
                          const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
                          ln_bf16* dbeta, int64_t rows, int64_t cols, void* workspace,
                          size_t workspace_bytes, ln_stream_t stream);
+
+/*
+ * Forward of the fused residual-add + RMSNorm ("GPU Performance from First Principles",
+ * section 6.1, the fused add + RMSNorm, and its exercise 4: one kernel reads x and the
+ * residual and writes the new residual stream and the normalised result).  The page names
+ * the operation without printing its formula; this library takes the usual RMSNorm: no mean
+ * is subtracted, no shift added, eps is added to the mean square inside the square root:
+ *
+ *   s = x + res (stored as res_out, rounded to the I/O type),  r = 1 / sqrt(mean(s^2) + eps),
+ *   out = gamma * s * r.
+ *
+ *   x, res, gamma, eps, out, res_out   as for ln_fwd_* (res and res_out may be NULL)
+ *   rrms     [rows] fp32   per-row r                                 (written)
+ *
+ * Conventions, limits and errors are those of ln_fwd_*.  Nothing is allocated.
+ */
+ln_status ln_rms_fwd_f32(const float* x, const float* res, const float* gamma, float eps,
+                         int64_t rows, int64_t cols, float* out, float* res_out, float* rrms,
+                         ln_stream_t stream);
+
+ln_status ln_rms_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma, float eps,
+                          int64_t rows, int64_t cols, ln_bf16* out, ln_bf16* res_out, float* rrms,
+                          ln_stream_t stream);
+
+/*
+ * Backward of the fused residual-add + RMSNorm, from the forward by the chain rule: with
+ * shat = s * r and g = gamma * dy,
+ *
+ *   dx = r * (g - shat * sum_j g_j shat_j / cols)   (one row sum; gradient of s, hence of
+ *                                                     x and res; OVERWRITTEN)
+ *   dgamma = sum over rows of dy * shat             (overwritten)
+ *
+ *   dy, x_or_res_out, gamma, dx, dgamma   as for ln_bwd_* (x_or_res_out: the tensor the
+ *                                         forward normalised)
+ *   rrms     [rows] fp32   as written by ln_rms_fwd_*
+ *
+ * dgamma is reduced in the same two deterministic stages as ln_bwd_*'s (no float atomics,
+ * bitwise identical run to run).  The plain variants use the library-owned workspace of the
+ * stream, the _ws variants a caller-owned one of at least ln_bwd_workspace_bytes(rows, cols)
+ * bytes, exactly as for ln_bwd_* and ln_bwd_*_ws (which may share it in stream order).
+ */
+ln_status ln_rms_bwd_f32(const float* dy, const float* x_or_res_out, const float* gamma,
+                         const float* rrms, float* dx, float* dgamma, int64_t rows, int64_t cols,
+                         ln_stream_t stream);
+
+ln_status ln_rms_bwd_bf16(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                          const float* rrms, ln_bf16* dx, ln_bf16* dgamma, int64_t rows,
+                          int64_t cols, ln_stream_t stream);
+
+ln_status ln_rms_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
+                            const float* rrms, float* dx, float* dgamma, int64_t rows,
+                            int64_t cols, void* workspace, size_t workspace_bytes,
+                            ln_stream_t stream);
+
+ln_status ln_rms_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out,
+                             const ln_bf16* gamma, const float* rrms, ln_bf16* dx,
+                             ln_bf16* dgamma, int64_t rows, int64_t cols, void* workspace,
+                             size_t workspace_bytes, ln_stream_t stream);
+
+/*
+ * Fused row softmax, forward ("Accelerating Transformer on GPU (I)", section 4.1: scale,
+ * add the mask, row maximum, exponentiate, row sum and divide in one kernel).  For each row
+ * r of a row-major [rows, cols] problem:
+ *
+ *   z = scale * x + mask[r % mask_rows],   y = exp(z - max z) / sum exp(z - max z).
+ *
+ *   x      [rows, cols]       input (attention scores, say: rows = batch * heads * queries)
+ *   mask   [mask_rows, cols]  additive mask (0 keeps an entry, -inf removes it), its rows
+ *                             repeating every mask_rows rows; may be NULL (no mask; then
+ *                             mask_rows is ignored)
+ *   scale                     factor on x (finite)
+ *   y      [rows, cols]       written; must not overlap x or mask
+ *
+ * A row whose entries are all -inf has no softmax; y is NaN there (0 / 0), as the
+ * definition gives.  Conventions, limits and errors as for ln_fwd_*; nothing is allocated.
+ */
+ln_status ln_softmax_fwd_f32(const float* x, const float* mask, int64_t mask_rows, float scale,
+                             int64_t rows, int64_t cols, float* y, ln_stream_t stream);
+
+ln_status ln_softmax_fwd_bf16(const ln_bf16* x, const ln_bf16* mask, int64_t mask_rows,
+                              float scale, int64_t rows, int64_t cols, ln_bf16* y,
+                              ln_stream_t stream);
+
+/*
+ * Fused row softmax, backward ("Accelerating Transformer on GPU (II): Training with
+ * LightSeq2", section 3.1: only the forward's output y is needed, and one row reduction):
+ *
+ *   dx = scale * y * (dy - sum_j dy_j y_j)      (the mask has no gradient)
+ *
+ *   dy, y  [rows, cols]   upstream gradient and the forward's output
+ *   scale                 the forward's factor on x
+ *   dx     [rows, cols]   written (may alias dy); must not overlap y
+ *
+ * Conventions, limits and errors as for ln_fwd_*; nothing is allocated.
+ */
+ln_status ln_softmax_bwd_f32(const float* dy, const float* y, float scale, int64_t rows,
+                             int64_t cols, float* dx, ln_stream_t stream);
+
+ln_status ln_softmax_bwd_bf16(const ln_bf16* dy, const ln_bf16* y, float scale, int64_t rows,
+                              int64_t cols, ln_bf16* dx, ln_stream_t stream);
 
 /*
  * Backward (bf16) that allocates nothing.  The pages have no counterpart to this entry

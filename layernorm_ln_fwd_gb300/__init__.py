@@ -1,4 +1,4 @@
-"""GB300 (sm_103a) fused residual-add + LayerNorm, forward and backward.
+"""GB300 (sm_103a) fused residual-add + LayerNorm (and RMSNorm), forward and backward.
 
 A thin ctypes binding over the C ABI of ``libln.so`` (declared in ``include/ln.h``).  It only
 marshals arguments: it checks dtypes, shapes, devices and contiguity, allocates outputs with
@@ -8,7 +8,9 @@ there is no fallback: if ``libln.so`` is missing, the first call raises RuntimeE
 
 Forward (``fwd``): s = x + res is written as ``res_out``; out = gamma * (s - mu) * rstd + beta,
 with per-row fp32 ``mean`` and ``rstd``.  Backward (``bwd``): dx with respect to s (hence to
-both x and res), dgamma and dbeta, the latter bitwise reproducible.  Definitions:
+both x and res), dgamma and dbeta, the latter bitwise reproducible.  ``rms_fwd`` and
+``rms_bwd`` do the same for the fused residual-add + RMSNorm ("GPU Performance from First
+Principles", section 6.1).  Definitions:
 "Accelerating Transformer on GPU (II): Training with LightSeq2", sections 2.1, 2.2 and 2.4;
 residual fusion as in "llm.c: the llmc/ CUDA kernel layer", section 3.2.
 """
@@ -49,6 +51,16 @@ SIGNATURES = {
     "ln_debug_wait_test": (None, [ctypes.c_uint]),
     "ln_last_launch_count": (_INT, []),
     "ln_bwd_bf16_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_rms_fwd_f32": (_INT, [_P, _P, _P, _F, _I64, _I64, _P, _P, _P, _P]),
+    "ln_rms_fwd_bf16": (_INT, [_P, _P, _P, _F, _I64, _I64, _P, _P, _P, _P]),
+    "ln_rms_bwd_f32": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_rms_bwd_bf16": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
+    "ln_rms_bwd_f32_ws": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "ln_rms_bwd_bf16_ws": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "ln_softmax_fwd_f32": (_INT, [_P, _P, _I64, _F, _I64, _I64, _P, _P]),
+    "ln_softmax_fwd_bf16": (_INT, [_P, _P, _I64, _F, _I64, _I64, _P, _P]),
+    "ln_softmax_bwd_f32": (_INT, [_P, _P, _F, _I64, _I64, _P, _P]),
+    "ln_softmax_bwd_bf16": (_INT, [_P, _P, _F, _I64, _I64, _P, _P]),
 }
 
 
@@ -214,3 +226,101 @@ def force_path(path: int) -> int:
 
 def last_launch_count() -> int:
     return int(lib().ln_last_launch_count())
+
+
+def rms_fwd(x, res, gamma, eps: float = 1e-5, out=None, res_out=None, rrms=None,
+            write_res_out: bool = True, stream=None):
+    """Fused residual-add + RMSNorm forward.  x, res: [rows, cols] (res may be None); gamma:
+    [cols].  Returns (out, res_out, rrms): out = gamma * s * rrms, s = x + res stored as
+    res_out, rrms = 1 / sqrt(mean(s^2) + eps) per row (fp32)."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [rows, cols]")
+    rows, cols = x.shape
+    dt, dev = x.dtype, x.device
+    sfx = _suffix(dt)
+    _need(x, "x", (rows, cols), dt, dev)
+    if res is not None:
+        _need(res, "res", (rows, cols), dt, dev)
+    _need(gamma, "gamma", (cols,), dt, dev)
+    out = torch.empty_like(x) if out is None else _need(out, "out", (rows, cols), dt, dev)
+    if res_out is None and write_res_out:
+        res_out = torch.empty_like(x)
+    elif res_out is not None:
+        _need(res_out, "res_out", (rows, cols), dt, dev)
+    rrms = (torch.empty(rows, dtype=torch.float32, device=dev) if rrms is None
+            else _need(rrms, "rrms", (rows,), torch.float32, dev))
+    name = f"ln_rms_fwd_{sfx}"
+    _check(name, getattr(lib(), name)(_ptr(x), _ptr(res), _ptr(gamma), float(eps), rows, cols,
+                                      _ptr(out), _ptr(res_out), _ptr(rrms), _stream(stream)))
+    return out, res_out, rrms
+
+
+def rms_bwd(dy, x_or_res_out, gamma, rrms, dx=None, dgamma=None, workspace=None, stream=None):
+    """Fused residual-add + RMSNorm backward.  Returns (dx, dgamma); ``workspace`` as for
+    :func:`bwd`."""
+    import torch
+    if dy.dim() != 2:
+        raise ValueError("dy must be 2-D [rows, cols]")
+    rows, cols = dy.shape
+    dt, dev = dy.dtype, dy.device
+    sfx = _suffix(dt)
+    _need(dy, "dy", (rows, cols), dt, dev)
+    _need(x_or_res_out, "x_or_res_out", (rows, cols), dt, dev)
+    _need(gamma, "gamma", (cols,), dt, dev)
+    _need(rrms, "rrms", (rows,), torch.float32, dev)
+    dx = torch.empty_like(dy) if dx is None else _need(dx, "dx", (rows, cols), dt, dev)
+    dgamma = (torch.empty(cols, dtype=dt, device=dev) if dgamma is None
+              else _need(dgamma, "dgamma", (cols,), dt, dev))
+    args = [_ptr(dy), _ptr(x_or_res_out), _ptr(gamma), _ptr(rrms), _ptr(dx), _ptr(dgamma),
+            rows, cols]
+    if workspace is None:
+        name = f"ln_rms_bwd_{sfx}"
+        _check(name, getattr(lib(), name)(*args, _stream(stream)))
+    else:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the same device")
+        nbytes = workspace.numel() * workspace.element_size()
+        name = f"ln_rms_bwd_{sfx}_ws"
+        _check(name, getattr(lib(), name)(*args, _ptr(workspace), nbytes, _stream(stream)))
+    return dx, dgamma
+
+
+def softmax_fwd(x, mask=None, scale: float = 1.0, y=None, stream=None):
+    """Fused row softmax: y = softmax(scale * x + mask[r % mask_rows]) per row r.  x:
+    [rows, cols]; mask: None or [mask_rows, cols] (additive, -inf removes an entry)."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [rows, cols]")
+    rows, cols = x.shape
+    dt, dev = x.dtype, x.device
+    sfx = _suffix(dt)
+    _need(x, "x", (rows, cols), dt, dev)
+    mask_rows = 1
+    if mask is not None:
+        if mask.dim() != 2:
+            raise ValueError("mask must be 2-D [mask_rows, cols]")
+        mask_rows = mask.shape[0]
+        _need(mask, "mask", (mask_rows, cols), dt, dev)
+    y = torch.empty_like(x) if y is None else _need(y, "y", (rows, cols), dt, dev)
+    name = f"ln_softmax_fwd_{sfx}"
+    _check(name, getattr(lib(), name)(_ptr(x), _ptr(mask), mask_rows, float(scale), rows, cols,
+                                      _ptr(y), _stream(stream)))
+    return y
+
+
+def softmax_bwd(dy, y, scale: float = 1.0, dx=None, stream=None):
+    """Fused row softmax backward: dx = scale * y * (dy - sum(dy * y)) per row."""
+    import torch
+    if dy.dim() != 2:
+        raise ValueError("dy must be 2-D [rows, cols]")
+    rows, cols = dy.shape
+    dt, dev = dy.dtype, dy.device
+    sfx = _suffix(dt)
+    _need(dy, "dy", (rows, cols), dt, dev)
+    _need(y, "y", (rows, cols), dt, dev)
+    dx = torch.empty_like(dy) if dx is None else _need(dx, "dx", (rows, cols), dt, dev)
+    name = f"ln_softmax_bwd_{sfx}"
+    _check(name, getattr(lib(), name)(_ptr(dy), _ptr(y), float(scale), rows, cols, _ptr(dx),
+                                      _stream(stream)))
+    return dx

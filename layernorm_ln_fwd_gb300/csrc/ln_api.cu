@@ -169,16 +169,17 @@ ln_status finish_call(cudaError_t e, int launches, cudaStream_t stream) {
     return LN_OK;
 }
 
+// `rms`: the RMSNorm forward (beta and mean unused, may be null; rstd receives 1 / rms).
 template <typename T>
-ln_status fwd_impl(Dtype dt, const T* x, const T* res, const T* gamma, const T* beta, float eps,
-                   int64_t rows, int64_t cols, T* out, T* res_out, float* mean, float* rstd,
-                   ln_stream_t stream_) {
+ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma, const T* beta,
+                   float eps, int64_t rows, int64_t cols, T* out, T* res_out, float* mean,
+                   float* rstd, ln_stream_t stream_) {
     t_last_launches = 0;
     if (!std::isfinite(eps) || eps < 0.f) return LN_EINVAL;
     ln_status st = check_sizes(rows, cols);
     if (st != LN_OK) return st;
     if (rows == 0) return LN_OK;  // nothing is read or written
-    if (!x || !gamma || !beta || !out || !mean || !rstd) return LN_EINVAL;
+    if (!x || !gamma || (!rms && (!beta || !mean)) || !out || !rstd) return LN_EINVAL;
     st = check_device();
     if (st != LN_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -199,21 +200,23 @@ ln_status fwd_impl(Dtype dt, const T* x, const T* res, const T* gamma, const T* 
     a.status = status_word();
     a.wait_limit_ns = wait_limit_ns();
     int launches = 0;
-    cudaError_t e = launch_fwd(dt, a, aligned, g_force_path.load(), stream, &launches);
+    cudaError_t e = rms ? launch_rms_fwd(dt, a, aligned, g_force_path.load(), stream, &launches)
+                        : launch_fwd(dt, a, aligned, g_force_path.load(), stream, &launches);
     return finish_call(e, launches, stream);
 }
 
 }  // namespace
 
 template <typename T>
-ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const float* mean,
-                   const float* rstd, T* dx, T* dgamma, T* dbeta, int64_t rows, int64_t cols,
-                   void* ws, size_t ws_bytes, bool own_ws, ln_stream_t stream_) {
+ln_status bwd_impl(Dtype dt, bool rms, const T* dy, const T* xr, const T* gamma,
+                   const float* mean, const float* rstd, T* dx, T* dgamma, T* dbeta,
+                   int64_t rows, int64_t cols, void* ws, size_t ws_bytes, bool own_ws,
+                   ln_stream_t stream_) {
     t_last_launches = 0;
     ln_status st = check_sizes(rows, cols);
     if (st != LN_OK) return st;
-    if (!dgamma || !dbeta) return LN_EINVAL;
-    if (rows > 0 && (!dy || !xr || !gamma || !mean || !rstd || !dx)) return LN_EINVAL;
+    if (!dgamma || (!rms && !dbeta)) return LN_EINVAL;
+    if (rows > 0 && (!dy || !xr || !gamma || (!rms && !mean) || !rstd || !dx)) return LN_EINVAL;
     if (!own_ws && !ws) return LN_EINVAL;
     if (!own_ws && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LN_EALIGN;
     st = check_device();
@@ -222,13 +225,13 @@ ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const flo
     const size_t esize = sizeof(T);
     if (rows == 0) {  // sums over no rows
         cudaError_t e = cudaMemsetAsync(dgamma, 0, (size_t)cols * esize, stream);
-        if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, (size_t)cols * esize, stream);
+        if (e == cudaSuccess && !rms) e = cudaMemsetAsync(dbeta, 0, (size_t)cols * esize, stream);
         return finish_call(e, 0, stream);
     }
     const void* ptrs[] = {dy, xr, gamma, dx};
     const bool aligned = vector_ok(dt, (int)cols, ptrs, 4);
     BwdPlan plan;
-    cudaError_t e = plan_bwd(dt, (int)rows, (int)cols, aligned, g_force_path.load(), &plan);
+    cudaError_t e = plan_bwd(dt, rms, (int)rows, (int)cols, aligned, g_force_path.load(), &plan);
     if (e != cudaSuccess) return cuda_fail(e);
     const size_t need = bwd_workspace_bytes(plan.grid, (int)cols, bwd_plan_acc_region(plan));
     if (own_ws) {
@@ -277,14 +280,50 @@ ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const flo
     return finish_call(e, launches, stream);
 }
 
-template ln_status bwd_impl<float>(Dtype, const float*, const float*, const float*,
+template ln_status bwd_impl<float>(Dtype, bool, const float*, const float*, const float*,
                                    const float*, const float*, float*, float*, float*, int64_t,
                                    int64_t, void*, size_t, bool, ln_stream_t);
-template ln_status bwd_impl<__nv_bfloat16>(Dtype, const __nv_bfloat16*, const __nv_bfloat16*,
+template ln_status bwd_impl<__nv_bfloat16>(Dtype, bool, const __nv_bfloat16*, const __nv_bfloat16*,
                                            const __nv_bfloat16*, const float*, const float*,
                                            __nv_bfloat16*, __nv_bfloat16*, __nv_bfloat16*,
                                            int64_t, int64_t, void*, size_t, bool, ln_stream_t);
 
+}  // namespace lnk
+
+namespace lnk {
+namespace {
+template <typename T>
+ln_status softmax_impl(Dtype dt, bool bwd, const T* a, const T* b, const T* mask,
+                       int64_t mask_rows, float scale, int64_t rows, int64_t cols, T* out,
+                       ln_stream_t stream_) {
+    t_last_launches = 0;
+    if (!std::isfinite(scale)) return LN_EINVAL;
+    ln_status st = check_sizes(rows, cols);
+    if (st != LN_OK) return st;
+    if (mask && (mask_rows < 1 || mask_rows > LN_MAX_ROWS)) return LN_EINVAL;
+    if (rows == 0) return LN_OK;
+    if (!a || !out || (bwd && !b)) return LN_EINVAL;
+    st = check_device();
+    if (st != LN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const void* ptrs[] = {a, b, mask, out};
+    SoftmaxArgs s;
+    s.a = a;
+    s.b = b;
+    s.mask = mask;
+    s.mask_rows = mask ? (int)mask_rows : 1;
+    s.scale = scale;
+    s.rows = (int)rows;
+    s.cols = (int)cols;
+    s.out = out;
+    s.status = status_word();
+    s.wait_limit_ns = wait_limit_ns();
+    int launches = 0;
+    cudaError_t e = launch_softmax(dt, bwd, s, vector_ok(dt, (int)cols, ptrs, 4),
+                                   g_force_path.load(), stream, &launches);
+    return finish_call(e, launches, stream);
+}
+}  // namespace
 }  // namespace lnk
 
 using lnk::Dtype;
@@ -294,7 +333,7 @@ extern "C" {
 ln_status ln_fwd_f32(const float* x, const float* res, const float* gamma, const float* beta,
                      float eps, int64_t rows, int64_t cols, float* out, float* res_out,
                      float* mean, float* rstd, ln_stream_t stream) {
-    return lnk::fwd_impl<float>(Dtype::F32, x, res, gamma, beta, eps, rows, cols, out, res_out,
+    return lnk::fwd_impl<float>(Dtype::F32, false, x, res, gamma, beta, eps, rows, cols, out, res_out,
                                 mean, rstd, stream);
 }
 
@@ -302,7 +341,7 @@ ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma
                       const ln_bf16* beta, float eps, int64_t rows, int64_t cols, ln_bf16* out,
                       ln_bf16* res_out, float* mean, float* rstd, ln_stream_t stream) {
     using B = __nv_bfloat16;
-    return lnk::fwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(x),
+    return lnk::fwd_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(x),
                             reinterpret_cast<const B*>(res), reinterpret_cast<const B*>(gamma),
                             reinterpret_cast<const B*>(beta), eps, rows, cols,
                             reinterpret_cast<B*>(out), reinterpret_cast<B*>(res_out), mean, rstd,
@@ -312,7 +351,7 @@ ln_status ln_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma
 ln_status ln_bwd_f32(const float* dy, const float* x_or_res_out, const float* gamma,
                      const float* mean, const float* rstd, float* dx, float* dgamma,
                      float* dbeta, int64_t rows, int64_t cols, ln_stream_t stream) {
-    return lnk::bwd_impl<float>(Dtype::F32, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
+    return lnk::bwd_impl<float>(Dtype::F32, false, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
                                 dbeta, rows, cols, nullptr, 0, true, stream);
 }
 
@@ -320,7 +359,7 @@ ln_status ln_bwd_bf16(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_b
                       const float* mean, const float* rstd, ln_bf16* dx, ln_bf16* dgamma,
                       ln_bf16* dbeta, int64_t rows, int64_t cols, ln_stream_t stream) {
     using B = __nv_bfloat16;
-    return lnk::bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(dy),
+    return lnk::bwd_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(dy),
                             reinterpret_cast<const B*>(x_or_res_out),
                             reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
                             reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols,
@@ -342,7 +381,7 @@ ln_status ln_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float*
                         const float* mean, const float* rstd, float* dx, float* dgamma,
                         float* dbeta, int64_t rows, int64_t cols, void* workspace,
                         size_t workspace_bytes, ln_stream_t stream) {
-    return lnk::bwd_impl<float>(Dtype::F32, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
+    return lnk::bwd_impl<float>(Dtype::F32, false, dy, x_or_res_out, gamma, mean, rstd, dx, dgamma,
                                 dbeta, rows, cols, workspace, workspace_bytes, false, stream);
 }
 
@@ -351,11 +390,97 @@ ln_status ln_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out, const l
                          ln_bf16* dbeta, int64_t rows, int64_t cols, void* workspace,
                          size_t workspace_bytes, ln_stream_t stream) {
     using B = __nv_bfloat16;
-    return lnk::bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(dy),
+    return lnk::bwd_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(dy),
                             reinterpret_cast<const B*>(x_or_res_out),
                             reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
                             reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols,
                             workspace, workspace_bytes, false, stream);
+}
+
+ln_status ln_rms_fwd_f32(const float* x, const float* res, const float* gamma, float eps,
+                         int64_t rows, int64_t cols, float* out, float* res_out, float* rrms,
+                         ln_stream_t stream) {
+    return lnk::fwd_impl<float>(Dtype::F32, true, x, res, gamma, nullptr, eps, rows, cols, out,
+                                res_out, nullptr, rrms, stream);
+}
+
+ln_status ln_rms_fwd_bf16(const ln_bf16* x, const ln_bf16* res, const ln_bf16* gamma, float eps,
+                          int64_t rows, int64_t cols, ln_bf16* out, ln_bf16* res_out, float* rrms,
+                          ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::fwd_impl<B>(Dtype::BF16, true, reinterpret_cast<const B*>(x),
+                            reinterpret_cast<const B*>(res), reinterpret_cast<const B*>(gamma),
+                            nullptr, eps, rows, cols, reinterpret_cast<B*>(out),
+                            reinterpret_cast<B*>(res_out), nullptr, rrms, stream);
+}
+
+ln_status ln_rms_bwd_f32(const float* dy, const float* x_or_res_out, const float* gamma,
+                         const float* rrms, float* dx, float* dgamma, int64_t rows, int64_t cols,
+                         ln_stream_t stream) {
+    return lnk::bwd_impl<float>(Dtype::F32, true, dy, x_or_res_out, gamma, nullptr, rrms, dx,
+                                dgamma, nullptr, rows, cols, nullptr, 0, true, stream);
+}
+
+ln_status ln_rms_bwd_bf16(const ln_bf16* dy, const ln_bf16* x_or_res_out, const ln_bf16* gamma,
+                          const float* rrms, ln_bf16* dx, ln_bf16* dgamma, int64_t rows,
+                          int64_t cols, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::bwd_impl<B>(Dtype::BF16, true, reinterpret_cast<const B*>(dy),
+                            reinterpret_cast<const B*>(x_or_res_out),
+                            reinterpret_cast<const B*>(gamma), nullptr, rrms,
+                            reinterpret_cast<B*>(dx), reinterpret_cast<B*>(dgamma), nullptr, rows,
+                            cols, nullptr, 0, true, stream);
+}
+
+ln_status ln_rms_bwd_f32_ws(const float* dy, const float* x_or_res_out, const float* gamma,
+                            const float* rrms, float* dx, float* dgamma, int64_t rows,
+                            int64_t cols, void* workspace, size_t workspace_bytes,
+                            ln_stream_t stream) {
+    return lnk::bwd_impl<float>(Dtype::F32, true, dy, x_or_res_out, gamma, nullptr, rrms, dx,
+                                dgamma, nullptr, rows, cols, workspace, workspace_bytes, false,
+                                stream);
+}
+
+ln_status ln_rms_bwd_bf16_ws(const ln_bf16* dy, const ln_bf16* x_or_res_out,
+                             const ln_bf16* gamma, const float* rrms, ln_bf16* dx,
+                             ln_bf16* dgamma, int64_t rows, int64_t cols, void* workspace,
+                             size_t workspace_bytes, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::bwd_impl<B>(Dtype::BF16, true, reinterpret_cast<const B*>(dy),
+                            reinterpret_cast<const B*>(x_or_res_out),
+                            reinterpret_cast<const B*>(gamma), nullptr, rrms,
+                            reinterpret_cast<B*>(dx), reinterpret_cast<B*>(dgamma), nullptr, rows,
+                            cols, workspace, workspace_bytes, false, stream);
+}
+
+
+ln_status ln_softmax_fwd_f32(const float* x, const float* mask, int64_t mask_rows, float scale,
+                             int64_t rows, int64_t cols, float* y, ln_stream_t stream) {
+    return lnk::softmax_impl<float>(Dtype::F32, false, x, nullptr, mask, mask_rows, scale, rows,
+                                    cols, y, stream);
+}
+
+ln_status ln_softmax_fwd_bf16(const ln_bf16* x, const ln_bf16* mask, int64_t mask_rows,
+                              float scale, int64_t rows, int64_t cols, ln_bf16* y,
+                              ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::softmax_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(x), nullptr,
+                                reinterpret_cast<const B*>(mask), mask_rows, scale, rows, cols,
+                                reinterpret_cast<B*>(y), stream);
+}
+
+ln_status ln_softmax_bwd_f32(const float* dy, const float* y, float scale, int64_t rows,
+                             int64_t cols, float* dx, ln_stream_t stream) {
+    return lnk::softmax_impl<float>(Dtype::F32, true, dy, y, nullptr, 1, scale, rows, cols, dx,
+                                    stream);
+}
+
+ln_status ln_softmax_bwd_bf16(const ln_bf16* dy, const ln_bf16* y, float scale, int64_t rows,
+                              int64_t cols, ln_bf16* dx, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::softmax_impl<B>(Dtype::BF16, true, reinterpret_cast<const B*>(dy),
+                                reinterpret_cast<const B*>(y), nullptr, 1, scale, rows, cols,
+                                reinterpret_cast<B*>(dx), stream);
 }
 
 ln_status ln_device_check(ln_stream_t stream_) {

@@ -1,1137 +1,22 @@
-// ln_bwd.cu -- backward kernels of the fused residual-add + LayerNorm.
-//
-// Row gradient, HW4 form ("Accelerating Transformer on GPU (II): Training with LightSeq2",
-// section 2.1), with the two row sums reduced together (section 2.2):
-//   xhat = (s - mu) * rstd,  g = gamma * dy,
-//   dx = rstd * (g - (sum g + xhat * sum g xhat) / n).
-// Column gradients (sections 2.1 and 2.4): dgamma = sum_rows dy * xhat, dbeta = sum_rows dy.
-//
-// g = gamma * dy is rounded once (__fmul_rn, never fused into a later subtraction) so that
-// the g in the row sums and the g in dx are the same number: when rstd is large (a row of
-// near-constant values) any difference between them would be amplified into dx.
-//
-// Column sums, deterministic and without float atomics, in two stages:
-//  1. Each block owns a FIXED set of rows (every G-th row or 7-row tile; a contiguous range
-//     in the scalar kernel).  While it computes dx it
-//     accumulates dy * xhat and dy for the columns its threads own and, at the end, writes
-//     one row of partial sums per statistic to the workspace: part[stat][block][col].
-//  2. The blocks that own a slice of the columns then read every block's partials of their
-//     slice, add them over blocks in a fixed order and write dgamma and dbeta; the others
-//     leave.  A partial announces itself: the workspace words are zero between calls and a
-//     stored partial never is (see part_enc), so a reader polls, bounded, only the words it
-//     is still missing -- no fence, arrival counter or grid-wide wait -- and zeroes what it
-//     has read for the next call.
-//  This is the last-block-finishes idea of llm.c's layernorm_backward_kernel10 ("llm.c: the
-//  llmc/ CUDA kernel layer", section 3.3), widened from one finishing block to many so that
-//  the finish is spread over SMs instead of serialising one SM on all partials.  The grid
-//  is launched cooperatively, so every block is resident and the polls always end.  Which
-//  block adds which rows, and in what order, depends only on (rows, cols, device), so
-//  dgamma and dbeta are bitwise reproducible run to run.
-//
-// Accuracy of the column sums.  A plain fp32 sum of n terms of size sigma carries an error
-// of about 2^-24 * sigma * sqrt(n * L) for chains of L additions, whatever the order: for
-// 262144 rows that is ~1e-4, far above the 2e-5 that fp32 results are held to.  So for fp32
-// I/O (and bf16 rows long enough to make chains long) each thread or lane keeps its running
-// sums compensated (Kahan: a second fp32 register holds the rounding error of every
-// addition), partial sums are stored as (hi, lo) fp32 pairs and every later addition is
-// error-free (TwoSum), so the only rounding left is the final one to the output type.  For
-// bf16 results over short chains plain fp32 sums are far more accurate than the bf16 unit
-// in the last place, and the partials are stored and added plainly.
-#include <algorithm>
-#include <climits>
-#include <type_traits>
-
-#include "ln_device.cuh"
-#include "ln_internal.h"
+// ln_bwd.cu -- the fused residual-add + LayerNorm backward: instantiations of the kernels in
+// ln_bwd_kernels.cuh and the library-facing plan / launch entry points (which hand RMSNorm
+// problems to rms_bwd.cu).
+#include "ln_bwd_kernels.cuh"
 
 namespace lnk {
-namespace {
-
-// Consumer warps = rows per tile, plus one producer warp: 8 warps, because registers are
-// allocated to warps in groups of four (a 9-warp block would pay for 12).
-constexpr int kTileRows = 7;
-constexpr int kTileThreads = (kTileRows + 1) * 32;
-constexpr int kBwdBlockMaxThreads = 512;
-constexpr int kBwdScalarThreads = 256;
-constexpr int kMaxStages = 8;
-constexpr int kBlockStages = 4;
-// The warp kernel is used for bf16 rows of up to 5 vectors per lane (1280 columns) and at
-// most this many rows, which keeps its plain per-lane chains short.
-constexpr int kWarpPathMaxRows = 65536;
-
-struct KParams {
-    const void* dy;
-    const void* xr;
-    const void* gamma;
-    const float* mean;
-    const float* rstd;
-    void* dx;
-    void* dgamma;
-    void* dbeta;
-    int rows;
-    int cols;
-    float2* part;  // [2][gridDim.x][cols] (hi, lo) pairs, or plain fp32 sums when compact
-    float2* acc;   // scalar kernel, rows too wide for shared memory: its running (hi, lo) sums
-    int compact;   // partials without the lo half (kernels whose column sums are plain)
-    int fin_rw;    // warps per unit group in the finish (divides the block's warp count)
-    unsigned* ctr;  // a zero word nothing writes (the bounded-wait test polls it)
-    unsigned* status;
-    uint64_t limit_ns;
-    unsigned wait_extra;
-    int stages;
-};
-
-// This block's share [r0, r1) of n items split over the grid: the first n % G blocks take
-// one item more (32-bit arithmetic: one division, no 64-bit products).
-__device__ __forceinline__ void row_range(int n, int& r0, int& r1) {
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int q = n / G, rem = n - q * G;
-    r0 = b * q + min(b, rem);
-    r1 = r0 + q + (b < rem ? 1 : 0);
-}
-
-// (S, C) += (h, l), where a compensated value is S + C.
-__device__ __forceinline__ void comp_add(float& S, float& C, float h, float l) {
-    float s, e;
-    two_sum_f(S, h, s, e);
-    S = s;
-    C += e + l;
-}
-
-// Kahan step on fp32 pairs: the running value is s - c.
-__device__ __forceinline__ void kahan2(f2& s, f2& c, f2 x) {
-    const f2 y = f2_sub(x, c);
-    const f2 t = f2_add(s, y);
-    c = f2_sub(f2_sub(t, s), y);
-    s = t;
-}
-
-// Kahan step: the running value is s - c.
-__device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
-    const float y = __fsub_rn(x, c);
-    const float t = __fadd_rn(s, y);
-    c = __fsub_rn(__fsub_rn(t, s), y);
-    s = t;
-}
-
-// ---------------------------------------------------------------------------------------
-// Stage 2: the finish.  A unit is U adjacent columns of one statistic; a partial is a
-// (hi, lo) pair per column, or one plain fp32 sum when COMPACT, and U is chosen so that one
-// unit of one partial row is a single 16-byte load where the row length allows.  Units are
-// taken in groups of kFinUnits adjacent ones (128 contiguous bytes of a partial row); block f
-// of P owns groups [f * g / P, (f + 1) * g / P).  The block's warps work on GW groups at a
-// time, RW warps per group (RW * GW = the warp count, RW chosen by the host so that a lane's
-// rows fit in one batch).  Warp r of a group's RW takes the contiguous range of partial rows
-// [r * P / RW, (r + 1) * P / RW); lane (s, k), s < kFinSub, k < kFinUnits, adds unit k of
-// rows s, s + kFinSub, ... of that range in increasing order (the loads of a batch issued
-// before the first addition, so the L2 latency is paid once per batch, and a warp's load
-// touches kFinSub lines); the kFinSub lane totals are folded by a fixed shuffle tree, and
-// the RW warp totals are added in warp order through shared memory.  The order depends
-// only on P, RW and the unit.
-// A loaded unit with a zero word belongs to a block that has not written its partials yet:
-// one lane of the warp watches a single word of the earliest such row, the lanes then reload
-// what they miss, until nothing is missing or the time limit passes; then each lane zeroes
-// the units it read and adds them.
-// Compensated partials are added with TwoSum; COMPACT partials (plain fp32 sums from
-// kernels with bf16 results) with plain fp32 additions: their error, about 2^-24 * sqrt(P)
-// times the partials' size, is far below a bf16 unit in the last place.
-// `scratch` holds at least 2 * U floats per thread.
-// ---------------------------------------------------------------------------------------
-constexpr int kFinUnits = 8;
-constexpr int kFinSub = 32 / kFinUnits;
-constexpr int kFinBatch = 48;  // at most this many words of partials per lane and batch,
-constexpr int kFinMaxRows = 10;  // from at most this many partial rows
-__host__ __device__ constexpr int fin_rows_per_lane(int words_per_unit) {
-    return kFinBatch / words_per_unit < kFinMaxRows ? kFinBatch / words_per_unit : kFinMaxRows;
-}
-
-// The same pointer, opaque to the compiler (so values derived from it are recomputed, not
-// kept live from an earlier computation).
-template <typename P>
-__device__ __forceinline__ P* opaque(P* p) {
-    asm volatile("" : "+l"(p));
-    return p;
-}
-
-template <int N>
-__device__ __forceinline__ bool has_zero(const uint32_t (&w)[N]) {
-    bool z = false;
-#pragma unroll
-    for (int i = 0; i < N; ++i) z |= w[i] == 0u;
-    return z;
-}
-
-template <typename T, int U, bool COMPACT>
-__device__ void finish_units(const KParams& a, int P, int f, float* scratch) {
-    using IO = Io<T>;
-    constexpr int E = COMPACT ? 1 : 2;  // floats per column of a partial
-    constexpr int W = E * U;            // words per unit of a partial row: 1, 2 or 4
-    constexpr int L = fin_rows_per_lane(W);  // partial rows one lane loads per batch
-    const int cols = a.cols;
-    const int ngroups = cols / U;       // units per statistic
-    const int nunits = 2 * ngroups;
-    const int ng = (nunits + kFinUnits - 1) / kFinUnits;
-    const int g0 = f * ng / P, g1 = (f + 1) * ng / P;  // f * ng < 2^24: 32-bit is exact
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int RW = a.fin_rw, GW = nw / RW;
-    const int gw = warp / RW, rw = warp - gw * RW;
-    const int k = lane % kFinUnits, sub = lane / kFinUnits;
-    const int p_lo = rw * P / RW, p_hi = (rw + 1) * P / RW;
-    uint32_t* part = reinterpret_cast<uint32_t*>(a.part);
-    const size_t stat_stride = (size_t)P * cols * E;
-    const size_t row_stride = (size_t)cols * E;
-    bool late = false;  // a partial did not arrive within the time limit
-    for (int gb = g0; gb < g1; gb += GW) {  // block-uniform
-        const int gi = gb + gw;
-        const int u = gi * kFinUnits + k;
-        const bool grp_ok = gi < g1;  // the same in the whole warp
-        const bool act = grp_ok && u < nunits;
-        const int stat = u >= ngroups ? 1 : 0, grp = u - stat * ngroups;
-        float S[U], C[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i) S[i] = C[i] = 0.f;
-        if (grp_ok) {
-            uint32_t* src = part + stat * stat_stride + (size_t)grp * W;
-            const size_t step = (size_t)kFinSub * row_stride;  // between a lane's rows
-            for (int pb = p_lo; pb < p_hi; pb += kFinSub * L) {  // the same trips in the warp
-                const int p0 = pb + sub;
-                const int nj = act && p0 < p_hi ? (p_hi - p0 + kFinSub - 1) / kFinSub : 0;
-                uint32_t* q0 = src + (size_t)p0 * row_stride;
-                uint32_t v[L][W];
-#pragma unroll
-                for (int j = 0; j < L; ++j) {
-                    if (j < nj) {
-                        ld_part<W>(q0 + j * step, v[j]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < W; ++i) v[j][i] = ~0u;  // reads as +0
-                    }
-                }
-                unsigned miss = 0;  // bit j: row j of this lane's batch is not all there
-#pragma unroll
-                for (int j = 0; j < L; ++j) miss |= has_zero<W>(v[j]) ? 1u << j : 0u;
-                if (__any_sync(kFullMask, miss != 0)) {
-                    // Blocks still writing.  Lane 0 watches one word (its unit) of the warp's
-                    // earliest missing row until it is written -- one load per warp and
-                    // round, not one per missing unit -- then the lanes reload what they
-                    // miss, until nothing is missing or the time limit passes.
-                    const uint64_t t0 = global_ns();
-                    while (true) {
-                        const int mine = miss ? p0 + (__ffs((int)miss) - 1) * kFinSub : INT_MAX;
-                        const int pw = __reduce_min_sync(kFullMask, mine);
-                        if (pw == INT_MAX) break;
-                        int gave_up = 0;
-                        if (lane == 0) {  // lane 0 owns unit 0 of the group, which exists
-                            const uint32_t* wq = opaque(src) + (size_t)pw * row_stride;
-                            uint32_t w1[1];
-                            ld_part<1>(wq, w1);
-                            while (w1[0] == 0u) {
-                                if (global_ns() - t0 > a.limit_ns) {
-                                    gave_up = 1;
-                                    break;
-                                }
-                                __nanosleep(128);
-                                ld_part<1>(wq, w1);
-                            }
-                        }
-                        if (__shfl_sync(kFullMask, gave_up, 0)) {
-                            late = true;
-                            break;
-                        }
-                        const uint32_t* q = opaque(q0);  // addresses recomputed, not kept live
-#pragma unroll
-                        for (int j = 0; j < L; ++j)
-                            if (miss & (1u << j)) ld_part<W>(q + j * step, v[j]);
-                        miss = 0;
-#pragma unroll
-                        for (int j = 0; j < L; ++j) miss |= has_zero<W>(v[j]) ? 1u << j : 0u;
-                    }
-                }
-                uint32_t* qz = opaque(q0);
-#pragma unroll
-                for (int j = 0; j < L; ++j)  // read: cleared for the next call
-                    if (j < nj) st_zero<W>(qz + j * step);
-#pragma unroll
-                for (int j = 0; j < L; ++j)
-#pragma unroll
-                    for (int i = 0; i < U; ++i) {
-                        if constexpr (COMPACT)
-                            S[i] += part_dec(v[j][i]);
-                        else
-                            comp_add(S[i], C[i], part_dec(v[j][2 * i]), part_dec(v[j][2 * i + 1]));
-                    }
-            }
-        }
-        // Fold the row subsets: lane (s, k) takes in lane (s + o, k) for o = 2, 1 (in units
-        // of kFinUnits lanes); lane (0, k) ends with the warp's total of unit k.
-#pragma unroll
-        for (int o = kFinSub / 2; o > 0; o >>= 1) {
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-                const float s2 = __shfl_down_sync(kFullMask, S[i], o * kFinUnits);
-                const float c2 = __shfl_down_sync(kFullMask, C[i], o * kFinUnits);
-                if constexpr (COMPACT)
-                    S[i] += s2;
-                else
-                    comp_add(S[i], C[i], s2, c2);
-            }
-        }
-        if (sub == 0) {
-            float* mine = scratch + ((size_t)warp * kFinUnits + k) * 2 * U;
-#pragma unroll
-            for (int i = 0; i < U; ++i) {
-                mine[2 * i] = S[i];
-                mine[2 * i + 1] = C[i];
-            }
-        }
-        __syncthreads();
-        if (rw == 0 && sub == 0 && act) {  // the group's warp totals, in warp order
-            float T2[U], C2[U];
-#pragma unroll
-            for (int i = 0; i < U; ++i) T2[i] = C2[i] = 0.f;
-            for (int w = warp; w < warp + RW; ++w) {
-                const float* o = scratch + ((size_t)w * kFinUnits + k) * 2 * U;
-#pragma unroll
-                for (int i = 0; i < U; ++i) {
-                    if constexpr (COMPACT)
-                        T2[i] += o[2 * i];
-                    else
-                        comp_add(T2[i], C2[i], o[2 * i], o[2 * i + 1]);
-                }
-            }
-            T* dst = static_cast<T*>(stat == 0 ? a.dgamma : a.dbeta) + (size_t)grp * U;
-#pragma unroll
-            for (int i = 0; i < U; ++i) dst[i] = IO::from_f(T2[i] + C2[i]);
-        }
-        __syncthreads();  // scratch is reused by the next group
-    }
-    if (late) raise_status(a.status, kStatusTimeout);
-}
-
-// Called by every thread of every block once the block's partial row is stored.  Blocks that
-// own no unit group of the finish are done and leave, freeing their SM; the others finish
-// their groups, picking up each block's partials as they land.
-template <typename T>
-__device__ void finish_if_owner(const KParams& a, float* scratch) {
-    const int P = (int)gridDim.x, f = (int)blockIdx.x;
-    const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
-                            : (a.cols % 2 == 0 ? 2 : 1);  // as finish_units is instantiated
-    const int ng = (2 * (a.cols / U) + kFinUnits - 1) / kFinUnits;
-    const bool finisher = (f + 1) * ng / P > f * ng / P;  // as finish_units splits the groups
-    if (!finisher) return;  // the same for every thread of the block
-    __syncthreads();        // shared memory becomes the finish's scratch
-    if (a.wait_extra && threadIdx.x == 0) {
-        // Test hook: also wait for a word that nothing writes, so the limit runs out.
-        if (!wait_counter_geq(a.ctr, 1u, a.limit_ns)) raise_status(a.status, kStatusTimeout);
-    }
-    if (a.compact) {
-        if (a.cols % 4 == 0)
-            finish_units<T, 4, true>(a, P, f, scratch);
-        else if (a.cols % 2 == 0)
-            finish_units<T, 2, true>(a, P, f, scratch);
-        else
-            finish_units<T, 1, true>(a, P, f, scratch);
-    } else {
-        if (a.cols % 2 == 0)
-            finish_units<T, 2, false>(a, P, f, scratch);
-        else
-            finish_units<T, 1, false>(a, P, f, scratch);
-    }
-}
-
-// ---------------------------------------------------------------------------------------
-// Warp per row, fed by a bulk-copy (TMA) pipeline (the forward's tile kernel, for dy and x).
-// The block owns a fixed set of tiles (7 consecutive rows each, every G-th); the producer
-// warp's lane 0 fetches each tile of dy and of x with one cp.async.bulk apiece, `stages`
-// tiles ahead; consumer warp w handles row w of every tile.  Lane l owns the columns of
-// vectors l, l+32, ... in every row, so its column sums stay in registers (Kahan-compensated
-// when KAHAN, for fp32 I/O and for long chains of rows); at the end the 7 consumer warps'
-// sums are added in warp order with TwoSum through shared memory (the drained ring) into
-// the block's (hi, lo) partial row.
-// ---------------------------------------------------------------------------------------
-// Two blocks per SM when the per-lane state (gamma, column sums and their compensations,
-// in fp32 pairs) leaves room: at most 128 registers per thread.
-template <typename T, int VPL, bool KAHAN>
-constexpr int tile_min_blocks() {
-    return (KAHAN ? 5 : 3) * VPL * Pairs<T>::kPairs <= 36 ? 2 : 1;
-}
-
-template <typename T, int VPL, bool KAHAN>
-__global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>())
-    bwd_tile_kernel(const KParams a) {
-    using IO = Io<T>;
-    constexpr int V = IO::kVec;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cols = a.cols, nvec = cols / V, stages = a.stages, rows = a.rows;
-    const RowDivisor rdiv(cols);
-    const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
-    const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
-    const unsigned slot_bytes = 2u * tile_bytes;
-    const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    const T* __restrict__ xr = static_cast<const T*>(a.xr);
-    const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
-    T* __restrict__ dx = static_cast<T*>(a.dx);
-    // This block's tiles: b, b + G, b + 2G, ... (G blocks).  Interleaved rather than a
-    // contiguous range, so the first tiles every block requests are the first tiles of the
-    // tensor and the DRAM queue serves all blocks evenly (measured on GB300: bf16 8192x1280
-    // backward 18.4 -> 17.8 us).  The assignment depends only on (rows, cols, device).
-    const int ntiles = (rows + kTileRows - 1) / kTileRows;
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int my_tiles = b < ntiles ? (ntiles - 1 - b) / G + 1 : 0;
-    auto tile_row0 = [&](int k) { return (b + k * G) * kTileRows; };  // first row of step k
-
-    if (tid == 0) {
-        for (int i = 0; i < stages; ++i) {
-            mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kTileRows);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
-    pdl_enter();
-
-    using PR = Pairs<T>;
-    constexpr int H = PR::kPairs;
-    constexpr int KV = KAHAN ? VPL : 1;
-    f2 accg[VPL][H], accb[VPL][H];  // this lane's column sums of dy * xhat and dy
-    f2 cmpg[KV][H], cmpb[KV][H];    // their Kahan compensations (the value is s - c)
-#pragma unroll
-    for (int v = 0; v < VPL; ++v)
-#pragma unroll
-        for (int h = 0; h < H; ++h) accg[v][h] = accb[v][h] = f2_splat(0.f);
-#pragma unroll
-    for (int v = 0; v < KV; ++v)
-#pragma unroll
-        for (int h = 0; h < H; ++h) cmpg[v][h] = cmpb[v][h] = f2_splat(0.f);
-
-    if (warp == kTileRows) {  // producer
-        if (lane == 0) {
-            int k = 0;
-            RingPos pos;
-            for (; k < my_tiles; ++k, pos.next(stages)) {
-                const int slot = pos.slot;
-                // With a 2-slot ring (two blocks per SM) the second tile is requested once the
-                // first has landed, so every block's first tile is ahead of all second tiles
-                // in the DRAM queue and the late blocks start sooner (measured on GB300: bf16
-                // 8192x768 backward 12.6 -> 12.2 us; with a 4-slot ring, one block per SM,
-                // holding back the rest of the first fill was slower: bf16 8192x1280
-                // 16.3 -> 17.2 us).  A timeout here shows again in the consumers' wait.
-                if (k == 1 && stages == 2) (void)mbar_wait(&full_bar[0], 0u, a.limit_ns);
-                // A slot's second and later fills wait for the consumers of the previous pass.
-                if (k >= stages && !mbar_wait(&empty_bar[slot], pos.phase ^ 1u, a.limit_ns)) {
-                    raise_status(a.status, kStatusTimeout);
-                    break;
-                }
-                const int r0 = tile_row0(k);
-                const unsigned bytes = (unsigned)min(kTileRows, rows - r0) * row_bytes;
-                unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
-                mbar_arrive_expect_tx(&full_bar[slot], 2u * bytes);
-                bulk_g2s(dst, dy + (size_t)r0 * cols, bytes, &full_bar[slot]);
-                bulk_g2s(dst + tile_bytes, xr + (size_t)r0 * cols, bytes, &full_bar[slot]);
-            }
-            for (int j = max(0, k - stages); j < k; ++j)  // drain: every copy has landed
-                (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
-        }
-    } else {  // consumers
-        f2 gm[VPL][H];  // gamma of this lane's columns as fp32 pairs, loaded once
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
-        }
-        // One or two rows through both passes.  With two (the warp's row of tile k and of
-        // tile k + 1), their first passes run together, their four row sums share one
-        // butterfly and their second passes run together; per lane the column sums still add
-        // tile k's terms before tile k + 1's, so the results are those of one row at a time.
-        auto body = [&](auto nr_c, const int (&row_)[2], const int (&slot_)[2],
-                        const float (&mu_)[2], const float (&rs_)[2]) {
-            constexpr int NR = decltype(nr_c)::value;
-            const T* dys[NR];
-            const T* xs[NR];
-            f2 mu2[NR], rs2[NR], sg[NR], sgx[NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                dys[r] = reinterpret_cast<const T*>(smem_raw + (size_t)slot_[r] * slot_bytes +
-                                                    (size_t)warp * row_bytes);
-                xs[r] = dys[r] + (size_t)kTileRows * cols;
-                mu2[r] = f2_splat(mu_[r]);
-                rs2[r] = f2_splat(rs_[r]);
-                // Row sums; the low halves take the even columns, the high halves the odd.
-                sg[r] = sgx[r] = f2_splat(0.f);
-            }
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
-                if (vi < nvec) {
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) {
-                        f2 d[H], xx[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
-#pragma unroll
-                        for (int h = 0; h < H; ++h) {
-                            const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
-                            const f2 g = f2_mul(gm[v][h], d[h]);
-                            sg[r] = f2_add(sg[r], g);
-                            sgx[r] = f2_fma(g, xh, sgx[r]);
-                            if constexpr (KAHAN) {
-                                kahan2(accg[v][h], cmpg[v][h], f2_mul(d[h], xh));
-                                kahan2(accb[v][h], cmpb[v][h], d[h]);
-                            } else {
-                                accg[v][h] = f2_fma(d[h], xh, accg[v][h]);
-                                accb[v][h] = f2_add(accb[v][h], d[h]);
-                            }
-                        }
-                    }
-                }
-            }
-            // The one reduction of each row: both of its sums together (xor butterfly).
-            float t[2 * NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                t[2 * r] = f2_lo(sg[r]) + f2_hi(sg[r]);
-                t[2 * r + 1] = f2_lo(sgx[r]) + f2_hi(sgx[r]);
-            }
-#pragma unroll
-            for (int r = 0; r < NR; ++r) warp_sum2(t[2 * r], t[2 * r + 1]);
-            // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
-            // g - mg cancels exactly where it should (a one-column row gives dx = 0).
-            f2 mg2[NR], mgx2[NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                mg2[r] = f2_splat(rdiv.div(t[2 * r]));
-                mgx2[r] = f2_splat(rdiv.div(t[2 * r + 1]));
-            }
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
-                if (vi < nvec) {  // second pass re-reads the rows from shared memory
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) {
-                        f2 d[H], xx[H], o[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
-#pragma unroll
-                        for (int h = 0; h < H; ++h) {
-                            const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
-                            const f2 g = f2_mul(gm[v][h], d[h]);
-                            o[h] = f2_mul(rs2[r], f2_sub(g, f2_fma(xh, mgx2[r], mg2[r])));
-                        }
-                        st_stream(dx + (size_t)row_[r] * cols + (size_t)vi * V, PR::pack(o));
-                    }
-                }
-            }
-        };
-        // Rows go in pairs of consecutive tiles when the ring is deep enough that the pair's
-        // two slots still leave tiles in flight behind them.  The paired form is built for
-        // bf16 rows of 4 or 5 vectors per lane and for fp32 rows, where it measured faster on
-        // GB300 (bf16 8192x1280: 21.8 -> 19.9 us; fp32 262144x1000: 544 -> 507 us, there
-        // even at ring depths that keep it to one row at a time); bf16 rows of 3 or fewer
-        // vectors per lane measured slower with it.
-        constexpr bool kPairRows = (Io<T>::kVec == 8 && VPL >= 4) || Io<T>::kVec == 4;
-        const int pair_max = (kPairRows && stages >= 4) ? 2 : 1;
-        // mean and rstd of the next step's rows are loaded a step ahead, so their latency is
-        // not on the rows' critical path.
-        auto load_stats = [&](int kk, int nr, float (&mu)[2], float (&rs)[2]) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int rr = tile_row0(kk + r) + warp;
-                const bool valid = r < nr && kk + r < my_tiles && rr < rows;
-                mu[r] = valid ? a.mean[rr] : 0.f;
-                rs[r] = valid ? a.rstd[rr] : 0.f;
-            }
-        };
-        float mu_n[2], rs_n[2];
-        load_stats(0, min(pair_max, my_tiles), mu_n, rs_n);
-        RingPos pos;
-        for (int k = 0; k < my_tiles;) {
-            const int nr = min(pair_max, my_tiles - k);
-            int slots[2];
-            unsigned phases[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                slots[r] = pos.slot;
-                phases[r] = pos.phase;
-                if (r < nr) pos.next(stages);
-            }
-            const float mu[2] = {mu_n[0], mu_n[1]}, rs[2] = {rs_n[0], rs_n[1]};
-            if (k + nr < my_tiles) load_stats(k + nr, min(pair_max, my_tiles - k - nr), mu_n, rs_n);
-            bool ok = mbar_wait(&full_bar[slots[0]], phases[0], a.limit_ns);
-            if (nr == 2) ok = mbar_wait(&full_bar[slots[1]], phases[1], a.limit_ns) && ok;
-            if (!__all_sync(kFullMask, ok)) {
-                if (lane == 0) raise_status(a.status, kStatusTimeout);
-                break;
-            }
-            const int rws[2] = {tile_row0(k) + warp, tile_row0(k + 1) + warp};
-            if constexpr (kPairRows) {
-                if (nr == 2 && rws[1] < rows)
-                    body(std::integral_constant<int, 2>{}, rws, slots, mu, rs);
-                else if (rws[0] < rows)
-                    body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
-            } else if (rws[0] < rows) {
-                body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
-            }
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&empty_bar[slots[0]]);
-                if (nr == 2) mbar_arrive(&empty_bar[slots[1]]);
-            }
-            k += nr;
-        }
-    }
-    __syncthreads();  // the ring is drained and no warp reads it any more
-
-    // Block partial row.  The consumer warps put their sums in shared memory as
-    // [stat][warp][cols] floats (the drained ring), followed by the negated compensations in
-    // the same layout when KAHAN; then each thread adds the 7 warps' values of a group of 4
-    // columns in warp order (with TwoSum when KAHAN) and stores the block's partials of them.
-    float* smem_f = reinterpret_cast<float*>(smem_raw);
-    const size_t lo_off = (size_t)2 * kTileRows * cols;
-    auto put = [&](float* dst, f2 a0, f2 a1) {
-        *reinterpret_cast<float4*>(dst) = make_float4(f2_lo(a0), f2_hi(a0), f2_lo(a1), f2_hi(a1));
-    };
-    if (warp < kTileRows) {
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
-            if (vi < nvec) {
-                float* dg = smem_f + (size_t)warp * cols + (size_t)vi * V;
-                float* db = dg + (size_t)kTileRows * cols;
-                const f2 z = f2_splat(0.f);
-                if constexpr (H == 4) {
-                    // A lane's 8 columns are two 16-byte halves at a 32-byte lane stride.
-                    // Lanes 4-7 of each group of 8 store their upper half first, so the 8
-                    // lanes of a 128-bit store phase hit 8 distinct groups of 4 banks.
-                    const bool sw = ((lane >> 2) & 1) != 0;
-                    const int o0 = sw ? 4 : 0, o1 = sw ? 0 : 4;
-                    put(dg + o0, sw ? accg[v][2] : accg[v][0], sw ? accg[v][3] : accg[v][1]);
-                    put(db + o0, sw ? accb[v][2] : accb[v][0], sw ? accb[v][3] : accb[v][1]);
-                    put(dg + o1, sw ? accg[v][0] : accg[v][2], sw ? accg[v][1] : accg[v][3]);
-                    put(db + o1, sw ? accb[v][0] : accb[v][2], sw ? accb[v][1] : accb[v][3]);
-                    if constexpr (KAHAN) {
-                        put(dg + lo_off + o0, f2_sub(z, sw ? cmpg[v][2] : cmpg[v][0]),
-                            f2_sub(z, sw ? cmpg[v][3] : cmpg[v][1]));
-                        put(db + lo_off + o0, f2_sub(z, sw ? cmpb[v][2] : cmpb[v][0]),
-                            f2_sub(z, sw ? cmpb[v][3] : cmpb[v][1]));
-                        put(dg + lo_off + o1, f2_sub(z, sw ? cmpg[v][0] : cmpg[v][2]),
-                            f2_sub(z, sw ? cmpg[v][1] : cmpg[v][3]));
-                        put(db + lo_off + o1, f2_sub(z, sw ? cmpb[v][0] : cmpb[v][2]),
-                            f2_sub(z, sw ? cmpb[v][1] : cmpb[v][3]));
-                    }
-                } else {  // fp32: one 16-byte store per vector, consecutive lanes adjacent
-                    put(dg, accg[v][0], accg[v][1]);
-                    put(db, accb[v][0], accb[v][1]);
-                    if constexpr (KAHAN) {
-                        put(dg + lo_off, f2_sub(z, cmpg[v][0]), f2_sub(z, cmpg[v][1]));
-                        put(db + lo_off, f2_sub(z, cmpb[v][0]), f2_sub(z, cmpb[v][1]));
-                    }
-                }
-            }
-        }
-    }
-    __syncthreads();
-    const int P = gridDim.x;
-    const int quarter = cols >> 2;  // groups of 4 columns per statistic (cols is a multiple of 4)
-    for (int u = tid; u < 2 * quarter; u += blockDim.x) {
-        const int stat = u >= quarter ? 1 : 0;
-        const int c = 4 * (u - stat * quarter);
-        const float* src = smem_f + (size_t)stat * kTileRows * cols + c;
-        if constexpr (KAHAN) {
-            float S[4] = {0.f, 0.f, 0.f, 0.f}, C[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kTileRows; ++w) {
-                const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
-                const float4 l = *reinterpret_cast<const float4*>(src + lo_off + (size_t)w * cols);
-                comp_add(S[0], C[0], t.x, l.x);
-                comp_add(S[1], C[1], t.y, l.y);
-                comp_add(S[2], C[2], t.z, l.z);
-                comp_add(S[3], C[3], t.w, l.w);
-            }
-            float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c);
-            st_part4(dst, S[0], C[0], S[1], C[1]);
-            st_part4(dst + 1, S[2], C[2], S[3], C[3]);
-        } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
-            f2 S01 = f2_splat(0.f), S23 = f2_splat(0.f);
-#pragma unroll
-            for (int w = 0; w < kTileRows; ++w) {
-                const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
-                S01 = f2_add(S01, f2_make(t.x, t.y));
-                S23 = f2_add(S23, f2_make(t.z, t.w));
-            }
-            st_part4(reinterpret_cast<float*>(a.part) + ((size_t)stat * P + blockIdx.x) * cols + c,
-                     f2_lo(S01), f2_hi(S01), f2_lo(S23), f2_hi(S23));
-        }
-    }
-    finish_if_owner<T>(a, smem_f);
-}
-
-// ---------------------------------------------------------------------------------------
-// Block per row with bulk-copy staging of dy and x rows (several rows ahead).  Thread t of
-// the block (blockDim.x threads) owns the columns of vectors t, t + blockDim.x, ... in
-// every row, so its column sums stay in registers (compensated when KAHAN) and go straight
-// to the block's partial row.
-// ---------------------------------------------------------------------------------------
-template <typename T, int VPT, bool KAHAN>
-__global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const KParams a) {
-    using IO = Io<T>;
-    constexpr int V = IO::kVec;
-    constexpr int MAXW = kBwdBlockMaxThreads / 32;
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    __shared__ uint64_t full_bar[kMaxStages];
-    __shared__ float red[2][MAXW];
-    __shared__ int abort_flag;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthreads = blockDim.x, nw = nthreads >> 5;
-    const int cols = a.cols, nvec = cols / V, stages = a.stages;
-    const RowDivisor rdiv(cols);
-    const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
-    const unsigned slot_bytes = 2u * row_bytes;
-    const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    const T* __restrict__ xr = static_cast<const T*>(a.xr);
-    const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
-    T* __restrict__ dx = static_cast<T*>(a.dx);
-    // This block's rows: b, b + G, b + 2G, ... (G blocks), interleaved as in the tile kernel.
-    const int G = (int)gridDim.x, b = (int)blockIdx.x;
-    const int nmy = b < a.rows ? (a.rows - 1 - b) / G + 1 : 0;
-
-    if (tid == 0) {
-        for (int i = 0; i < stages; ++i) mbar_init(&full_bar[i], 1);
-        abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-    // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
-    pdl_enter();
-    auto issue = [&](int k, int slot) {  // thread 0 only: fetch the block's k-th row into `slot`
-        if (k >= nmy) return;
-        const int row = b + k * G;
-        unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
-        mbar_arrive_expect_tx(&full_bar[slot], slot_bytes);
-        bulk_g2s(dst, dy + (size_t)row * cols, row_bytes, &full_bar[slot]);
-        bulk_g2s(dst + row_bytes, xr + (size_t)row * cols, row_bytes, &full_bar[slot]);
-    };
-    if (tid == 0)
-        for (int k = 0; k < stages; ++k) issue(k, k);
-
-    using PR = Pairs<T>;
-    constexpr int H = PR::kPairs;
-    constexpr int KV = KAHAN ? VPT : 1;
-    f2 gp[VPT][H];            // gamma of this thread's columns as fp32 pairs
-    f2 sg[VPT][H], sb[VPT][H];  // running column sums of dy * xhat and dy
-    f2 cg[KV][H], cb[KV][H];    // their Kahan compensations (the value is s - c)
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int vi = v * nthreads + tid;
-        PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
-#pragma unroll
-        for (int h = 0; h < H; ++h) sg[v][h] = sb[v][h] = f2_splat(0.f);
-    }
-#pragma unroll
-    for (int v = 0; v < KV; ++v)
-#pragma unroll
-        for (int h = 0; h < H; ++h) cg[v][h] = cb[v][h] = f2_splat(0.f);
-
-    int k = 0;
-    // mean and rstd are loaded one row ahead (off the row's critical path).
-    float mu_next = nmy > 0 ? a.mean[b] : 0.f, rs_next = nmy > 0 ? a.rstd[b] : 0.f;
-    RingPos pos;
-    for (int row = b; k < nmy; row += G, ++k, pos.next(stages)) {
-        const int slot = pos.slot;
-        const float mu = mu_next, rs = rs_next;
-        if (k + 1 < nmy) {
-            mu_next = a.mean[row + G];
-            rs_next = a.rstd[row + G];
-        }
-        if (!mbar_wait(&full_bar[slot], pos.phase, a.limit_ns)) abort_flag = 1;
-        const T* dys = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
-        const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
-        const size_t base = (size_t)row * cols;
-        const f2 mu2 = f2_splat(mu), rs2 = f2_splat(rs);
-        f2 rg = f2_splat(0.f), rgx = f2_splat(0.f);  // row sums: even columns low, odd high
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int vi = v * nthreads + tid;
-            if (vi < nvec) {
-                f2 d[H], xx[H];
-                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-#pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
-                    const f2 g = f2_mul(gp[v][h], d[h]);
-                    rg = f2_add(rg, g);
-                    rgx = f2_fma(g, xh, rgx);
-                    if constexpr (KAHAN) {
-                        kahan2(sg[v][h], cg[v][h], f2_mul(d[h], xh));
-                        kahan2(sb[v][h], cb[v][h], d[h]);
-                    } else {
-                        sg[v][h] = f2_fma(d[h], xh, sg[v][h]);
-                        sb[v][h] = f2_add(sb[v][h], d[h]);
-                    }
-                }
-            }
-        }
-        float tg = f2_lo(rg) + f2_hi(rg), tgx = f2_lo(rgx) + f2_hi(rgx);
-        warp_sum2(tg, tgx);
-        if (lane == 0) {
-            red[0][warp] = tg;
-            red[1][warp] = tgx;
-        }
-        __syncthreads();  // the one cross-warp exchange of the row
-        if (abort_flag) break;
-        tg = 0.f;
-        tgx = 0.f;
-        for (int w = 0; w < nw; ++w) {  // same order in every thread
-            tg += red[0][w];
-            tgx += red[1][w];
-        }
-        const f2 mg2 = f2_splat(rdiv.div(tg)), mgx2 = f2_splat(rdiv.div(tgx));
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int vi = v * nthreads + tid;
-            if (vi < nvec) {
-                f2 d[H], xx[H], o[H];
-                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
-#pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
-                    const f2 g = f2_mul(gp[v][h], d[h]);
-                    o[h] = f2_mul(rs2, f2_sub(g, f2_fma(xh, mgx2, mg2)));
-                }
-                st_stream(dx + base + (size_t)vi * V, PR::pack(o));
-            }
-        }
-        __syncthreads();  // slot and `red` free again
-        if (tid == 0) issue(k + stages, slot);  // row k + stages takes row k's slot
-    }
-
-    if (abort_flag) {
-        if (tid == 0) {
-            raise_status(a.status, kStatusTimeout);
-            for (int j = k; j < k + stages && j < nmy; ++j)
-                (void)mbar_wait(&full_bar[j % stages], (unsigned)(j / stages) & 1u, a.limit_ns);
-        }
-        __syncthreads();
-        return;  // no partial row: the finishing blocks' bounded polls run out as well
-    }
-
-    // Partial row: (hi, lo) for each column, two columns per 16-byte store; plain sums four
-    // columns per 16-byte store when the sums are not compensated.
-    const int P = gridDim.x;
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int vi = v * nthreads + tid;
-        if (vi < nvec) {
-            if constexpr (KAHAN) {
-                float2* pg = a.part + (size_t)blockIdx.x * cols + (size_t)vi * V;
-                float2* pb = a.part + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
-#pragma unroll
-                for (int h = 0; h < H; ++h) {
-                    st_part4(pg + 2 * h, f2_lo(sg[v][h]), -f2_lo(cg[v][h]), f2_hi(sg[v][h]), -f2_hi(cg[v][h]));
-                    st_part4(pb + 2 * h, f2_lo(sb[v][h]), -f2_lo(cb[v][h]), f2_hi(sb[v][h]), -f2_hi(cb[v][h]));
-                }
-            } else {
-                float* pg = reinterpret_cast<float*>(a.part) + (size_t)blockIdx.x * cols + (size_t)vi * V;
-                float* pb = reinterpret_cast<float*>(a.part) + ((size_t)P + blockIdx.x) * cols + (size_t)vi * V;
-#pragma unroll
-                for (int h = 0; h < H; h += 2) {
-                    st_part4(pg + 2 * h, f2_lo(sg[v][h]), f2_hi(sg[v][h]), f2_lo(sg[v][h + 1]), f2_hi(sg[v][h + 1]));
-                    st_part4(pb + 2 * h, f2_lo(sb[v][h]), f2_hi(sb[v][h]), f2_lo(sb[v][h + 1]), f2_hi(sb[v][h + 1]));
-                }
-            }
-        }
-    }
-    finish_if_owner<T>(a, reinterpret_cast<float*>(smem_raw));
-}
-
-// ---------------------------------------------------------------------------------------
-// Scalar kernel (any alignment, any width).  Each column is owned by one thread of the
-// block; its compensated running sums live in shared memory when 16 bytes per column fit,
-// else in a region of the workspace behind the partial rows (L2-resident), so that the
-// partial rows themselves are written only once, when they are final.
-// ---------------------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(kBwdScalarThreads, 1) bwd_scalar_kernel(const KParams a) {
-    using IO = Io<T>;
-    pdl_enter();
-    constexpr int NW = kBwdScalarThreads / 32;
-    extern __shared__ __align__(16) float smem_f[];
-    __shared__ float red[2][NW];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int cols = a.cols, P = gridDim.x;
-    const RowDivisor rdiv(cols);
-    const T* __restrict__ dy = static_cast<const T*>(a.dy);
-    const T* __restrict__ xr = static_cast<const T*>(a.xr);
-    const T* __restrict__ gamma = static_cast<const T*>(a.gamma);
-    T* __restrict__ dx = static_cast<T*>(a.dx);
-    int r0, r1;
-    row_range(a.rows, r0, r1);
-    // acc_g[c] = (s, c) Kahan pair of dgamma, acc_b[c] the one of dbeta.
-    const bool in_smem = a.stages != 0;  // the host sets it when 16 * cols bytes fit
-    float2* acc_g = in_smem ? reinterpret_cast<float2*>(smem_f)
-                            : a.acc + (size_t)blockIdx.x * cols;
-    float2* acc_b = in_smem ? reinterpret_cast<float2*>(smem_f) + cols
-                            : a.acc + ((size_t)P + blockIdx.x) * cols;
-    for (int j = tid; j < cols; j += kBwdScalarThreads)
-        acc_g[j] = acc_b[j] = make_float2(0.f, 0.f);
-
-    for (int row = r0; row < r1; ++row) {
-        const size_t base = (size_t)row * cols;
-        const float mu = a.mean[row], rs = a.rstd[row];
-        float sg = 0.f, sgx = 0.f;
-        for (int j = tid; j < cols; j += kBwdScalarThreads) {
-            const float d = IO::to_f(dy[base + j]);
-            const float xh = (IO::to_f(xr[base + j]) - mu) * rs;
-            const float g = __fmul_rn(IO::to_f(gamma[j]), d);
-            sg += g;
-            sgx += g * xh;
-            float2 pg = acc_g[j], pb = acc_b[j];
-            kahan_add(pg.x, pg.y, __fmul_rn(d, xh));
-            kahan_add(pb.x, pb.y, d);
-            acc_g[j] = pg;
-            acc_b[j] = pb;
-        }
-        warp_sum2(sg, sgx);
-        if (lane == 0) {
-            red[0][warp] = sg;
-            red[1][warp] = sgx;
-        }
-        __syncthreads();
-        float tg = 0.f, tgx = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            tg += red[0][w];
-            tgx += red[1][w];
-        }
-        const float mg = rdiv.div(tg), mgx = rdiv.div(tgx);
-        for (int j = tid; j < cols; j += kBwdScalarThreads) {
-            const float d = IO::to_f(dy[base + j]);
-            const float xh = (IO::to_f(xr[base + j]) - mu) * rs;
-            dx[base + j] = IO::from_f(rs * (__fmul_rn(IO::to_f(gamma[j]), d) - (mg + xh * mgx)));
-        }
-        __syncthreads();
-    }
-    // Partial row as (hi, lo): Kahan's value is s - c.
-    for (int j = tid; j < cols; j += kBwdScalarThreads) {
-        const float2 pg = acc_g[j], pb = acc_b[j];
-        st_part2(a.part + (size_t)blockIdx.x * cols + j, pg.x, -pg.y);
-        st_part2(a.part + ((size_t)P + blockIdx.x) * cols + j, pb.x, -pb.y);
-        if (!in_smem) acc_g[j] = acc_b[j] = make_float2(0.f, 0.f);  // the workspace is left zero
-    }
-    __syncthreads();  // the shared accumulators become the finish scratch
-    finish_if_owner<T>(a, smem_f);
-}
-
-// ---------------------------------------------------------------------------------------
-// Host side.
-// ---------------------------------------------------------------------------------------
-// Warp path: up to 8 vectors per lane for fp32 (1024 columns), 5 for bf16 (1280 columns),
-// 4 for bf16 with compensated sums: beyond that the register-resident column sums no
-// longer fit without spilling.
-template <typename T, bool K>
-const void* warp_kernel_k(int vpl) {
-    switch (vpl) {
-        case 1: return (const void*)bwd_tile_kernel<T, 1, K>;
-        case 2: return (const void*)bwd_tile_kernel<T, 2, K>;
-        case 3: return (const void*)bwd_tile_kernel<T, 3, K>;
-        case 4: return (const void*)bwd_tile_kernel<T, 4, K>;
-        default: break;
-    }
-    if constexpr (Io<T>::kVec == 8) {
-        if (vpl == 5 && !K) return (const void*)bwd_tile_kernel<T, 5, false>;
-    } else {
-        switch (vpl) {
-            case 5: return (const void*)bwd_tile_kernel<T, 5, K>;
-            case 6: return (const void*)bwd_tile_kernel<T, 6, K>;
-            case 7: return (const void*)bwd_tile_kernel<T, 7, K>;
-            case 8: return (const void*)bwd_tile_kernel<T, 8, K>;
-            default: break;
-        }
-    }
-    return nullptr;
-}
-
-template <typename T>
-const void* warp_kernel(int vpl, bool kahan) {
-    return kahan ? warp_kernel_k<T, true>(vpl) : warp_kernel_k<T, false>(vpl);
-}
-
-int warp_max_vpl(Dtype dt, bool kahan) { return dt == Dtype::F32 ? 8 : (kahan ? 4 : 5); }
-
-// Block path: cols <= 16384 and 512 threads give at most 4 vectors per thread for bf16 and
-// 8 for fp32.  Compensated (Kahan) column sums where the plan asks for them: the registers
-// are there for at most 16 columns per thread.
-template <typename T>
-const void* block_kernel(int vpt, bool kahan) {
-    if constexpr (Io<T>::kVec == 8) {
-        switch (vpt) {
-            case 1: return kahan ? (const void*)bwd_block_kernel<T, 1, true> : (const void*)bwd_block_kernel<T, 1, false>;
-            case 2: return kahan ? (const void*)bwd_block_kernel<T, 2, true> : (const void*)bwd_block_kernel<T, 2, false>;
-            case 3: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 3, false>;
-            case 4: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 4, false>;
-            default: return nullptr;
-        }
-    } else {
-        switch (vpt) {
-            case 1: return kahan ? (const void*)bwd_block_kernel<T, 1, true> : (const void*)bwd_block_kernel<T, 1, false>;
-            case 2: return kahan ? (const void*)bwd_block_kernel<T, 2, true> : (const void*)bwd_block_kernel<T, 2, false>;
-            case 3: return kahan ? (const void*)bwd_block_kernel<T, 3, true> : (const void*)bwd_block_kernel<T, 3, false>;
-            case 4: return kahan ? (const void*)bwd_block_kernel<T, 4, true> : (const void*)bwd_block_kernel<T, 4, false>;
-            case 5: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 5, false>;
-            case 6: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 6, false>;
-            case 7: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 7, false>;
-            case 8: return kahan ? nullptr : (const void*)bwd_block_kernel<T, 8, false>;
-            default: return nullptr;
-        }
-    }
-}
-
-const void* kernel_for(Dtype dt, const BwdPlan& p) {
-    const bool f = dt == Dtype::F32;
-    if (p.path == kPathWarp)
-        return f ? warp_kernel<float>(p.per_thread, p.kahan)
-                 : warp_kernel<__nv_bfloat16>(p.per_thread, p.kahan);
-    if (p.path == kPathBlock)
-        return f ? block_kernel<float>(p.per_thread, p.kahan)
-                 : block_kernel<__nv_bfloat16>(p.per_thread, p.kahan);
-    return f ? (const void*)bwd_scalar_kernel<float> : (const void*)bwd_scalar_kernel<__nv_bfloat16>;
-}
-
-}  // namespace
 
 int bwd_max_grid(int rows, int sms) { return std::max(1, std::min(rows, sms * 8)); }
 
-cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_override,
+cudaError_t plan_bwd(Dtype dt, bool rms, int rows, int cols, bool aligned, int path_override,
                      BwdPlan* plan) {
-    const DeviceInfo& di = device_info(-1);
-    const int V = dt == Dtype::F32 ? 4 : 8;
-    const int esize = dt == Dtype::F32 ? 4 : 2;
-    BwdPlan p;
-    if (aligned && path_override != kPathScalar) {
-        const int nvec = cols / V;
-        const int vpl = (nvec + 31) / 32;
-        // The warp path keeps each lane's column sums over all the rows its warp handles:
-        // compensated for fp32 I/O, and for bf16 once those chains can get long.
-        const bool wk = dt == Dtype::F32 || rows > kWarpPathMaxRows;
-        const bool warp_fits = vpl <= warp_max_vpl(dt, wk);
-        if (warp_fits && (path_override == kPathWarp || path_override == kPathAuto)) {
-            p.path = kPathWarp;
-            p.per_thread = vpl;
-            p.threads = kTileThreads;
-            p.kahan = wk;
-            const size_t slot = 2ull * kTileRows * cols * esize;  // a tile of dy and of x
-            const size_t combine = (wk ? 4ull : 2ull) * kTileRows * cols * 4;
-            // About four tiles in flight per SM, split over the blocks the registers allow
-            // on an SM, within each block's share of its shared memory.  Measured on GB300:
-            // deeper rings request a block's whole share of rows at once, the DRAM queue then
-            // serves blocks roughly in launch order and the late ones set the kernel's end
-            // (bf16 8192x768, two blocks per SM: 5 stages 14.2 us, 2 stages 13.5 us; bf16
-            // 8192x1280, one block per SM: 6 stages 18.8 us, 4 stages 18.5 us, 2 stages 19.4 us).
-            const void* kern = kernel_for(dt, p);
-            if (!kern) return cudaErrorInvalidValue;
-            const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
-            const size_t share = std::min<size_t>(
-                (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
-            int stages = (int)std::min<size_t>(std::min(kMaxStages, 4 / occ_regs), share / slot);
-            stages = std::max(2, stages);
-            p.stages = stages;
-            // The ring, reused afterwards for the warps' sums.
-            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)kTileThreads * 32});
-        } else {
-            p.path = kPathBlock;
-            p.per_thread = (nvec + kBwdBlockMaxThreads - 1) / kBwdBlockMaxThreads;
-            const int t = (nvec + p.per_thread - 1) / p.per_thread;
-            p.threads = std::max(32, (t + 31) / 32 * 32);
-            // Compensated column sums: always for fp32 I/O (as far as the registers go); for
-            // bf16 only when a thread's chain of rows can be long (more than 64 rows per
-            // block even at one block per SM): over short chains an fp32 sum is far more
-            // accurate than the bf16 result it is rounded to.
-            p.kahan = dt == Dtype::F32 ? p.per_thread <= 4
-                                       : (p.per_thread <= 2 && rows > 64 * di.sms);
-            const size_t slot = 2ull * cols * esize;  // a row of dy and of x
-            const void* kern = kernel_for(dt, p);
-            if (!kern) return cudaErrorInvalidValue;
-            const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
-            const size_t share = std::min<size_t>(
-                (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
-            // Rows in flight: up to 4, within the block's share of shared memory (measured on
-            // GB300, deeper prefetch only delays every block's first row).
-            const int stages = (int)std::min<size_t>(kBlockStages, share / slot);
-            p.stages = std::max(1, stages);
-            p.smem = std::max<size_t>((size_t)p.stages * slot, (size_t)p.threads * 32);
-        }
-    }
-    if (p.path == kPathAuto) {
-        p.path = kPathScalar;
-        p.threads = kBwdScalarThreads;
-        const size_t acc = 16ull * cols;  // (hi, lo) pairs for both statistics
-        const bool fits = bwd_scalar_acc_in_smem(cols, (size_t)di.smem_optin);
-        p.smem = std::max<size_t>(fits ? acc : 0, (size_t)kBwdScalarThreads * 16);
-        p.stages = fits ? 1 : 0;  // tells the kernel where its accumulators live
-    }
-    if (p.smem > (size_t)di.smem_optin) return cudaErrorInvalidValue;
-    const void* kern = kernel_for(dt, p);
-    if (!kern) return cudaErrorInvalidValue;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return e;
-    const int occ = blocks_per_sm(kern, p.threads, p.smem);
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int need = p.path == kPathWarp ? (rows + kTileRows - 1) / kTileRows : rows;
-    p.grid = std::max(1, std::min(need, di.sms * occ));
-    *plan = p;
-    return cudaSuccess;
+    if (rms) return plan_rms_bwd(dt, rows, cols, aligned, path_override, plan);
+    return plan_bwd_t<false>(dt, rows, cols, aligned, path_override, plan);
 }
 
-cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStream_t stream,
+cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStream_t stream,
                        int* launches) {
-    *launches = 0;
-    const void* kern = kernel_for(dt, p);
-    if (!kern) return cudaErrorInvalidValue;
-    KParams k;
-    k.dy = a.dy;
-    k.xr = a.xr;
-    k.gamma = a.gamma;
-    k.mean = a.mean;
-    k.rstd = a.rstd;
-    k.dx = a.dx;
-    k.dgamma = a.dgamma;
-    k.dbeta = a.dbeta;
-    k.rows = a.rows;
-    k.cols = a.cols;
-    k.part = reinterpret_cast<float2*>(a.partials);
-    k.acc = bwd_plan_acc_region(p) ? k.part + 2ull * (size_t)p.grid * (size_t)a.cols : nullptr;
-    k.compact = (p.path == kPathScalar || p.kahan) ? 0 : 1;
-    {
-        // Warps per unit group in the finish: the fewest (a divisor of the warp count) for
-        // which one batch of loads per lane covers all P partial rows.
-        const int nw = p.threads / 32;
-        const int U = k.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
-                                : (a.cols % 2 == 0 ? 2 : 1);
-        const int rows_per_warp_batch = kFinSub * fin_rows_per_lane((k.compact ? 1 : 2) * U);
-        const int need = (p.grid + rows_per_warp_batch - 1) / rows_per_warp_batch;
-        int rw = nw;
-        for (int d = 1; d <= nw; ++d)
-            if (nw % d == 0 && d >= need) {
-                rw = d;
-                break;
-            }
-        k.fin_rw = rw;
-    }
-    k.ctr = a.counters;
-    k.status = a.status;
-    k.limit_ns = a.wait_limit_ns;
-    k.wait_extra = a.wait_extra;
-    k.stages = p.stages;
-    void* args[] = {&k};
-    // A cooperative launch: all blocks co-resident, as the finish's polls need.
-    cudaError_t e = launch_kernel(kern, dim3(p.grid), dim3(p.threads), p.smem, stream, args, true);
-    if (e == cudaSuccess) *launches = 1;
-    return e;
+    if (plan.rms) return launch_rms_bwd(dt, a, plan, stream, launches);
+    return launch_bwd_t<false>(dt, a, plan, stream, launches);
 }
 
 }  // namespace lnk

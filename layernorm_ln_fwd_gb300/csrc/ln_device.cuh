@@ -285,12 +285,12 @@ __device__ __forceinline__ void chan_reduce_any(float n, float& S, float& m, flo
     }
 }
 
-// The row's shift K: the median of five of its stored values (in the block and scalar
-// kernels those at columns 0, C/4, C/2, 3C/4 and C - 1; in the warp kernel the first values
-// of five lanes spread over the row).  Any K gives the same M2; K only sets the size of the shifted values d, whose
-// rounding (when |d| is large next to s) and whose mean's rounding reach xhat as about the
-// unit roundoff times |K - mean| * rstd.  The median of a spread sample stays within the
-// body of the row whatever a few values (an outlier in the first column, say) are.
+// The shift K of the scalar kernel's Welford summaries: the median of five of the row's
+// stored values, at columns 0, C/4, C/2, 3C/4 and C - 1.  Any K gives the same M2; K only
+// sets the size of the shifted values d, whose rounding (when |d| is large next to s) and
+// whose mean's rounding reach xhat as about the unit roundoff times |K - mean| * rstd.  The
+// median of a spread sample stays within the body of the row whatever a few values (an
+// outlier in the first column, say) are.
 __device__ __forceinline__ float median5(float a, float b, float c, float d, float e) {
     const float f = fmaxf(fminf(a, b), fminf(c, d));
     const float g = fminf(fmaxf(a, b), fmaxf(c, d));

@@ -48,11 +48,11 @@ struct BwdArgs {
     const void* dy;
     const void* xr;
     const void* gamma;
-    const float* mean;
-    const float* rstd;
+    const float* mean;    // null for the RMSNorm backward
+    const float* rstd;    // rstd, or the RMSNorm's 1 / rms
     void* dx;
     void* dgamma;
-    void* dbeta;
+    void* dbeta;          // null for the RMSNorm backward
     int rows;
     int cols;
     float* partials;      // [2][grid][cols] (hi, lo) fp32 pairs: dgamma, then dbeta
@@ -64,6 +64,7 @@ struct BwdArgs {
 
 // A launch plan for the backward: which kernel, how many blocks (= rows of partials).
 struct BwdPlan {
+    bool rms = false;     // the RMSNorm backward (one row sum, one column sum: dgamma)
     int path = kPathAuto;
     int per_thread = 0;   // vectors per lane (warp path) or per thread (block path)
     int threads = 0;
@@ -84,9 +85,16 @@ cudaError_t launch_kernel(const void* kern, dim3 grid, dim3 block, size_t smem,
 
 cudaError_t launch_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
                        cudaStream_t stream, int* launches);
+// The RMSNorm forward: `beta` and `mean` are unused (may be null); `rstd` receives 1 / rms.
+cudaError_t launch_rms_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
+                           cudaStream_t stream, int* launches);
 
-cudaError_t plan_bwd(Dtype dt, int rows, int cols, bool aligned, int path_override,
+// Plans (kernel, grid, shared memory) the backward of a LayerNorm, or of an RMSNorm when
+// `rms` (then the plan's launch goes to launch_rms_bwd).
+cudaError_t plan_bwd(Dtype dt, bool rms, int rows, int cols, bool aligned, int path_override,
                      BwdPlan* plan);
+cudaError_t plan_rms_bwd(Dtype dt, int rows, int cols, bool aligned, int path_override,
+                         BwdPlan* plan);
 
 // Largest grid any backward plan can use for `rows` rows on a device with `sms` SMs.
 int bwd_max_grid(int rows, int sms);
@@ -113,6 +121,26 @@ inline bool bwd_plan_acc_region(const BwdPlan& p) {
 
 cudaError_t launch_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStream_t stream,
                        int* launches);
+cudaError_t launch_rms_bwd(Dtype dt, const BwdArgs& a, const BwdPlan& plan, cudaStream_t stream,
+                           int* launches);
+
+// The fused softmax: forward (a = x, optional additive mask [mask_rows, cols], out = y) or
+// backward (a = dy, b = y, out = dx).
+struct SoftmaxArgs {
+    const void* a;
+    const void* b;
+    const void* mask;
+    int mask_rows;
+    float scale;
+    int rows;
+    int cols;
+    void* out;
+    unsigned* status;
+    uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_softmax(Dtype dt, bool bwd, const SoftmaxArgs& a, bool aligned,
+                           int path_override, cudaStream_t stream, int* launches);
 
 // Zeroes the allocation-free entry point's fixed scratch on the current device, if a call
 // there has used it: on `stream`, which is then synchronised (after a backward gave up).
@@ -122,10 +150,12 @@ cudaError_t noalloc_scratch_clear(cudaStream_t stream);
 // workspace (the library's own per-stream one when `own_ws`, else `ws` of `ws_bytes` bytes,
 // zero between calls), the launch, and the LN_CHECK handling.  Instantiated for float and
 // __nv_bfloat16.
+// `rms`: the RMSNorm backward (mean and dbeta unused and may be null).
 template <typename T>
-ln_status bwd_impl(Dtype dt, const T* dy, const T* xr, const T* gamma, const float* mean,
-                   const float* rstd, T* dx, T* dgamma, T* dbeta, int64_t rows, int64_t cols,
-                   void* ws, size_t ws_bytes, bool own_ws, ln_stream_t stream);
+ln_status bwd_impl(Dtype dt, bool rms, const T* dy, const T* xr, const T* gamma,
+                   const float* mean, const float* rstd, T* dx, T* dgamma, T* dbeta,
+                   int64_t rows, int64_t cols, void* ws, size_t ws_bytes, bool own_ws,
+                   ln_stream_t stream);
 
 // Occupancy (resident blocks per SM) of a kernel, cached per (device, kernel, threads, smem).
 int blocks_per_sm(const void* kernel, int threads, size_t smem);

@@ -79,7 +79,7 @@ extern "C" ln_status ln_bwd_bf16_noalloc(const ln_bf16* dy, const ln_bf16* x_or_
     // The regular backward with the fixed array as a caller-owned workspace: the same plan,
     // kernels, checks and test hooks as ln_bwd_bf16.
     const ln_status st = lnk::bwd_impl<B>(
-        lnk::Dtype::BF16, reinterpret_cast<const B*>(dy), reinterpret_cast<const B*>(x_or_res_out),
+        lnk::Dtype::BF16, false, reinterpret_cast<const B*>(dy), reinterpret_cast<const B*>(x_or_res_out),
         reinterpret_cast<const B*>(gamma), mean, rstd, reinterpret_cast<B*>(dx),
         reinterpret_cast<B*>(dgamma), reinterpret_cast<B*>(dbeta), rows, cols, ws,
         LN_NOALLOC_SCRATCH_BYTES, false, stream);

@@ -1,0 +1,12 @@
+// rms_fwd.cu -- the fused residual-add + RMSNorm forward: the RMSNorm instantiations of the
+// kernels in ln_fwd_kernels.cuh.
+#include "ln_fwd_kernels.cuh"
+
+namespace lnk {
+
+cudaError_t launch_rms_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
+                           cudaStream_t stream, int* launches) {
+    return launch_norm_fwd<true>(dt, a, aligned, path_override, stream, launches);
+}
+
+}  // namespace lnk

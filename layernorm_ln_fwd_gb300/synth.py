@@ -102,3 +102,29 @@ def workload_inputs(name: str, seed: int = 0, device="cpu") -> dict:
     w = WORKLOADS[name]
     return make_inputs(w.rows, w.cols, w.dtype, seed=seed, x=w.x, res=w.res, dy=w.dy,
                        gamma=w.gamma, beta=w.beta, device=device)
+
+
+# Workloads of the other fused row operations (the pages' shapes):
+#  * fused add + RMSNorm ("GPU Performance from First Principles", section 6.1) at the two
+#    GPT-2 LayerNorm shapes above, same distributions (no beta);
+#  * fused softmax of attention scores, batch x heads x L rows of L columns with a causal
+#    mask and the 1/sqrt(64) scale: 8 x 16 x 512 x 512 ("Accelerating Transformer on GPU
+#    (II)", section 3.2) and 2 x 16 x 256 x 256 ("... (I)", section 4.1); scores ~ N(0, 3),
+#    dy ~ N(0, 1).
+OP_WORKLOADS = {
+    "rms_bf16_8192x768": dict(kind="rms", dtype="bf16", rows=8192, cols=768),
+    "rms_bf16_8192x1280": dict(kind="rms", dtype="bf16", rows=8192, cols=1280),
+    "softmax_bf16_65536x512_causal": dict(kind="softmax", dtype="bf16", rows=65536, cols=512,
+                                          mask_rows=512, scale=0.125),
+    "softmax_bf16_8192x256_causal": dict(kind="softmax", dtype="bf16", rows=8192, cols=256,
+                                         mask_rows=256, scale=0.125),
+}
+
+
+def causal_mask(L: int, cols: int, dtype: str, device="cpu") -> torch.Tensor:
+    """[L, cols] additive mask: query q keeps keys k <= q * cols / L (0), the rest -inf."""
+    q = torch.arange(L, device=device)[:, None]
+    k = torch.arange(cols, device=device)[None, :]
+    m = torch.zeros(L, cols, device=device)
+    m[k > q * cols // L] = float("-inf")
+    return m.to(torch_dtype(dtype))

@@ -91,6 +91,16 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.ln_bwd_workspace_bytes(4, 0) == 0
     assert lib.ln_bwd_workspace_bytes(-1, 4) == 0
     assert lib.ln_last_launch_count() == 0
+    # RMSNorm: beta and mean do not exist, gamma and rrms are required.
+    assert lib.ln_rms_fwd_f32(p, NULL, NULL, 1e-5, 4, 4, p, NULL, p, NULL) == 1
+    assert lib.ln_rms_fwd_bf16(p, NULL, p, 1e-5, 4, 4, p, NULL, NULL, NULL) == 1
+    assert lib.ln_rms_fwd_f32(p, NULL, p, -1.0, 4, 4, p, NULL, p, NULL) == 1
+    assert lib.ln_rms_fwd_bf16(p, NULL, p, 1e-5, 4, ln.MAX_COLS + 1, p, NULL, p, NULL) == 3
+    assert lib.ln_rms_bwd_f32(p, p, p, NULL, p, p, 4, 4, NULL) == 1
+    assert lib.ln_rms_bwd_bf16(p, p, p, p, p, NULL, 4, 4, NULL) == 1
+    assert lib.ln_rms_bwd_bf16_ws(p, p, p, p, p, p, 4, 4, ctypes.c_void_p(272), 1 << 20,
+                                  NULL) == 2
+    assert lib.ln_rms_fwd_f32(NULL, NULL, NULL, 1e-5, 0, 4, NULL, NULL, NULL, NULL) == 0
 
 
 def test_force_path_hook_round_trips(lib):
