@@ -5,8 +5,8 @@ legs of ``bench.py`` may import this package.  The CUDA library never calls it a
 code with it.
 
 It covers the fused residual-add + LayerNorm (``ln_fwd``, ``ln_bwd``), the fused
-residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``) and the fused softmax (``softmax_fwd``,
-``softmax_bwd``).  Two independent implementations of the
+residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``), the fused softmax (``softmax_fwd``,
+``softmax_bwd``) and the fused cross-entropy (``xent``).  Two independent implementations of the
 same definitions live here:
 
 * ``ln_oracle.c`` (float64 C, OpenMP over rows; built into ``libln_oracle.so`` by
@@ -88,6 +88,10 @@ def _load():
             lib.oracle_softmax_bwd.argtypes = [d, d, ctypes.c_double, i64, i64, ctypes.c_int, d,
                                                ctypes.c_int]
             lib.oracle_softmax_bwd.restype = None
+            lib.oracle_xent.argtypes = [d, ctypes.POINTER(ctypes.c_int32), i64, i64,
+                                        ctypes.c_double, ctypes.c_double, ctypes.c_int, d, d,
+                                        ctypes.c_int]
+            lib.oracle_xent.restype = None
             lib.oracle_round_io.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_round_io.restype = ctypes.c_double
             lib.oracle_max_threads.argtypes = []
@@ -252,3 +256,21 @@ def softmax_bwd(dy, y, scale: float = 1.0, io: str = "f64", threads: int = 0):
     _load().oracle_softmax_bwd(_ptr(dy), _ptr(y), float(scale), rows, cols, IO_CODES[io],
                                _ptr(dx), int(threads))
     return dx
+
+
+def xent(x, targets, alpha: float = 0.0, dloss: float = 1.0, io: str = "f64", threads: int = 0,
+         want_dx: bool = True):
+    """Fused cross-entropy with label smoothing ("Accelerating Transformer on GPU (I)",
+    section 5.2): per row, loss = log Z + m - [(1 - alpha) x_t + (alpha / V) sum x] and
+    dx = dloss * (softmax(x) - p), p = (1 - alpha) onehot(t) + alpha / V.  Returns
+    ``losses`` (float64) and ``dx`` (rounded to ``io``)."""
+    x = _f64(x)
+    rows, V = x.shape
+    t = np.ascontiguousarray(np.asarray(targets, dtype=np.int32))
+    assert t.shape == (rows,) and np.all((t >= 0) & (t < V))
+    losses = np.empty(rows)
+    dx = np.empty((rows, V)) if want_dx else None
+    _load().oracle_xent(_ptr(x), t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), rows, V,
+                        float(alpha), float(dloss), IO_CODES[io], _ptr(losses), _ptr(dx),
+                        int(threads))
+    return {"loss": losses, "dx": dx}

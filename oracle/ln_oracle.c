@@ -386,3 +386,38 @@ void oracle_softmax_bwd(const double* dy, const double* y, double scale, int64_t
         for (int64_t j = 0; j < cols; ++j) dx[r * cols + j] = round_io(scale * yr[j] * (d[j] - s), io);
     }
 }
+
+/*
+ * Fused cross-entropy with label smoothing, forward and backward in one pass
+ * ("Accelerating Transformer on GPU (I)", section 5.2; the fused classifier of "llm.c: the
+ * llmc/ CUDA kernel layer", section 6).  Per row of V logits x with target t:
+ *    p = (1 - alpha) onehot(t) + alpha / V,   q = softmax(x),
+ *    loss = -sum_i p_i log q_i = log Z + m - [(1 - alpha) x_t + (alpha / V) sum_i x_i]
+ * with m = max x and Z = sum exp(x - m), and the gradient of the loss, scaled by dloss,
+ *    dx = dloss * (q - p).
+ * targets must lie in [0, V).  Outputs: losses [rows] (unrounded float64; may be NULL),
+ * dx [rows, V] rounded to `io` (may be NULL).
+ */
+void oracle_xent(const double* x, const int32_t* targets, int64_t rows, int64_t V, double alpha,
+                 double dloss, int io, double* losses, double* dx, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * V;
+        const int64_t t = targets[r];
+        double m = -INFINITY, sx = 0.0;
+        for (int64_t j = 0; j < V; ++j) {
+            if (xr[j] > m) m = xr[j];
+            sx += xr[j];
+        }
+        double z = 0.0;
+        for (int64_t j = 0; j < V; ++j) z += exp(xr[j] - m);
+        if (losses) losses[r] = log(z) + m - ((1.0 - alpha) * xr[t] + alpha / (double)V * sx);
+        if (dx) {
+            for (int64_t j = 0; j < V; ++j) {
+                double p = alpha / (double)V + (j == t ? 1.0 - alpha : 0.0);
+                dx[r * V + j] = round_io(dloss * (exp(xr[j] - m) / z - p), io);
+            }
+        }
+    }
+}

@@ -9,7 +9,8 @@ independent code so that the two can be compared:
 * the fused residual-add + RMSNorm forward and backward ("GPU Performance from First
   Principles", section 6.1);
 * the fused softmax forward ("Accelerating Transformer on GPU (I)", section 4.1) and backward
-  ("... (II)", section 3.1).
+  ("... (II)", section 3.1);
+* the fused cross-entropy with label smoothing ("... (I)", section 5.2), as -sum p log q.
 """
 from __future__ import annotations
 
@@ -110,3 +111,16 @@ def softmax_bwd(dy, y, scale: float = 1.0, io: str = "f64"):
     dy = np.asarray(dy, dtype=np.float64)
     y = np.asarray(y, dtype=np.float64)
     return round_io(scale * y * (dy - (dy * y).sum(axis=1, keepdims=True)), io)
+
+
+def xent(x, targets, alpha: float = 0.0, dloss: float = 1.0, io: str = "f64"):
+    """Fused cross-entropy with label smoothing ("Accelerating Transformer on GPU (I)",
+    section 5.2), written as the page's sum: loss = -sum p log q, dx = dloss (q - p)."""
+    x = np.asarray(x, dtype=np.float64)
+    rows, V = x.shape
+    t = np.asarray(targets)
+    p = np.full((rows, V), alpha / V)
+    p[np.arange(rows), t] += 1.0 - alpha
+    z = x - x.max(axis=1, keepdims=True)
+    logq = z - np.log(np.exp(z).sum(axis=1, keepdims=True))
+    return {"loss": -(p * logq).sum(axis=1), "dx": round_io(dloss * (np.exp(logq) - p), io)}
