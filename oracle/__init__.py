@@ -6,7 +6,9 @@ code with it.
 
 It covers the fused residual-add + LayerNorm (``ln_fwd``, ``ln_bwd``), the fused
 residual-add + RMSNorm (``rms_fwd``, ``rms_bwd``), the fused softmax (``softmax_fwd``,
-``softmax_bwd``) and the fused cross-entropy (``xent``).  Two independent implementations of the
+``softmax_bwd``), the fused cross-entropy (``xent``) and the bias + dropout + residual
+prologue of the LayerNorm forward with its backward (``bdr_ln_fwd``, ``dropout_bwd``, on
+a Philox-4x32-10 counter-based generator, ``philox4x32``).  Two independent implementations of the
 same definitions live here:
 
 * ``ln_oracle.c`` (float64 C, OpenMP over rows; built into ``libln_oracle.so`` by
@@ -92,6 +94,20 @@ def _load():
                                         ctypes.c_double, ctypes.c_double, ctypes.c_int, d, d,
                                         ctypes.c_int]
             lib.oracle_xent.restype = None
+            u32p = ctypes.POINTER(ctypes.c_uint32)
+            u64 = ctypes.c_uint64
+            lib.oracle_philox4x32.argtypes = [u32p, u32p, u32p]
+            lib.oracle_philox4x32.restype = None
+            lib.oracle_dropout_mask.argtypes = [u64, u64, ctypes.c_double, i64, i64,
+                                                ctypes.POINTER(ctypes.c_uint8), ctypes.c_int]
+            lib.oracle_dropout_mask.restype = None
+            lib.oracle_bdr_ln_fwd.argtypes = [d, d, d, d, d, ctypes.c_double, ctypes.c_double,
+                                              u64, u64, i64, i64, ctypes.c_int, d, d, d, d,
+                                              ctypes.c_int]
+            lib.oracle_bdr_ln_fwd.restype = None
+            lib.oracle_dropout_bwd.argtypes = [d, ctypes.c_double, u64, u64, i64, i64,
+                                               ctypes.c_int, d, d, ctypes.c_int]
+            lib.oracle_dropout_bwd.restype = None
             lib.oracle_round_io.argtypes = [ctypes.c_double, ctypes.c_int]
             lib.oracle_round_io.restype = ctypes.c_double
             lib.oracle_max_threads.argtypes = []
@@ -274,3 +290,51 @@ def xent(x, targets, alpha: float = 0.0, dloss: float = 1.0, io: str = "f64", th
                         float(alpha), float(dloss), IO_CODES[io], _ptr(losses), _ptr(dx),
                         int(threads))
     return {"loss": losses, "dx": dx}
+
+
+def philox4x32(ctr, key):
+    """Philox-4x32-10 of one counter (4 words) under one key (2 words): 4 words."""
+    c = (ctypes.c_uint32 * 4)(*ctr)
+    k = (ctypes.c_uint32 * 2)(*key)
+    o = (ctypes.c_uint32 * 4)()
+    _load().oracle_philox4x32(c, k, o)
+    return list(o)
+
+
+def dropout_mask(seed: int, offset: int, p: float, rows: int, cols: int, threads: int = 0):
+    """uint8 [rows, cols]: 1 where the element is kept (see oracle_dropout_mask)."""
+    keep = np.empty((rows, cols), dtype=np.uint8)
+    _load().oracle_dropout_mask(seed, offset, float(p), rows, cols,
+                                keep.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)),
+                                int(threads))
+    return keep
+
+
+def bdr_ln_fwd(h, bias, res, gamma, beta, eps: float, p: float, seed: int, offset: int,
+               io: str = "f64", threads: int = 0):
+    """Bias + dropout + residual prologue ("Accelerating Transformer on GPU (I)", section
+    2.3) fused with the LayerNorm forward: s = res + keep * (h + bias) / (1 - p), rounded to
+    ``io``, then LN(s).  Returns ``out``, ``res_out``, ``mean``, ``rstd``."""
+    h = _f64(h)
+    rows, cols = h.shape
+    res = _f64(res)
+    out = np.empty((rows, cols))
+    res_out = np.empty((rows, cols))
+    mean = np.empty(rows)
+    rstd = np.empty(rows)
+    _load().oracle_bdr_ln_fwd(_ptr(h), _ptr(_f64(bias)), _ptr(res), _ptr(_f64(gamma)),
+                              _ptr(_f64(beta)), float(eps), float(p), seed, offset, rows, cols,
+                              IO_CODES[io], _ptr(out), _ptr(res_out), _ptr(mean), _ptr(rstd),
+                              int(threads))
+    return {"out": out, "res_out": res_out, "mean": mean, "rstd": rstd}
+
+
+def dropout_bwd(ds, p: float, seed: int, offset: int, io: str = "f64", threads: int = 0):
+    """Backward of the prologue: dh = ds * keep / (1 - p), dbias = sum over rows of dh."""
+    ds = _f64(ds)
+    rows, cols = ds.shape
+    dh = np.empty((rows, cols))
+    dbias = np.empty(cols)
+    _load().oracle_dropout_bwd(_ptr(ds), float(p), seed, offset, rows, cols, IO_CODES[io],
+                               _ptr(dh), _ptr(dbias), int(threads))
+    return {"dh": dh, "dbias": dbias}

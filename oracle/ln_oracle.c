@@ -421,3 +421,119 @@ void oracle_xent(const double* x, const int32_t* targets, int64_t rows, int64_t 
         }
     }
 }
+
+/*
+ * Counter-based random numbers for dropout: Philox-4x32 with 10 rounds (Salmon, Moraes,
+ * Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011).  One round maps
+ * the counter (c0, c1, c2, c3) under the key (k0, k1) to
+ *    (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ * with M0 = 0xD2511F53, M1 = 0xCD9E8D57 (64-bit products split into 32-bit halves); the key
+ * is advanced by the Weyl constants (0x9E3779B9, 0xBB67AE85) before every round after the
+ * first.  The generator is written here from that definition; the CUDA path has its own.
+ */
+void oracle_philox4x32(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/*
+ * The dropout decision of element i (= row * cols + col) under (seed, offset) with drop
+ * probability p: the word i % 4 of Philox-4x32-10 at counter (i / 4 split into low and high
+ * 32 bits, offset split likewise) and key (seed split likewise); the element is kept when that
+ * word is at least floor(p * 2^32), so it is dropped with probability p (to 2^-32).
+ * This is the reading taken for the RNG, which the pages do not specify.
+ */
+static uint32_t drop_threshold(double p) {
+    const double t = floor(p * 4294967296.0);
+    return t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+}
+
+static int dropout_keep(uint64_t seed, uint64_t offset, uint32_t thr, uint64_t i) {
+    const uint64_t blk = i >> 2;
+    const uint32_t ctr[4] = {(uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset,
+                             (uint32_t)(offset >> 32)};
+    const uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    oracle_philox4x32(ctr, key, out);
+    return out[i & 3] >= thr;
+}
+
+void oracle_dropout_mask(uint64_t seed, uint64_t offset, double p, int64_t rows, int64_t cols,
+                         uint8_t* keep, int nthreads) {
+    set_threads(nthreads);
+    const uint32_t thr = drop_threshold(p);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < cols; ++j)
+            keep[r * cols + j] = (uint8_t)dropout_keep(seed, offset, thr, (uint64_t)(r * cols + j));
+}
+
+/*
+ * Bias + dropout + residual, the prologue fused into the LayerNorm forward ("Accelerating
+ * Transformer on GPU (I)", section 2.3: after a linear layer, add the bias, apply dropout,
+ * add the residual).  With keep from oracle_dropout_mask:
+ *    s = res + keep * (h + bias) / (1 - p)     (rounded to `io`, written as res_out)
+ * followed by the LayerNorm of s exactly as oracle_ln_fwd.
+ */
+void oracle_bdr_ln_fwd(const double* h, const double* bias, const double* res,
+                       const double* gamma, const double* beta, double eps, double p,
+                       uint64_t seed, uint64_t offset, int64_t rows, int64_t cols, int io,
+                       double* out, double* res_out, double* mean, double* rstd, int nthreads) {
+    double* s = (double*)malloc((size_t)(rows * cols) * sizeof(double));
+    if (!s) return;
+    set_threads(nthreads);
+    const uint32_t thr = drop_threshold(p);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < cols; ++j) {
+            const int64_t i = r * cols + j;
+            const double v = dropout_keep(seed, offset, thr, (uint64_t)i) ? (h[i] + bias[j]) / (1.0 - p)
+                                                                          : 0.0;
+            s[i] = round_io(res[i] + v, io);
+        }
+    oracle_ln_fwd(s, NULL, gamma, beta, eps, rows, cols, io, out, res_out, mean, rstd, nthreads);
+    free(s);
+}
+
+/*
+ * Backward of the prologue: ds is the gradient with respect to s (the LayerNorm backward's
+ * dx); the residual's gradient is ds itself, and
+ *    dh = ds * keep / (1 - p),   dbias = sum over rows of dh
+ * (dh rounded to `io`; dbias summed unrounded in row order, then rounded).
+ */
+void oracle_dropout_bwd(const double* ds, double p, uint64_t seed, uint64_t offset, int64_t rows,
+                        int64_t cols, int io, double* dh, double* dbias, int nthreads) {
+    set_threads(nthreads);
+    const uint32_t thr = drop_threshold(p);
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < cols; ++j) {
+        double acc = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            const int64_t i = r * cols + j;
+            const double v = dropout_keep(seed, offset, thr, (uint64_t)i) ? ds[i] / (1.0 - p) : 0.0;
+            if (dh) dh[i] = round_io(v, io);
+            acc += v;
+        }
+        if (dbias) dbias[j] = round_io(acc, io);
+    }
+}

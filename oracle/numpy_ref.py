@@ -10,7 +10,8 @@ independent code so that the two can be compared:
   Principles", section 6.1);
 * the fused softmax forward ("Accelerating Transformer on GPU (I)", section 4.1) and backward
   ("... (II)", section 3.1);
-* the fused cross-entropy with label smoothing ("... (I)", section 5.2), as -sum p log q.
+* the fused cross-entropy with label smoothing ("... (I)", section 5.2), as -sum p log q;
+* the bias + dropout + residual prologue ("... (I)", section 2.3) on Philox-4x32-10.
 """
 from __future__ import annotations
 
@@ -124,3 +125,45 @@ def xent(x, targets, alpha: float = 0.0, dloss: float = 1.0, io: str = "f64"):
     z = x - x.max(axis=1, keepdims=True)
     logq = z - np.log(np.exp(z).sum(axis=1, keepdims=True))
     return {"loss": -(p * logq).sum(axis=1), "dx": round_io(dloss * (np.exp(logq) - p), io)}
+
+
+_M0, _M1, _W0, _W1 = 0xD2511F53, 0xCD9E8D57, 0x9E3779B9, 0xBB67AE85
+
+
+def philox4x32(c0, c1, c2, c3, k0, k1):
+    """Philox-4x32-10 on uint64 arrays holding 32-bit words (vectorised over counters)."""
+    m32 = np.uint64(0xFFFFFFFF)
+    c = [np.asarray(v, dtype=np.uint64) for v in (c0, c1, c2, c3)]
+    k = [np.uint64(k0), np.uint64(k1)]
+    for r in range(10):
+        if r:
+            k = [(k[0] + np.uint64(_W0)) & m32, (k[1] + np.uint64(_W1)) & m32]
+        p0 = np.uint64(_M0) * c[0]
+        p1 = np.uint64(_M1) * c[2]
+        c = [(p1 >> np.uint64(32)) ^ c[1] ^ k[0], p1 & m32, (p0 >> np.uint64(32)) ^ c[3] ^ k[1],
+             p0 & m32]
+    return c
+
+
+def dropout_mask(seed, offset, p, rows, cols):
+    i = np.arange(rows * cols, dtype=np.uint64)
+    blk = i >> np.uint64(2)
+    m32 = np.uint64(0xFFFFFFFF)
+    w = philox4x32(blk & m32, blk >> np.uint64(32), np.full_like(blk, offset & 0xFFFFFFFF),
+                   np.full_like(blk, offset >> 32), seed & 0xFFFFFFFF, seed >> 32)
+    word = np.choose((i & np.uint64(3)).astype(np.int64), w)
+    thr = min(int(np.floor(p * 2.0 ** 32)), 0xFFFFFFFF)
+    return (word >= np.uint64(thr)).astype(np.uint8).reshape(rows, cols)
+
+
+def bdr_ln_fwd(h, bias, res, gamma, beta, eps, p, seed, offset, io="f64"):
+    h = np.asarray(h, dtype=np.float64)
+    keep = dropout_mask(seed, offset, p, *h.shape)
+    s = round_io(np.asarray(res, np.float64) + keep * (h + np.asarray(bias)[None, :]) / (1 - p), io)
+    return ln_fwd(s, None, gamma, beta, eps, io)
+
+
+def dropout_bwd(ds, p, seed, offset, io="f64"):
+    ds = np.asarray(ds, dtype=np.float64)
+    dh = dropout_mask(seed, offset, p, *ds.shape) * ds / (1 - p)
+    return {"dh": round_io(dh, io), "dbias": round_io(dh.sum(axis=0), io)}
