@@ -400,13 +400,17 @@ class Workbench:
         for name, fn, nb in (("fwd", self.fwd, self.fwd_b),
                              ("bwd", lambda k: self.bwd(k + self.nsets // 2), self.bwd_b),
                              ("step", self.step, self.fwd_b + self.bwd_b)):
+            if nb == 0 or (name == "step" and self.bwd_b == 0):
+                continue  # a single fused kernel: no separate backward
             us, reps = self.time_graph(fn, n)
             gbs = nb / us / 1e3
             out[name] = {"us": us, "algorithmic_bytes": nb, "gbs": gbs,
                          "frac_of_measured": gbs / peak, "frac_of_8tbs": gbs / ROOFLINE_NOMINAL_GBS,
                          "repeats_us": [round(v, 3) for v in reps], "launches_per_repeat": n}
-        out["rows_per_s"] = self.R / (out["step"]["us"] * 1e-6)
-        out["dominant"] = "ln_fwd" if out["fwd"]["us"] >= out["bwd"]["us"] else "ln_bwd"
+        step_us = out["step"]["us"] if "step" in out else out["fwd"]["us"]
+        out["rows_per_s"] = self.R / (step_us * 1e-6)
+        out["dominant"] = ("fwd" if "bwd" not in out or out["fwd"]["us"] >= out["bwd"]["us"]
+                           else "bwd")
         out["buffer_sets"] = self.nsets
         return out
 
@@ -446,17 +450,37 @@ class OpBench(Workbench):
         if op["kind"] == "rms":
             self.set_bytes = 6 * R * C * s
             self.fwd_b, self.bwd_b = rms_fwd_bytes(R, C, s), rms_bwd_bytes(R, C, s)
-        else:
+        elif op["kind"] == "softmax":
             self.set_bytes = 4 * R * C * s
             self.fwd_b = softmax_fwd_bytes(R, C, op["mask_rows"], s)
             self.bwd_b = softmax_bwd_bytes(R, C, s)
+        elif op["kind"] == "xent":  # one fused kernel: read the logits, write the gradient
+            self.set_bytes = 2 * R * C * s
+            self.fwd_b, self.bwd_b = 2 * R * C * s + 8 * R, 0
+        else:  # bdr: the prologue-fused LayerNorm forward; the prologue's backward
+            self.set_bytes = 7 * R * C * s
+            self.fwd_b = fwd_bytes(R, C, s) + C * s
+            self.bwd_b = 2 * R * C * s + C * s
         nsets = max(2, -(-3 * l2 // self.set_bytes) + 1)
         self.nsets = nsets + nsets % 2
         self.sets = []
         for i in range(self.nsets):
+            spread = {"softmax": 3.0, "xent": 2.0}.get(op["kind"], 1.0)
             d = synth.make_inputs(R, C, op["dtype"], seed=1000 * rank + i, device="cuda",
-                                  x=("normal", 0.0, 3.0 if op["kind"] == "softmax" else 1.0))
-            if op["kind"] == "rms":
+                                  x=("normal", 0.0, spread))
+            if op["kind"] == "xent":
+                g = torch.Generator(device="cuda").manual_seed(1000 * rank + i)
+                d = {"x": d["x"], "t": torch.randint(0, C, (R,), generator=g, device="cuda",
+                                                     dtype=torch.int32),
+                     "loss": torch.empty(R, dtype=torch.float32, device="cuda"),
+                     "dx": torch.empty_like(d["x"])}
+            elif op["kind"] == "bdr":
+                d.update(bias=(0.1 * d["beta"].float()).to(td), out=torch.empty_like(d["x"]),
+                         res_out=torch.empty_like(d["x"]), dx=torch.empty_like(d["x"]),
+                         mean=torch.empty(R, dtype=torch.float32, device="cuda"),
+                         rstd=torch.empty(R, dtype=torch.float32, device="cuda"),
+                         dbias=torch.empty(C, dtype=td, device="cuda"))
+            elif op["kind"] == "rms":
                 d.update(out=torch.empty_like(d["x"]), res_out=torch.empty_like(d["x"]),
                          dx=torch.empty_like(d["x"]),
                          rrms=torch.empty(R, dtype=torch.float32, device="cuda"),
@@ -473,19 +497,31 @@ class OpBench(Workbench):
 
     def fwd(self, i):
         S = self.sets[i % self.nsets]
-        if self.op["kind"] == "rms":
+        kind = self.op["kind"]
+        if kind == "rms":
             self.ln.rms_fwd(S["x"], S["res"], S["gamma"], 1e-5, out=S["out"],
                             res_out=S["res_out"], rrms=S["rrms"], stream=self.stream)
-        else:
+        elif kind == "softmax":
             self.ln.softmax_fwd(S["x"], S["mask"], self.op["scale"], y=S["y"], stream=self.stream)
+        elif kind == "xent":
+            self.ln.xent(S["x"], S["t"], self.op["alpha"], 1.0 / self.R, losses=S["loss"],
+                         dlogits=S["dx"], stream=self.stream)
+        else:
+            self.ln.fwd_bias_dropout(S["x"], S["bias"], S["res"], S["gamma"], S["beta"], 1e-5,
+                                     self.op["p"], 17, i, out=S["out"], res_out=S["res_out"],
+                                     mean=S["mean"], rstd=S["rstd"], stream=self.stream)
 
     def bwd(self, i):
         S = self.sets[i % self.nsets]
-        if self.op["kind"] == "rms":
+        kind = self.op["kind"]
+        if kind == "rms":
             self.ln.rms_bwd(S["dy"], S["res_out"], S["gamma"], S["rrms"], dx=S["dx"],
                             dgamma=S["dgamma"], workspace=self.ws, stream=self.stream)
-        else:
+        elif kind == "softmax":
             self.ln.softmax_bwd(S["dy"], S["y"], self.op["scale"], dx=S["dx"], stream=self.stream)
+        elif kind == "bdr":
+            self.ln.dropout_bwd(S["dy"], self.op["p"], 17, i, dh=S["dx"], dbias=S["dbias"],
+                                workspace=self.ws, stream=self.stream)
 
 
 def run_ours(args):

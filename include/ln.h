@@ -1,7 +1,8 @@
 /*
  * ln.h -- C ABI of the GB300 (sm_103a) fused residual-add + LayerNorm library (libln.so),
- * with the fused residual-add + RMSNorm (ln_rms_*) and the fused row softmax (ln_softmax_*)
- * alongside.
+ * with the bias + dropout + residual prologue (ln_fwd_bias_dropout_*, ln_dropout_bwd_*), the
+ * fused residual-add + RMSNorm (ln_rms_*), the fused row softmax (ln_softmax_*) and the fused
+ * cross-entropy (ln_xent_*) alongside.
  *
  * The library computes, for a row-major [rows, cols] problem:
  *
@@ -263,6 +264,102 @@ ln_status ln_softmax_bwd_f32(const float* dy, const float* y, float scale, int64
 
 ln_status ln_softmax_bwd_bf16(const ln_bf16* dy, const ln_bf16* y, float scale, int64_t rows,
                               int64_t cols, ln_bf16* dx, ln_stream_t stream);
+
+/*
+ * Fused cross-entropy with label smoothing, forward and backward in one kernel
+ * ("Accelerating Transformer on GPU (I): Kernel Fusion and LightSeq Inference", section 5.2;
+ * the fused classifier of "llm.c: the llmc/ CUDA kernel layer", section 6).  For each row r
+ * of V logits x with target t = targets[r]:
+ *
+ *   p = (1 - alpha) onehot(t) + alpha / V,   q = softmax(x)
+ *   losses[r] = -sum_j p_j log q_j = log Z + m - [(1 - alpha) x_t + (alpha / V) sum_j x_j]
+ *   dlogits   = dloss * (q - p)
+ *
+ * with m = max x and Z = sum exp(x - m).
+ *
+ *   logits   [rows, V]  input
+ *   targets  [rows]     int32, each in [0, V) (a row with another target gets a NaN loss)
+ *   alpha               label smoothing, 0 <= alpha <= 1
+ *   dloss               factor of the gradient (1 / rows for a mean over rows)
+ *   losses   [rows]     fp32, written; may be NULL
+ *   dlogits  [rows, V]  written; may be NULL; may be the logits themselves (the gradient
+ *                       then overwrites them in place)
+ *
+ * At least one of losses and dlogits must be given.  Limits: 1 <= V <= LN_XENT_MAX_V,
+ * 0 <= rows <= LN_MAX_ROWS.  Other conventions and errors as for ln_fwd_*.
+ */
+#define LN_XENT_MAX_V (1 << 24)
+
+ln_status ln_xent_f32(const float* logits, const int32_t* targets, int64_t rows, int64_t V,
+                      float alpha, float dloss, float* losses, float* dlogits,
+                      ln_stream_t stream);
+
+ln_status ln_xent_bf16(const ln_bf16* logits, const int32_t* targets, int64_t rows, int64_t V,
+                       float alpha, float dloss, float* losses, ln_bf16* dlogits,
+                       ln_stream_t stream);
+
+/*
+ * LayerNorm forward with the bias + dropout + residual prologue fused in ("Accelerating
+ * Transformer on GPU (I): Kernel Fusion and LightSeq Inference", section 2.3: after a linear
+ * layer, add its bias, apply dropout, add the residual -- one kernel instead of three):
+ *
+ *   s = res + keep * (h + bias) / (1 - p)        (stored as res_out, rounded to the I/O type)
+ *   out, mean, rstd = the LayerNorm of s exactly as ln_fwd_*
+ *
+ * keep is 0 with probability p: element i = row * cols + col is kept when word i % 4 of the
+ * counter-based generator Philox-4x32-10 (Salmon, Moraes, Dror and Shaw, SC 2011) at counter
+ * (i / 4 as two 32-bit words, offset as two 32-bit words) under key (seed as two 32-bit
+ * words) is at least floor(p * 2^32).  The mask is a pure function of (seed, offset, i), so
+ * the backward regenerates it; nothing is stored.  Use a new offset (or seed) per call.
+ *
+ *   h        [rows, cols]  the linear layer's output
+ *   bias     [cols]        its bias
+ *   res      [rows, cols]  the residual (required)
+ *   p                      drop probability, 0 <= p < 1
+ *   the rest               as for ln_fwd_*
+ *
+ * Errors as for ln_fwd_*; LN_EINVAL also for a NULL bias or res or p outside [0, 1).
+ */
+ln_status ln_fwd_bias_dropout_f32(const float* h, const float* bias, const float* res,
+                                  const float* gamma, const float* beta, float eps, float p,
+                                  uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                  float* out, float* res_out, float* mean, float* rstd,
+                                  ln_stream_t stream);
+
+ln_status ln_fwd_bias_dropout_bf16(const ln_bf16* h, const ln_bf16* bias, const ln_bf16* res,
+                                   const ln_bf16* gamma, const ln_bf16* beta, float eps, float p,
+                                   uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                   ln_bf16* out, ln_bf16* res_out, float* mean, float* rstd,
+                                   ln_stream_t stream);
+
+/*
+ * Backward of the prologue.  ds is the gradient with respect to s -- the dx that ln_bwd_*
+ * returns for the forward's res_out, mean and rstd, which is also the residual's gradient:
+ *
+ *   dh    = ds * keep / (1 - p)          [rows, cols]  (written)
+ *   dbias = sum over rows of dh          [cols]        (written; bitwise reproducible, no
+ *                                                       float atomics)
+ *
+ * p, seed and offset must be the forward's.  The plain variants use the library-owned
+ * workspace of the stream, the _ws variants a caller-owned one of at least
+ * ln_bwd_workspace_bytes(rows, cols) bytes (shared with ln_bwd_* in stream order); every
+ * completed call leaves it all zero.  Errors as for ln_bwd_*.
+ */
+ln_status ln_dropout_bwd_f32(const float* ds, float p, uint64_t seed, uint64_t offset,
+                             int64_t rows, int64_t cols, float* dh, float* dbias,
+                             ln_stream_t stream);
+
+ln_status ln_dropout_bwd_bf16(const ln_bf16* ds, float p, uint64_t seed, uint64_t offset,
+                              int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                              ln_stream_t stream);
+
+ln_status ln_dropout_bwd_f32_ws(const float* ds, float p, uint64_t seed, uint64_t offset,
+                                int64_t rows, int64_t cols, float* dh, float* dbias,
+                                void* workspace, size_t workspace_bytes, ln_stream_t stream);
+
+ln_status ln_dropout_bwd_bf16_ws(const ln_bf16* ds, float p, uint64_t seed, uint64_t offset,
+                                 int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                 void* workspace, size_t workspace_bytes, ln_stream_t stream);
 
 /*
  * Backward (bf16) that allocates nothing.  The pages have no counterpart to this entry

@@ -34,6 +34,7 @@ _I64 = ctypes.c_int64
 _F = ctypes.c_float
 _INT = ctypes.c_int
 _SZ = ctypes.c_size_t
+_U64 = ctypes.c_uint64
 SIGNATURES = {
     "ln_fwd_f32": (_INT, [_P, _P, _P, _P, _F, _I64, _I64, _P, _P, _P, _P, _P]),
     "ln_fwd_bf16": (_INT, [_P, _P, _P, _P, _F, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -61,6 +62,16 @@ SIGNATURES = {
     "ln_softmax_fwd_bf16": (_INT, [_P, _P, _I64, _F, _I64, _I64, _P, _P]),
     "ln_softmax_bwd_f32": (_INT, [_P, _P, _F, _I64, _I64, _P, _P]),
     "ln_softmax_bwd_bf16": (_INT, [_P, _P, _F, _I64, _I64, _P, _P]),
+    "ln_xent_f32": (_INT, [_P, _P, _I64, _I64, _F, _F, _P, _P, _P]),
+    "ln_xent_bf16": (_INT, [_P, _P, _I64, _I64, _F, _F, _P, _P, _P]),
+    "ln_fwd_bias_dropout_f32": (_INT, [_P, _P, _P, _P, _P, _F, _F, _U64, _U64, _I64, _I64, _P, _P,
+                                       _P, _P, _P]),
+    "ln_fwd_bias_dropout_bf16": (_INT, [_P, _P, _P, _P, _P, _F, _F, _U64, _U64, _I64, _I64, _P,
+                                        _P, _P, _P, _P]),
+    "ln_dropout_bwd_f32": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P]),
+    "ln_dropout_bwd_bf16": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P]),
+    "ln_dropout_bwd_f32_ws": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "ln_dropout_bwd_bf16_ws": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -324,3 +335,87 @@ def softmax_bwd(dy, y, scale: float = 1.0, dx=None, stream=None):
     _check(name, getattr(lib(), name)(_ptr(dy), _ptr(y), float(scale), rows, cols, _ptr(dx),
                                       _stream(stream)))
     return dx
+
+
+def xent(logits, targets, alpha: float = 0.0, dloss: float = 1.0, losses=None, dlogits=None,
+         want_losses: bool = True, want_grad: bool = True, in_place: bool = False, stream=None):
+    """Fused cross-entropy with label smoothing.  logits: [rows, V]; targets: int32 [rows].
+    Returns (losses, dlogits): losses fp32 [rows] = -sum p log softmax(logits), dlogits =
+    dloss * (softmax(logits) - p), p = (1 - alpha) onehot + alpha / V.  ``in_place`` writes
+    the gradient over the logits."""
+    import torch
+    if logits.dim() != 2:
+        raise ValueError("logits must be 2-D [rows, V]")
+    rows, V = logits.shape
+    dt, dev = logits.dtype, logits.device
+    sfx = _suffix(dt)
+    _need(logits, "logits", (rows, V), dt, dev)
+    _need(targets, "targets", (rows,), torch.int32, dev)
+    if want_losses and losses is None:
+        losses = torch.empty(rows, dtype=torch.float32, device=dev)
+    elif losses is not None:
+        _need(losses, "losses", (rows,), torch.float32, dev)
+    if in_place:
+        dlogits = logits
+    elif want_grad and dlogits is None:
+        dlogits = torch.empty_like(logits)
+    elif dlogits is not None:
+        _need(dlogits, "dlogits", (rows, V), dt, dev)
+    name = f"ln_xent_{sfx}"
+    _check(name, getattr(lib(), name)(_ptr(logits), _ptr(targets), rows, V, float(alpha),
+                                      float(dloss), _ptr(losses), _ptr(dlogits), _stream(stream)))
+    return losses, dlogits
+
+
+def fwd_bias_dropout(h, bias, res, gamma, beta, eps: float = 1e-5, p: float = 0.1, seed: int = 0,
+                     offset: int = 0, out=None, res_out=None, mean=None, rstd=None, stream=None):
+    """LayerNorm forward with the bias + dropout + residual prologue: s = res + keep * (h +
+    bias) / (1 - p) (stored as res_out), then LN(s).  The dropout mask is a function of
+    (seed, offset, element index).  Returns (out, res_out, mean, rstd)."""
+    import torch
+    if h.dim() != 2:
+        raise ValueError("h must be 2-D [rows, cols]")
+    rows, cols = h.shape
+    dt, dev = h.dtype, h.device
+    sfx = _suffix(dt)
+    _need(h, "h", (rows, cols), dt, dev)
+    _need(res, "res", (rows, cols), dt, dev)
+    for name, t in (("bias", bias), ("gamma", gamma), ("beta", beta)):
+        _need(t, name, (cols,), dt, dev)
+    out = torch.empty_like(h) if out is None else _need(out, "out", (rows, cols), dt, dev)
+    res_out = torch.empty_like(h) if res_out is None else _need(res_out, "res_out", (rows, cols), dt, dev)
+    mean = (torch.empty(rows, dtype=torch.float32, device=dev) if mean is None
+            else _need(mean, "mean", (rows,), torch.float32, dev))
+    rstd = (torch.empty(rows, dtype=torch.float32, device=dev) if rstd is None
+            else _need(rstd, "rstd", (rows,), torch.float32, dev))
+    name = f"ln_fwd_bias_dropout_{sfx}"
+    _check(name, getattr(lib(), name)(_ptr(h), _ptr(bias), _ptr(res), _ptr(gamma), _ptr(beta),
+                                      float(eps), float(p), int(seed), int(offset), rows, cols,
+                                      _ptr(out), _ptr(res_out), _ptr(mean), _ptr(rstd),
+                                      _stream(stream)))
+    return out, res_out, mean, rstd
+
+
+def dropout_bwd(ds, p: float, seed: int, offset: int, dh=None, dbias=None, workspace=None,
+                stream=None):
+    """Backward of the prologue: dh = ds * keep / (1 - p), dbias = sum over rows of dh (ds:
+    the gradient with respect to s, i.e. :func:`bwd`'s dx).  Returns (dh, dbias)."""
+    import torch
+    if ds.dim() != 2:
+        raise ValueError("ds must be 2-D [rows, cols]")
+    rows, cols = ds.shape
+    dt, dev = ds.dtype, ds.device
+    sfx = _suffix(dt)
+    _need(ds, "ds", (rows, cols), dt, dev)
+    dh = torch.empty_like(ds) if dh is None else _need(dh, "dh", (rows, cols), dt, dev)
+    dbias = (torch.empty(cols, dtype=dt, device=dev) if dbias is None
+             else _need(dbias, "dbias", (cols,), dt, dev))
+    args = [_ptr(ds), float(p), int(seed), int(offset), rows, cols, _ptr(dh), _ptr(dbias)]
+    if workspace is None:
+        name = f"ln_dropout_bwd_{sfx}"
+        _check(name, getattr(lib(), name)(*args, _stream(stream)))
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+        name = f"ln_dropout_bwd_{sfx}_ws"
+        _check(name, getattr(lib(), name)(*args, _ptr(workspace), nbytes, _stream(stream)))
+    return dh, dbias

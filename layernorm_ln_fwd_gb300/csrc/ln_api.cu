@@ -170,10 +170,47 @@ ln_status finish_call(cudaError_t e, int launches, cudaStream_t stream) {
 }
 
 // `rms`: the RMSNorm forward (beta and mean unused, may be null; rstd receives 1 / rms).
+// The dropout threshold floor(p 2^32) (p in [0, 1)).
+uint32_t drop_threshold(float p) {
+    const double t = std::floor((double)p * 4294967296.0);
+    return t >= 4294967295.0 ? 4294967295u : (uint32_t)t;
+}
+
+// The workspace of a backward: the library's own one for `stream` (allocated, or grown, and
+// zeroed on first use) when `own_ws`, else the caller's `ws` if it holds `need` bytes.
+ln_status acquire_workspace(bool own_ws, void*& ws, size_t ws_bytes, size_t need,
+                            cudaStream_t stream) {
+    if (!own_ws) return ws_bytes < need ? LN_ENOSPACE : LN_OK;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_workspaces[std::make_pair(dev, stream)];
+    if (w.bytes < need) {
+        cudaError_t e = cudaSuccess;
+        if (w.ptr) {
+            e = cudaStreamSynchronize(stream);  // the old workspace may still be in use
+            if (e == cudaSuccess) e = cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        e = cudaMalloc(&w.ptr, need);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return cuda_fail(e);
+        }
+        w.bytes = need;
+        e = cudaMemsetAsync(w.ptr, 0, need, stream);  // zero between calls, from the start
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    ws = w.ptr;
+    return LN_OK;
+}
+
 template <typename T>
 ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma, const T* beta,
                    float eps, int64_t rows, int64_t cols, T* out, T* res_out, float* mean,
-                   float* rstd, ln_stream_t stream_) {
+                   float* rstd, ln_stream_t stream_, const T* bias = nullptr, float p = 0.f,
+                   uint64_t seed = 0, uint64_t offset = 0) {
     t_last_launches = 0;
     if (!std::isfinite(eps) || eps < 0.f) return LN_EINVAL;
     ln_status st = check_sizes(rows, cols);
@@ -183,9 +220,16 @@ ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma,
     st = check_device();
     if (st != LN_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    const void* ptrs[] = {x, res, gamma, beta, out, res_out};
-    const bool aligned = vector_ok(dt, (int)cols, ptrs, 6);
+    const void* ptrs[] = {x, res, gamma, beta, out, res_out, bias};
+    const bool aligned = vector_ok(dt, (int)cols, ptrs, 7);
     FwdArgs a;
+    if (bias) {
+        a.pro.bias = bias;
+        a.pro.thr = drop_threshold(p);
+        a.pro.scale = 1.0f / (1.0f - p);
+        a.pro.seed = seed;
+        a.pro.offset = offset;
+    }
     a.x = x;
     a.res = res;
     a.gamma = gamma;
@@ -200,8 +244,9 @@ ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma,
     a.status = status_word();
     a.wait_limit_ns = wait_limit_ns();
     int launches = 0;
-    cudaError_t e = rms ? launch_rms_fwd(dt, a, aligned, g_force_path.load(), stream, &launches)
-                        : launch_fwd(dt, a, aligned, g_force_path.load(), stream, &launches);
+    cudaError_t e = rms    ? launch_rms_fwd(dt, a, aligned, g_force_path.load(), stream, &launches)
+                    : bias ? launch_bdr_fwd(dt, a, aligned, g_force_path.load(), stream, &launches)
+                           : launch_fwd(dt, a, aligned, g_force_path.load(), stream, &launches);
     return finish_call(e, launches, stream);
 }
 
@@ -234,31 +279,8 @@ ln_status bwd_impl(Dtype dt, bool rms, const T* dy, const T* xr, const T* gamma,
     cudaError_t e = plan_bwd(dt, rms, (int)rows, (int)cols, aligned, g_force_path.load(), &plan);
     if (e != cudaSuccess) return cuda_fail(e);
     const size_t need = bwd_workspace_bytes(plan.grid, (int)cols, bwd_plan_acc_region(plan));
-    if (own_ws) {
-        const int dev = current_device();
-        std::lock_guard<std::mutex> lk(g_mu);
-        Workspace& w = g_workspaces[std::make_pair(dev, stream)];
-        if (w.bytes < need) {
-            if (w.ptr) {
-                e = cudaStreamSynchronize(stream);  // the old workspace may still be in use
-                if (e == cudaSuccess) e = cudaFree(w.ptr);
-                w.ptr = nullptr;
-                w.bytes = 0;
-                if (e != cudaSuccess) return cuda_fail(e);
-            }
-            e = cudaMalloc(&w.ptr, need);
-            if (e != cudaSuccess) {
-                w.ptr = nullptr;
-                return cuda_fail(e);
-            }
-            w.bytes = need;
-            e = cudaMemsetAsync(w.ptr, 0, need, stream);  // zero between calls, from the start
-            if (e != cudaSuccess) return cuda_fail(e);
-        }
-        ws = w.ptr;
-    } else if (ws_bytes < need) {
-        return LN_ENOSPACE;
-    }
+    st = acquire_workspace(own_ws, ws, ws_bytes, need, stream);
+    if (st != LN_OK) return st;
     BwdArgs a;
     a.dy = dy;
     a.xr = xr;
@@ -321,6 +343,79 @@ ln_status softmax_impl(Dtype dt, bool bwd, const T* a, const T* b, const T* mask
     int launches = 0;
     cudaError_t e = launch_softmax(dt, bwd, s, vector_ok(dt, (int)cols, ptrs, 4),
                                    g_force_path.load(), stream, &launches);
+    return finish_call(e, launches, stream);
+}
+}  // namespace
+}  // namespace lnk
+
+namespace lnk {
+namespace {
+template <typename T>
+ln_status xent_impl(Dtype dt, const T* logits, const int32_t* targets, int64_t rows, int64_t V,
+                    float alpha, float dloss, float* losses, T* dlogits, ln_stream_t stream_) {
+    t_last_launches = 0;
+    if (!std::isfinite(alpha) || alpha < 0.f || alpha > 1.f || !std::isfinite(dloss))
+        return LN_EINVAL;
+    if (rows < 0 || V <= 0) return LN_EINVAL;
+    if (rows > LN_MAX_ROWS || V > LN_XENT_MAX_V) return LN_EUNSUPPORTED;
+    if (rows == 0) return LN_OK;
+    if (!logits || !targets || (!losses && !dlogits)) return LN_EINVAL;
+    ln_status st = check_device();
+    if (st != LN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    const void* ptrs[] = {logits, dlogits};
+    XentArgs a;
+    a.logits = logits;
+    a.targets = targets;
+    a.rows = (int)rows;
+    a.V = (int)V;
+    a.alpha = alpha;
+    a.dloss = dloss;
+    a.losses = losses;
+    a.dlogits = dlogits;
+    int launches = 0;
+    cudaError_t e = launch_xent(dt, a, vector_ok(dt, (int)V, ptrs, 2), stream, &launches);
+    return finish_call(e, launches, stream);
+}
+}  // namespace
+}  // namespace lnk
+
+namespace lnk {
+namespace {
+template <typename T>
+ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64_t offset,
+                           int64_t rows, int64_t cols, T* dh, T* dbias, void* ws, size_t ws_bytes,
+                           bool own_ws, ln_stream_t stream_) {
+    t_last_launches = 0;
+    if (!std::isfinite(p) || p < 0.f || p >= 1.f) return LN_EINVAL;
+    ln_status st = check_sizes(rows, cols);
+    if (st != LN_OK) return st;
+    if (!dbias || (rows > 0 && (!ds || !dh))) return LN_EINVAL;
+    if (!own_ws && !ws) return LN_EINVAL;
+    if (!own_ws && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return LN_EALIGN;
+    st = check_device();
+    if (st != LN_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (rows == 0) return finish_call(cudaMemsetAsync(dbias, 0, (size_t)cols * sizeof(T), stream), 0, stream);
+    const int segs = dropout_bwd_segments((int)rows, (int)cols, device_info(-1).sms);
+    const size_t need = kWorkspaceHeader + (size_t)segs * (size_t)cols * 2 * sizeof(float);
+    st = acquire_workspace(own_ws, ws, ws_bytes, need, stream);
+    if (st != LN_OK) return st;
+    const void* ptrs[] = {ds, dh};
+    DropoutBwdArgs a;
+    a.ds = ds;
+    a.dh = dh;
+    a.dbias = dbias;
+    a.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kWorkspaceHeader);
+    a.rows = (int)rows;
+    a.cols = (int)cols;
+    a.segs = segs;
+    a.scale = 1.0f / (1.0f - p);
+    a.thr = drop_threshold(p);
+    a.seed = seed;
+    a.offset = offset;
+    int launches = 0;
+    cudaError_t e = launch_dropout_bwd(dt, a, vector_ok(dt, (int)cols, ptrs, 2), stream, &launches);
     return finish_call(e, launches, stream);
 }
 }  // namespace
@@ -481,6 +576,78 @@ ln_status ln_softmax_bwd_bf16(const ln_bf16* dy, const ln_bf16* y, float scale, 
     return lnk::softmax_impl<B>(Dtype::BF16, true, reinterpret_cast<const B*>(dy),
                                 reinterpret_cast<const B*>(y), nullptr, 1, scale, rows, cols,
                                 reinterpret_cast<B*>(dx), stream);
+}
+
+ln_status ln_xent_f32(const float* logits, const int32_t* targets, int64_t rows, int64_t V,
+                      float alpha, float dloss, float* losses, float* dlogits,
+                      ln_stream_t stream) {
+    return lnk::xent_impl<float>(Dtype::F32, logits, targets, rows, V, alpha, dloss, losses,
+                                 dlogits, stream);
+}
+
+ln_status ln_xent_bf16(const ln_bf16* logits, const int32_t* targets, int64_t rows, int64_t V,
+                       float alpha, float dloss, float* losses, ln_bf16* dlogits,
+                       ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::xent_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(logits), targets, rows, V,
+                             alpha, dloss, losses, reinterpret_cast<B*>(dlogits), stream);
+}
+
+ln_status ln_fwd_bias_dropout_f32(const float* h, const float* bias, const float* res,
+                                  const float* gamma, const float* beta, float eps, float p,
+                                  uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                  float* out, float* res_out, float* mean, float* rstd,
+                                  ln_stream_t stream) {
+    if (!bias || (rows > 0 && !res) || !std::isfinite(p) || p < 0.f || p >= 1.f) return LN_EINVAL;
+    return lnk::fwd_impl<float>(Dtype::F32, false, h, res, gamma, beta, eps, rows, cols, out,
+                                res_out, mean, rstd, stream, bias, p, seed, offset);
+}
+
+ln_status ln_fwd_bias_dropout_bf16(const ln_bf16* h, const ln_bf16* bias, const ln_bf16* res,
+                                   const ln_bf16* gamma, const ln_bf16* beta, float eps, float p,
+                                   uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                   ln_bf16* out, ln_bf16* res_out, float* mean, float* rstd,
+                                   ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    if (!bias || (rows > 0 && !res) || !std::isfinite(p) || p < 0.f || p >= 1.f) return LN_EINVAL;
+    return lnk::fwd_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(h),
+                            reinterpret_cast<const B*>(res), reinterpret_cast<const B*>(gamma),
+                            reinterpret_cast<const B*>(beta), eps, rows, cols,
+                            reinterpret_cast<B*>(out), reinterpret_cast<B*>(res_out), mean, rstd,
+                            stream, reinterpret_cast<const B*>(bias), p, seed, offset);
+}
+
+ln_status ln_dropout_bwd_f32(const float* ds, float p, uint64_t seed, uint64_t offset,
+                             int64_t rows, int64_t cols, float* dh, float* dbias,
+                             ln_stream_t stream) {
+    return lnk::dropout_bwd_impl<float>(Dtype::F32, ds, p, seed, offset, rows, cols, dh, dbias,
+                                        nullptr, 0, true, stream);
+}
+
+ln_status ln_dropout_bwd_bf16(const ln_bf16* ds, float p, uint64_t seed, uint64_t offset,
+                              int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                              ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::dropout_bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(ds), p, seed, offset,
+                                    rows, cols, reinterpret_cast<B*>(dh),
+                                    reinterpret_cast<B*>(dbias), nullptr, 0, true, stream);
+}
+
+ln_status ln_dropout_bwd_f32_ws(const float* ds, float p, uint64_t seed, uint64_t offset,
+                                int64_t rows, int64_t cols, float* dh, float* dbias,
+                                void* workspace, size_t workspace_bytes, ln_stream_t stream) {
+    return lnk::dropout_bwd_impl<float>(Dtype::F32, ds, p, seed, offset, rows, cols, dh, dbias,
+                                        workspace, workspace_bytes, false, stream);
+}
+
+ln_status ln_dropout_bwd_bf16_ws(const ln_bf16* ds, float p, uint64_t seed, uint64_t offset,
+                                 int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                 void* workspace, size_t workspace_bytes, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    return lnk::dropout_bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(ds), p, seed, offset,
+                                    rows, cols, reinterpret_cast<B*>(dh),
+                                    reinterpret_cast<B*>(dbias), workspace, workspace_bytes, false,
+                                    stream);
 }
 
 ln_status ln_device_check(ln_stream_t stream_) {

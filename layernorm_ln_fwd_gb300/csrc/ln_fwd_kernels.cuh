@@ -62,6 +62,32 @@ __device__ __forceinline__ float warp_sum1(float a) {
     return a;
 }
 
+// The prologue of one 16-byte vector: s = res + keep * (x + bias) * scale for the V elements
+// starting at element index i0 (a multiple of 4), rounded to the I/O type.  Dropped elements
+// take res itself.
+template <typename T>
+__device__ __forceinline__ uint4 prologue_vec(const uint4& xv, const uint4& rv, const uint4& bv,
+                                              const DropoutRng& rng, float scale,
+                                              unsigned long long i0) {
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    f2 hv[H], r2[H], bias[H], o[H];
+    PR::unpack(xv, hv);
+    PR::unpack(rv, r2);
+    PR::unpack(bv, bias);
+    unsigned keep = rng.keep4(i0 >> 2);
+    if constexpr (H == 4) keep |= rng.keep4((i0 >> 2) + 1) << 4;
+    const f2 sc = f2_splat(scale);
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const f2 t = f2_mul(f2_add(hv[h], bias[h]), sc);
+        const f2 kt = f2_make(((keep >> (2 * h)) & 1u) ? f2_lo(t) : 0.f,
+                              ((keep >> (2 * h + 1)) & 1u) ? f2_hi(t) : 0.f);
+        o[h] = f2_add(r2[h], kt);
+    }
+    return PR::pack(o);
+}
+
 // ---------------------------------------------------------------------------------------
 // Warp per row, fed by a bulk-copy (TMA) pipeline.
 //
@@ -74,13 +100,13 @@ __device__ __forceinline__ float warp_sum1(float a) {
 // completes when its copies land; the empty barrier when all consumer warps are done.
 // The bytes in flight per SM are set by the ring, not by the registers of resident warps.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPL, bool HAS_RES, bool RMS>
-__global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
+template <typename T, int VPL, bool HAS_RES, bool RMS, bool PRO = false>
+__global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
     fwd_tile_kernel(const T* __restrict__ x, const T* __restrict__ res,
                     const T* __restrict__ gamma, const T* __restrict__ beta, float eps, int rows,
                     int cols, T* __restrict__ out, T* __restrict__ res_out,
                     float* __restrict__ mean, float* __restrict__ rstd, int stages,
-                    unsigned* status, uint64_t wait_limit_ns) {
+                    unsigned* status, uint64_t wait_limit_ns, Prologue pro) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -141,6 +167,9 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
         if constexpr (!RMS)
             PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
+    // The prologue's bias (read through L1 where it is used) and generator.
+    const T* bptr = static_cast<const T*>(pro.bias);
+    const DropoutRng rng{pro.seed, pro.offset, pro.thr};
     const bool write_res = res_out != nullptr;
     RingPos pos;
     for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
@@ -156,16 +185,25 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
             const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
                                                      (size_t)warp * row_bytes);
             const T* rsm = xs + (size_t)kTileRows * cols;
-            // s = x + res, rounded to the stored type (one packed add per pair for bf16);
-            // it is what gets normalised.
+            // s = x + res, rounded to the stored type (one packed add per pair for bf16), or
+            // the prologue's res + keep * (x + bias) * scale; it is what gets normalised.
+            auto s_vec = [&](int v) {
+                const int vi = v * 32 + lane;
+                const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
+                if constexpr (PRO)
+                    return prologue_vec<T>(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V),
+                                           ld_keep(bptr + (size_t)vi * V), rng, pro.scale,
+                                           base + (size_t)vi * V);
+                else
+                    return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
+                                   : xv;
+            };
             uint4 sp[VPL];
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 const int vi = v * 32 + lane;
                 if (vi < nvec) {
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
-                    sp[v] = HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
-                                    : xv;
+                    sp[v] = s_vec(v);
                     if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
                 } else {
                     sp[v] = make_uint4(0, 0, 0, 0);
@@ -230,11 +268,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
                     // K is far from the mean (warp-uniform: every lane has the same sums): a
                     // second reduction about K + mean(d), on s re-read from shared memory.
                     K += md;
-                    shifted_sums([&](int v) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)(v * 32 + lane) * V);
-                        return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)(v * 32 + lane) * V))
-                                       : xv;
-                    }, K);
+                    shifted_sums(s_vec, K);
                 }
                 const float rs = rsqrtf(fmaxf(var, 0.f) + eps);
                 if (lane == 0) {
@@ -269,13 +303,13 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= 4 ? 2 : 1)
 // (end-of-row barrier) it refills that slot with the row `stages` iterations ahead.
 // Thread t of the block owns vectors t, t + blockDim.x, ... of every row.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPT, bool HAS_RES, bool RMS>
+template <typename T, int VPT, bool HAS_RES, bool RMS, bool PRO = false>
 __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     fwd_block_kernel(const T* __restrict__ x, const T* __restrict__ res,
                      const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
                      int rows, int cols, T* __restrict__ out, T* __restrict__ res_out,
                      float* __restrict__ mean, float* __restrict__ rstd, int stages,
-                     unsigned* status, uint64_t wait_limit_ns) {
+                     unsigned* status, uint64_t wait_limit_ns, Prologue pro) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -322,6 +356,9 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         if constexpr (!RMS)
             PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
     }
+    // The prologue's bias (read through L1 where it is used) and generator.
+    const T* bptr = static_cast<const T*>(pro.bias);
+    const DropoutRng rng{pro.seed, pro.offset, pro.thr};
 
     // The block's sum of (a, b): one warp butterfly, one exchange through shared memory
     // (exchange `e` of the row), then every thread adds the warps' sums in the same order, so
@@ -352,15 +389,24 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
+        auto s_vec = [&](int v) {
+            const int vi = v * nthreads + tid;
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
+            if constexpr (PRO)
+                return prologue_vec<T>(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V),
+                                       ld_keep(bptr + (size_t)vi * V), rng, pro.scale,
+                                       base + (size_t)vi * V);
+            else
+                return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
+                               : xv;
+        };
 
         uint4 sp[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
-                const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
-                sp[v] = HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
-                                : xv;
+                sp[v] = s_vec(v);
                 if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
             } else {
                 sp[v] = make_uint4(0, 0, 0, 0);
@@ -396,9 +442,13 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
             // Shifted sums: K = the row's first stored value (every thread reads it from
             // shared memory).  The low halves of the pairs sum the even columns, the high
             // halves the odd ones.
-            const uint4 first = HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
-                                                       *reinterpret_cast<const uint4*>(rsm))
-                                        : *reinterpret_cast<const uint4*>(xs);
+            // (With the prologue every thread recomputes s of the first vector.)
+            const uint4 first = PRO ? prologue_vec<T>(*reinterpret_cast<const uint4*>(xs),
+                                                      *reinterpret_cast<const uint4*>(rsm),
+                                                      ld_keep(bptr), rng, pro.scale, base)
+                                : HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
+                                                          *reinterpret_cast<const uint4*>(rsm))
+                                          : *reinterpret_cast<const uint4*>(xs);
             float K = first_value<T>(first);
             f2 d[VPT][H];
             float md = 0.f, var = 0.f;
@@ -429,12 +479,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
                 // K is far from the mean (block-uniform: every thread has the same sums): a
                 // second exchange about K + mean(d), on s re-read from shared memory.
                 K += md;
-                if (!shifted_sums([&](int v) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)(v * nthreads + tid) * V);
-                        return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)(v * nthreads + tid) * V))
-                                       : xv;
-                    }, K, 1))
-                    break;
+                if (!shifted_sums(s_vec, K, 1)) break;
             }
             const float rs = rsqrtf(fmaxf(var, 0.f) + eps);
             if (tid == 0) {
@@ -481,12 +526,12 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
 // pairwise (Welford/Chan), with the plain sum of s alongside for the stored mean.  RMSNorm:
 // per-thread sums of squares.
 // ---------------------------------------------------------------------------------------
-template <typename T, bool HAS_RES, bool RMS>
+template <typename T, bool HAS_RES, bool RMS, bool PRO = false>
 __global__ void __launch_bounds__(kFwdScalarThreads)
     fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ res,
                       const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
                       int rows, int cols, T* __restrict__ out, T* __restrict__ res_out,
-                      float* __restrict__ mean, float* __restrict__ rstd) {
+                      float* __restrict__ mean, float* __restrict__ rstd, Prologue pro) {
     using IO = Io<T>;
     pdl_enter();
     constexpr int NW = kFwdScalarThreads / 32;
@@ -504,8 +549,13 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
     const bool equal = cols % kFwdScalarThreads == 0;
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * cols;
+        const DropoutRng rng{pro.seed, pro.offset, pro.thr};
         auto load_s = [&](int j) -> float {
             float v = IO::to_f(x[base + j]);
+            if constexpr (PRO) {
+                const float t = (v + IO::to_f(static_cast<const T*>(pro.bias)[j])) * pro.scale;
+                return IO::round(IO::to_f(res[base + j]) + (rng.keep(base + j) ? t : 0.f));
+            }
             if (HAS_RES) v = IO::round(v + IO::to_f(res[base + j]));
             return v;
         };
@@ -527,7 +577,10 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
             for (int j = tid; j < cols; j += kFwdScalarThreads)
                 out[base + j] = IO::from_f(IO::to_f(gamma[j]) * (load_s(j) * r));
         } else {
-            const float K = row_shift<T, HAS_RES>(x + base, HAS_RES ? res + base : nullptr, cols);
+            const float K = PRO ? median5(load_s(sample_col(0, cols)), load_s(sample_col(1, cols)),
+                                          load_s(sample_col(2, cols)), load_s(sample_col(3, cols)),
+                                          load_s(sample_col(4, cols)))
+                                : row_shift<T, HAS_RES>(x + base, HAS_RES ? res + base : nullptr, cols);
             // This thread's summary of its values: their plain sum S, and Welford's running
             // mean and M2 of d = s - K.
             float S = 0.f, md = 0.f, M2 = 0.f, n = 0.f;
@@ -580,14 +633,32 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
 // ---------------------------------------------------------------------------------------
 // Host-side dispatch.
 // ---------------------------------------------------------------------------------------
-template <bool RMS, typename T>
+// The kernel of a family for a residual (or not); the prologue always has a residual, and
+// its instantiations exist only in that form.
+template <typename T, int N, bool RMS, bool PRO>
+const void* tile_ptr(bool has_res) {
+    if constexpr (PRO)
+        return (const void*)fwd_tile_kernel<T, N, true, RMS, true>;
+    else
+        return has_res ? (const void*)fwd_tile_kernel<T, N, true, RMS, false>
+                       : (const void*)fwd_tile_kernel<T, N, false, RMS, false>;
+}
+template <typename T, int N, bool RMS, bool PRO>
+const void* block_ptr(bool has_res) {
+    if constexpr (PRO)
+        return (const void*)fwd_block_kernel<T, N, true, RMS, true>;
+    else
+        return has_res ? (const void*)fwd_block_kernel<T, N, true, RMS, false>
+                       : (const void*)fwd_block_kernel<T, N, false, RMS, false>;
+}
+
+template <bool RMS, bool PRO, typename T>
 cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     const void* kern = nullptr;
     const bool has_res = a.res != nullptr;
 #define LNK_FWD_TILE_CASE(N)                                                               \
     case N:                                                                                \
-        kern = has_res ? (const void*)fwd_tile_kernel<T, N, true, RMS>                          \
-                       : (const void*)fwd_tile_kernel<T, N, false, RMS>;                        \
+        kern = tile_ptr<T, N, RMS, PRO>(has_res);                                          \
         break;
     switch (vpl) {
         LNK_FWD_TILE_CASE(1)
@@ -627,12 +698,13 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     float* rstd = a.rstd;
     unsigned* status = a.status;
     uint64_t limit = a.wait_limit_ns;
+    Prologue pro = a.pro;
     void* args[] = {&x,   &res,     &gamma, &beta, &eps,    &rows,   &cols,
-                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
+                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit, &pro};
     return launch_kernel(kern, dim3(grid), dim3(kTileThreads), smem, stream, args, false);
 }
 
-template <bool RMS, typename T>
+template <bool RMS, bool PRO, typename T>
 cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
     const int nvec = a.cols / V;
@@ -646,8 +718,7 @@ cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     const void* kern = nullptr;
 #define LNK_FWD_BLOCK_CASE(N)                                                              \
     case N:                                                                                \
-        kern = has_res ? (const void*)fwd_block_kernel<T, N, true, RMS>                         \
-                       : (const void*)fwd_block_kernel<T, N, false, RMS>;                       \
+        kern = block_ptr<T, N, RMS, PRO>(has_res);                                         \
         break;
     // cols <= 16384: at most 4 vectors per thread for bf16, 8 for fp32.
     if constexpr (V == 8) {
@@ -704,16 +775,21 @@ cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     float* rstd = a.rstd;
     unsigned* status = a.status;
     uint64_t limit = a.wait_limit_ns;
+    Prologue pro = a.pro;
     void* args[] = {&x,   &res,     &gamma, &beta, &eps,   &rows,   &cols,
-                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit};
+                    &out, &res_out, &mean,  &rstd, &stages, &status, &limit, &pro};
     return launch_kernel(kern, dim3(grid), dim3(threads), smem, stream, args, false);
 }
 
-template <bool RMS, typename T>
+template <bool RMS, bool PRO, typename T>
 cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     const bool has_res = a.res != nullptr;
-    const void* kern = has_res ? (const void*)fwd_scalar_kernel<T, true, RMS>
-                               : (const void*)fwd_scalar_kernel<T, false, RMS>;
+    const void* kern;
+    if constexpr (PRO)
+        kern = (const void*)fwd_scalar_kernel<T, true, RMS, true>;
+    else
+        kern = has_res ? (const void*)fwd_scalar_kernel<T, true, RMS, false>
+                       : (const void*)fwd_scalar_kernel<T, false, RMS, false>;
     const DeviceInfo& di = device_info(-1);
     const int occ = std::max(1, blocks_per_sm(kern, kFwdScalarThreads, 0));
     const int grid = std::max(1, std::min(a.rows, di.sms * occ));
@@ -727,30 +803,31 @@ cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     int rows = a.rows, cols = a.cols;
     float* mean = a.mean;
     float* rstd = a.rstd;
-    void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd};
+    Prologue pro = a.pro;
+    void* args[] = {&x, &res, &gamma, &beta, &eps, &rows, &cols, &out, &res_out, &mean, &rstd, &pro};
     return launch_kernel(kern, dim3(grid), dim3(kFwdScalarThreads), 0, stream, args, false);
 }
 
-template <bool RMS, typename T>
+template <bool RMS, bool PRO, typename T>
 cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
-    if (!aligned || path == kPathScalar) return launch_scalar<RMS, T>(a, stream);
+    if (!aligned || path == kPathScalar) return launch_scalar<RMS, PRO, T>(a, stream);
     const int nvec = a.cols / V;
     const int vpl = (nvec + 31) / 32;
-    if (path == kPathBlock) return launch_block<RMS, T>(a, stream);
-    if (vpl <= 8) return launch_warp<RMS, T>(a, vpl, stream);
-    return launch_block<RMS, T>(a, stream);
+    if (path == kPathBlock) return launch_block<RMS, PRO, T>(a, stream);
+    if (vpl <= 8) return launch_warp<RMS, PRO, T>(a, vpl, stream);
+    return launch_block<RMS, PRO, T>(a, stream);
 }
 
 // The forward of a LayerNorm (RMS = false) or an RMSNorm (RMS = true): one kernel launch.
-template <bool RMS>
+template <bool RMS, bool PRO = false>
 cudaError_t launch_norm_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
                             cudaStream_t stream, int* launches) {
     *launches = 0;
     if (a.rows == 0) return cudaSuccess;
     cudaError_t e = dt == Dtype::F32
-                        ? launch_fwd_t<RMS, float>(a, aligned, path_override, stream)
-                        : launch_fwd_t<RMS, __nv_bfloat16>(a, aligned, path_override, stream);
+                        ? launch_fwd_t<RMS, PRO, float>(a, aligned, path_override, stream)
+                        : launch_fwd_t<RMS, PRO, __nv_bfloat16>(a, aligned, path_override, stream);
     if (e == cudaSuccess) *launches = 1;
     return e;
 }

@@ -28,6 +28,16 @@ const DeviceInfo& device_info(int dev);
 // Per-device status word (a __device__ variable); its device address on the current device.
 unsigned* status_word();
 
+// The bias + dropout + residual prologue of the LayerNorm forward: s = res + keep * (x +
+// bias) * scale, keep from Philox-4x32-10 at (seed, offset) with threshold thr (see
+// DropoutRng), scale = 1 / (1 - p).  bias == nullptr: no prologue.
+struct Prologue {
+    const void* bias = nullptr;
+    uint32_t thr = 0;
+    float scale = 1.f;
+    unsigned long long seed = 0, offset = 0;
+};
+
 struct FwdArgs {
     const void* x;
     const void* res;    // may be null
@@ -42,6 +52,7 @@ struct FwdArgs {
     float* rstd;
     unsigned* status;
     uint64_t wait_limit_ns;
+    Prologue pro;
 };
 
 struct BwdArgs {
@@ -87,6 +98,9 @@ cudaError_t launch_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_overri
                        cudaStream_t stream, int* launches);
 // The RMSNorm forward: `beta` and `mean` are unused (may be null); `rstd` receives 1 / rms.
 cudaError_t launch_rms_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
+                           cudaStream_t stream, int* launches);
+// The LayerNorm forward with the bias + dropout + residual prologue (a.pro.bias set).
+cudaError_t launch_bdr_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
                            cudaStream_t stream, int* launches);
 
 // Plans (kernel, grid, shared memory) the backward of a LayerNorm, or of an RMSNorm when
@@ -141,6 +155,39 @@ struct SoftmaxArgs {
 
 cudaError_t launch_softmax(Dtype dt, bool bwd, const SoftmaxArgs& a, bool aligned,
                            int path_override, cudaStream_t stream, int* launches);
+
+// The fused cross-entropy with label smoothing: losses (optional) and dlogits (optional;
+// may alias logits).
+struct XentArgs {
+    const void* logits;
+    const int* targets;
+    int rows;
+    int V;
+    float alpha;
+    float dloss;
+    float* losses;
+    void* dlogits;
+};
+
+cudaError_t launch_xent(Dtype dt, const XentArgs& a, bool aligned, cudaStream_t stream,
+                        int* launches);
+
+// Backward of the bias + dropout + residual prologue: dh = ds * keep * scale and the
+// deterministic column sums dbias (partials: [segs][cols] (hi, lo) fp32 pairs, left zero).
+struct DropoutBwdArgs {
+    const void* ds;
+    void* dh;
+    void* dbias;
+    float* partials;
+    int rows, cols, segs;
+    float scale;
+    uint32_t thr;
+    unsigned long long seed, offset;
+};
+
+int dropout_bwd_segments(int rows, int cols, int sms);
+cudaError_t launch_dropout_bwd(Dtype dt, const DropoutBwdArgs& a, bool aligned,
+                               cudaStream_t stream, int* launches);
 
 // Zeroes the allocation-free entry point's fixed scratch on the current device, if a call
 // there has used it: on `stream`, which is then synchronised (after a backward gave up).

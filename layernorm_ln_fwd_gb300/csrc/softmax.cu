@@ -7,7 +7,9 @@
 // values and the sum s of exp(z - m), and the (m, s) pairs are merged in ONE reduction -- the
 // "online" merge m = max(ma, mb), s = sa exp(ma - m) + sb exp(mb - m) -- instead of the
 // page's two dependent reductions (max, then sum).  Each exponential is taken once:
-// y = exp(z - m_lane) * (exp(m_lane - M) / S).
+// y = exp(z - m_lane) * (exp(m_lane - M) / S).  The kernels work in base 2 -- z' = z log2(e)
+// = (scale log2 e) x + mask log2 e, and exp(z - m) = exp2(z' - m') -- so that every
+// exponential is one exp2f.
 // Backward ("Accelerating Transformer on GPU (II)", section 3.1: only y is needed, one row
 // reduction): dx = scale * y * (dy - sum dy y).
 //
@@ -31,6 +33,7 @@ constexpr int kSmTileThreads = (kSmTileRows + 1) * 32;
 constexpr int kSmMaxStages = 4;
 constexpr int kSmBlockThreads = 512;
 constexpr int kSmScalarThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct SmParams {
     const void* a;       // x (forward) or dy (backward)
@@ -53,7 +56,7 @@ __device__ __forceinline__ void online_merge(float& m, float& s, float mb, float
     if (mm == -INFINITY) {
         s = 0.f;
     } else {
-        s = __fadd_rn(__fmul_rn(s, expf(m - mm)), __fmul_rn(sb, expf(mb - mm)));
+        s = __fadd_rn(__fmul_rn(s, exp2f(m - mm)), __fmul_rn(sb, exp2f(mb - mm)));
     }
     m = mm;
 }
@@ -94,7 +97,8 @@ struct SmRow {
             Pairs<T>::unpack(ms(v), mv);
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-                z[v][h] = f2_fma(f2_splat(scale), xv[h], mv[h]);
+                // z' = (scale log2 e) x + mask log2 e: the score in base 2.
+                z[v][h] = f2_fma(f2_splat(scale * kLog2e), xv[h], f2_mul(mv[h], f2_splat(kLog2e)));
                 m = fmaxf(m, fmaxf(f2_lo(z[v][h]), f2_hi(z[v][h])));
             }
         }
@@ -106,8 +110,8 @@ struct SmRow {
             if (!valid(v)) continue;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-                e[v][2 * h] = expf(f2_lo(z[v][h]) - sh);
-                e[v][2 * h + 1] = expf(f2_hi(z[v][h]) - sh);
+                e[v][2 * h] = exp2f(f2_lo(z[v][h]) - sh);
+                e[v][2 * h + 1] = exp2f(f2_hi(z[v][h]) - sh);
                 acc0 += e[v][2 * h];
                 acc1 += e[v][2 * h + 1];
             }
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kSmTileThreads, VPL <= 4 ? 2 : 1) sm_tile_kern
                 float mw = r.m, sw = r.s;
                 warp_online(mw, sw);  // the one reduction of the row
                 const float c = mw == -INFINITY ? __int_as_float(0x7fc00000)
-                                            : (r.m == -INFINITY ? 0.f : expf(r.m - mw) / sw);
+                                            : (r.m == -INFINITY ? 0.f : exp2f(r.m - mw) / sw);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v)
                     if (valid(v)) st_stream(out + base + (size_t)(v * 32 + lane) * V, r.y(v, c));
@@ -311,7 +315,7 @@ __global__ void __launch_bounds__(kSmBlockThreads, 1) sm_block_kernel(const SmPa
             float mb = red[0][0], sb = red[1][0];
             for (int w = 1; w < nw; ++w) online_merge(mb, sb, red[0][w], red[1][w]);
             const float c = mb == -INFINITY ? __int_as_float(0x7fc00000)
-                                            : (r.m == -INFINITY ? 0.f : expf(r.m - mb) / sb);
+                                            : (r.m == -INFINITY ? 0.f : exp2f(r.m - mb) / sb);
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
                 if (valid(v)) st_stream(at_out(base, v), r.y(v, c));
@@ -355,8 +359,9 @@ __global__ void __launch_bounds__(kSmScalarThreads) sm_scalar_kernel(const SmPar
             }
         } else {
             const T* mrow = M ? M + (size_t)(row % p.mask_rows) * cols : nullptr;
-            auto z = [&](int j) {
-                return __fmaf_rn(p.scale, IO::to_f(A[base + j]), mrow ? IO::to_f(mrow[j]) : 0.f);
+            auto z = [&](int j) {  // in base 2
+                return __fmaf_rn(p.scale * kLog2e, IO::to_f(A[base + j]),
+                                 mrow ? IO::to_f(mrow[j]) * kLog2e : 0.f);
             };
             float m = -INFINITY, s = 0.f;
             for (int j = tid; j < cols; j += kSmScalarThreads) online_merge(m, s, z(j), 1.f);
@@ -372,7 +377,7 @@ __global__ void __launch_bounds__(kSmScalarThreads) sm_scalar_kernel(const SmPar
             const float inv = 1.0f / s;
             for (int j = tid; j < cols; j += kSmScalarThreads)
                 out[base + j] = IO::from_f(m == -INFINITY ? __int_as_float(0x7fc00000)
-                                                          : expf(z(j) - m) * inv);
+                                                          : exp2f(z(j) - m) * inv);
         }
         __syncthreads();
     }

@@ -118,6 +118,13 @@ OP_WORKLOADS = {
                                           mask_rows=512, scale=0.125),
     "softmax_bf16_8192x256_causal": dict(kind="softmax", dtype="bf16", rows=8192, cols=256,
                                          mask_rows=256, scale=0.125),
+    # fused cross-entropy of GPT-2 small's classifier: 8 x 1024 tokens over llm.c's padded
+    # vocabulary of 50304 ("llm.c: the llmc/ CUDA kernel layer", section 6), logits ~ N(0, 2),
+    # label smoothing 0.1 ("Accelerating Transformer on GPU (I)", section 5.2), mean loss.
+    "xent_bf16_8192x50304": dict(kind="xent", dtype="bf16", rows=8192, cols=50304, alpha=0.1),
+    # bias + dropout + residual prologue of the LayerNorm forward at the GPT-2 small shape,
+    # p = 0.1 ("Accelerating Transformer on GPU (I)", section 2.3).
+    "bdr_bf16_8192x768": dict(kind="bdr", dtype="bf16", rows=8192, cols=768, p=0.1),
 }
 
 
