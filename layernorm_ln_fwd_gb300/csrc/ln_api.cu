@@ -225,10 +225,8 @@ ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma,
     FwdArgs a;
     if (bias) {
         a.pro.bias = bias;
-        a.pro.thr = drop_threshold(p);
         a.pro.scale = 1.0f / (1.0f - p);
-        a.pro.seed = seed;
-        a.pro.offset = offset;
+        a.pro.rng = DropoutRng::make(seed, offset, drop_threshold(p));
     }
     a.x = x;
     a.res = res;
@@ -397,11 +395,13 @@ ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64
     if (st != LN_OK) return st;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (rows == 0) return finish_call(cudaMemsetAsync(dbias, 0, (size_t)cols * sizeof(T), stream), 0, stream);
-    const int segs = dropout_bwd_segments((int)rows, (int)cols, device_info(-1).sms);
+    const void* ptrs[] = {ds, dh};
+    const bool vec = dropout_bwd_vector(dt, (int)cols, vector_ok(dt, (int)cols, ptrs, 2));
+    const int segs = dropout_bwd_segments((int)rows, (int)cols, device_info(-1).sms,
+                                          vec ? (dt == Dtype::F32 ? 4 : 8) : 1);
     const size_t need = kWorkspaceHeader + (size_t)segs * (size_t)cols * 2 * sizeof(float);
     st = acquire_workspace(own_ws, ws, ws_bytes, need, stream);
     if (st != LN_OK) return st;
-    const void* ptrs[] = {ds, dh};
     DropoutBwdArgs a;
     a.ds = ds;
     a.dh = dh;
@@ -415,7 +415,7 @@ ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64
     a.seed = seed;
     a.offset = offset;
     int launches = 0;
-    cudaError_t e = launch_dropout_bwd(dt, a, vector_ok(dt, (int)cols, ptrs, 2), stream, &launches);
+    cudaError_t e = launch_dropout_bwd(dt, a, vec, stream, &launches);
     return finish_call(e, launches, stream);
 }
 }  // namespace

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "dropout_rng.h"
+
 namespace lnk {
 
 constexpr unsigned kFullMask = 0xffffffffu;
@@ -325,44 +327,6 @@ __device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) 
     const float bb = __fsub_rn(s, a);
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
-
-// ---------------------------------------------------------------------------------------
-// Dropout masks from the counter-based generator Philox-4x32 with 10 rounds (Salmon,
-// Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC 2011), written
-// from the paper's definition.  Element i of a [rows, cols] tensor takes word i % 4 of the
-// generator at counter (i / 4, offset) under key `seed`, and is kept when that word is at
-// least `thr` = floor(p 2^32): dropped with probability p, and the same mask whenever the
-// same (seed, offset) is given again (the backward regenerates it instead of storing it).
-// ---------------------------------------------------------------------------------------
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
-    }
-    return c;
-}
-
-struct DropoutRng {
-    unsigned long long seed, offset;
-    uint32_t thr;
-    // The four keep decisions of elements 4 * blk .. 4 * blk + 3, as bits 0..3.
-    __device__ __forceinline__ unsigned keep4(unsigned long long blk) const {
-        const uint4 w = philox4x32_10(
-            make_uint4((uint32_t)blk, (uint32_t)(blk >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
-            (uint32_t)seed, (uint32_t)(seed >> 32));
-        return (w.x >= thr ? 1u : 0u) | (w.y >= thr ? 2u : 0u) | (w.z >= thr ? 4u : 0u) |
-               (w.w >= thr ? 8u : 0u);
-    }
-    __device__ __forceinline__ bool keep(unsigned long long i) const {
-        return (keep4(i >> 2) >> (i & 3)) & 1u;
-    }
-};
 
 // ---------------------------------------------------------------------------------------
 // Status word and time.

@@ -75,14 +75,20 @@ __device__ __forceinline__ uint4 prologue_vec(const uint4& xv, const uint4& rv, 
     PR::unpack(xv, hv);
     PR::unpack(rv, r2);
     PR::unpack(bv, bias);
-    unsigned keep = rng.keep4(i0 >> 2);
-    if constexpr (H == 4) keep |= rng.keep4((i0 >> 2) + 1) << 4;
+    // The generator's words for the vector's 2 H elements (i0 % (2 H) == 0).
+    uint32_t w[2 * H];
+    const uint4 wa = rng.words(i0 >> 2);
+    w[0] = wa.x; w[1] = wa.y; w[2] = wa.z; w[3] = wa.w;
+    if constexpr (H == 4) {
+        const uint4 wb = rng.words((i0 >> 2) + 1);
+        w[4] = wb.x; w[5] = wb.y; w[6] = wb.z; w[7] = wb.w;
+    }
     const f2 sc = f2_splat(scale);
 #pragma unroll
     for (int h = 0; h < H; ++h) {
         const f2 t = f2_mul(f2_add(hv[h], bias[h]), sc);
-        const f2 kt = f2_make(((keep >> (2 * h)) & 1u) ? f2_lo(t) : 0.f,
-                              ((keep >> (2 * h + 1)) & 1u) ? f2_hi(t) : 0.f);
+        const f2 kt = f2_make(w[2 * h] >= rng.thr ? f2_lo(t) : 0.f,
+                              w[2 * h + 1] >= rng.thr ? f2_hi(t) : 0.f);
         o[h] = f2_add(r2[h], kt);
     }
     return PR::pack(o);
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
     }
     // The prologue's bias (read through L1 where it is used) and generator.
     const T* bptr = static_cast<const T*>(pro.bias);
-    const DropoutRng rng{pro.seed, pro.offset, pro.thr};
+    const DropoutRng& rng = pro.rng;
     const bool write_res = res_out != nullptr;
     RingPos pos;
     for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
@@ -358,7 +364,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     }
     // The prologue's bias (read through L1 where it is used) and generator.
     const T* bptr = static_cast<const T*>(pro.bias);
-    const DropoutRng rng{pro.seed, pro.offset, pro.thr};
+    const DropoutRng& rng = pro.rng;
 
     // The block's sum of (a, b): one warp butterfly, one exchange through shared memory
     // (exchange `e` of the row), then every thread adds the warps' sums in the same order, so
@@ -549,7 +555,7 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
     const bool equal = cols % kFwdScalarThreads == 0;
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * cols;
-        const DropoutRng rng{pro.seed, pro.offset, pro.thr};
+        const DropoutRng& rng = pro.rng;
         auto load_s = [&](int j) -> float {
             float v = IO::to_f(x[base + j]);
             if constexpr (PRO) {

@@ -5,6 +5,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "dropout_rng.h"
 #include "ln.h"
 
 namespace lnk {
@@ -29,13 +30,12 @@ const DeviceInfo& device_info(int dev);
 unsigned* status_word();
 
 // The bias + dropout + residual prologue of the LayerNorm forward: s = res + keep * (x +
-// bias) * scale, keep from Philox-4x32-10 at (seed, offset) with threshold thr (see
-// DropoutRng), scale = 1 / (1 - p).  bias == nullptr: no prologue.
+// bias) * scale, keep from Philox-4x32-10 at (seed, offset) with threshold floor(p 2^32)
+// (DropoutRng::make), scale = 1 / (1 - p).  bias == nullptr: no prologue.
 struct Prologue {
     const void* bias = nullptr;
-    uint32_t thr = 0;
     float scale = 1.f;
-    unsigned long long seed = 0, offset = 0;
+    DropoutRng rng{};
 };
 
 struct FwdArgs {
@@ -185,9 +185,13 @@ struct DropoutBwdArgs {
     unsigned long long seed, offset;
 };
 
-int dropout_bwd_segments(int rows, int cols, int sms);
-cudaError_t launch_dropout_bwd(Dtype dt, const DropoutBwdArgs& a, bool aligned,
-                               cudaStream_t stream, int* launches);
+// Whether the kernels take 16-byte vectors (rows of whole vectors, aligned pointers).
+bool dropout_bwd_vector(Dtype dt, int cols, bool aligned);
+// Row segments (partial rows) for cv columns per thread (16-byte vectors or 1); at most
+// min(rows, 8 * sms).
+int dropout_bwd_segments(int rows, int cols, int sms, int cv);
+cudaError_t launch_dropout_bwd(Dtype dt, const DropoutBwdArgs& a, bool vec, cudaStream_t stream,
+                               int* launches);
 
 // Zeroes the allocation-free entry point's fixed scratch on the current device, if a call
 // there has used it: on `stream`, which is then synchronised (after a backward gave up).

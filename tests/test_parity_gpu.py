@@ -222,6 +222,7 @@ def test_integer_dy_gives_exact_dbeta(dtype, rows, cols):
 # The full-size workloads compared on every row (the oracle finishes them in seconds); the
 # 262144-row fp32 workload on a sample of rows (dgamma and dbeta always over all rows).
 SAMPLED_WORKLOADS = {"f32_262144x1000"}
+MAX_COLUMNS_OVER_STATED = 5
 
 
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
@@ -230,7 +231,8 @@ def test_workload_full_size(name):
     output element by element (all rows; a 256-row sample of the largest), dgamma/dbeta over
     all rows, and bitwise-repeatable results.  Every output meets the bare stated tolerance
     (no element needs the column-sum allowance), except dgamma/dbeta of the 262144-row
-    fp32 workload, whose sums over 262144 rows the allowance covers."""
+    fp32 workload, whose sums over 262144 rows the allowance covers for at most
+    MAX_COLUMNS_OVER_STATED columns."""
     w = synth.WORKLOADS[name]
     inp = synth.workload_inputs(name, seed=0)
     gpu = P.run_gpu(inp, w.eps)
@@ -251,6 +253,9 @@ def test_workload_full_size(name):
     over = {i["name"]: i["n_over_stated"] for i in infos if i["n_over_stated"]}
     allowed = {"dgamma", "dbeta"} if name in SAMPLED_WORKLOADS else set()
     assert set(over) <= allowed, over
+    # Where the allowance is used at all, only a few columns lean on it (2 of the 1000 dgamma
+    # columns at 262144 rows when this was written): more means the sums got worse.
+    assert all(n <= MAX_COLUMNS_OVER_STATED for n in over.values()), over
     # Run to run: the backward gives the same bits (dgamma, dbeta and dx).
     d = P.to_device(inp)
     stable = True
