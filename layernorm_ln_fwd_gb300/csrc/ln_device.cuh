@@ -186,6 +186,16 @@ struct Pairs<__nv_bfloat16> {
     }
 };
 
+// 2^t by the special-function unit's approximate exponent (PTX ex2.approx.ftz.f32: one
+// instruction, a few units in the last place; results below 2^-126 flush to zero).  Used
+// for softmax weights, where t <= 0 and a flushed term is below 2^-126 of the row's
+// largest; the full-range library exp2f costs several instructions more per element.
+__device__ __forceinline__ float ex2_fast(float t) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+    return r;
+}
+
 // ---------------------------------------------------------------------------------------
 // Global memory access with cache hints.  The row outputs are written once per kernel with
 // the evict-first ("cs") policy so they do not push gamma/beta or the backward's partial sums

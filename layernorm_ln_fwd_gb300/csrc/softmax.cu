@@ -9,7 +9,7 @@
 // page's two dependent reductions (max, then sum).  Each exponential is taken once:
 // y = exp(z - m_lane) * (exp(m_lane - M) / S).  The kernels work in base 2 -- z' = z log2(e)
 // = (scale log2 e) x + mask log2 e, and exp(z - m) = exp2(z' - m') -- so that every
-// exponential is one exp2f.
+// exponential is one approximate base-2 exponent of the special-function unit (ex2_fast).
 // Backward ("Accelerating Transformer on GPU (II)", section 3.1: only y is needed, one row
 // reduction): dx = scale * y * (dy - sum dy y).
 //
@@ -56,7 +56,7 @@ __device__ __forceinline__ void online_merge(float& m, float& s, float mb, float
     if (mm == -INFINITY) {
         s = 0.f;
     } else {
-        s = __fadd_rn(__fmul_rn(s, exp2f(m - mm)), __fmul_rn(sb, exp2f(mb - mm)));
+        s = __fadd_rn(__fmul_rn(s, ex2_fast(m - mm)), __fmul_rn(sb, ex2_fast(mb - mm)));
     }
     m = mm;
 }
@@ -110,8 +110,8 @@ struct SmRow {
             if (!valid(v)) continue;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
-                e[v][2 * h] = exp2f(f2_lo(z[v][h]) - sh);
-                e[v][2 * h + 1] = exp2f(f2_hi(z[v][h]) - sh);
+                e[v][2 * h] = ex2_fast(f2_lo(z[v][h]) - sh);
+                e[v][2 * h + 1] = ex2_fast(f2_hi(z[v][h]) - sh);
                 acc0 += e[v][2 * h];
                 acc1 += e[v][2 * h + 1];
             }
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kSmTileThreads, VPL <= 4 ? 2 : 1) sm_tile_kern
                 float mw = r.m, sw = r.s;
                 warp_online(mw, sw);  // the one reduction of the row
                 const float c = mw == -INFINITY ? __int_as_float(0x7fc00000)
-                                            : (r.m == -INFINITY ? 0.f : exp2f(r.m - mw) / sw);
+                                            : (r.m == -INFINITY ? 0.f : ex2_fast(r.m - mw) / sw);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v)
                     if (valid(v)) st_stream(out + base + (size_t)(v * 32 + lane) * V, r.y(v, c));
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kSmBlockThreads, 1) sm_block_kernel(const SmPa
             float mb = red[0][0], sb = red[1][0];
             for (int w = 1; w < nw; ++w) online_merge(mb, sb, red[0][w], red[1][w]);
             const float c = mb == -INFINITY ? __int_as_float(0x7fc00000)
-                                            : (r.m == -INFINITY ? 0.f : exp2f(r.m - mb) / sb);
+                                            : (r.m == -INFINITY ? 0.f : ex2_fast(r.m - mb) / sb);
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
                 if (valid(v)) st_stream(at_out(base, v), r.y(v, c));
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kSmScalarThreads) sm_scalar_kernel(const SmPar
             const float inv = 1.0f / s;
             for (int j = tid; j < cols; j += kSmScalarThreads)
                 out[base + j] = IO::from_f(m == -INFINITY ? __int_as_float(0x7fc00000)
-                                                          : exp2f(z(j) - m) * inv);
+                                                          : ex2_fast(z(j) - m) * inv);
         }
         __syncthreads();
     }

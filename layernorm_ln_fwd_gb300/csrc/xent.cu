@@ -9,7 +9,8 @@
 // and x_t in one block reduction; pass 2 reads the row again (from L2: the rows in flight
 // are a small part of it) and writes dx, which may overwrite the logits in place (every
 // element is read in pass 2 by the thread that writes it, after the whole block has finished
-// pass 1).  Exponentials are exp2f of (x - m) * log2(e).
+// pass 1).  exp(x - m) is one fma and one approximate base-2 exponent (ex2_fast):
+// 2^(x log2 e - m log2 e).
 #include <algorithm>
 #include <math.h>
 
@@ -20,7 +21,8 @@ namespace lnk {
 namespace {
 
 constexpr int kXeThreads = 512;
-constexpr int kXeUnroll = 4;  // 128-bit loads in flight per thread in pass 1
+constexpr int kXeBlocksPerSm = 3;  // resident blocks: at most 40 registers a thread
+constexpr int kXeUnroll = 4;  // 128-bit loads in flight per thread in each pass
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct XeParams {
@@ -34,19 +36,24 @@ struct XeParams {
     void* dx;
 };
 
-__device__ __forceinline__ float ex(float t) { return exp2f(t * kLog2e); }
+// exp(x - m) = 2^(x log2 e + nm) with nm = -m log2 e: one fma and one ex2.
+__device__ __forceinline__ float ex_shift(float x, float nm) { return ex2_fast(fmaf(x, kLog2e, nm)); }
 
 // (m, s) += (mb, sb): s sums exp(value - m); a pair with m = -inf holds nothing.
 __device__ __forceinline__ void xe_merge(float& m, float& s, float mb, float sb) {
     const float mm = fmaxf(m, mb);
-    s = mm == -INFINITY ? 0.f : __fadd_rn(__fmul_rn(s, ex(m - mm)), __fmul_rn(sb, ex(mb - mm)));
+    s = mm == -INFINITY ? 0.f
+                        : __fadd_rn(__fmul_rn(s, ex2_fast((m - mm) * kLog2e)),
+                                    __fmul_rn(sb, ex2_fast((mb - mm) * kLog2e)));
     m = mm;
 }
 
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kXeThreads) xent_kernel(const XeParams p) {
+__global__ void __launch_bounds__(kXeThreads, kXeBlocksPerSm) xent_kernel(const XeParams p) {
     using IO = Io<T>;
+    using PR = Pairs<T>;
     constexpr int V8 = IO::kVec;
+    constexpr int H = PR::kPairs;
     constexpr int NW = kXeThreads / 32;
     __shared__ float red[3][NW];
     __shared__ float xt_sh;
@@ -56,23 +63,15 @@ __global__ void __launch_bounds__(kXeThreads) xent_kernel(const XeParams p) {
     const T* X = static_cast<const T*>(p.x);
     T* DX = static_cast<T*>(p.dx);
     const float inv_v = 1.0f / (float)V;
+    const f2 l2e2 = f2_splat(kLog2e);
     for (int row = blockIdx.x; row < p.rows; row += gridDim.x) {
         const size_t base = (size_t)row * V;
         const int t = p.targets[row];
         if (tid == 0) xt_sh = (t >= 0 && t < V) ? IO::to_f(X[base + t]) : __int_as_float(0x7fc00000);
-        // Pass 1: this thread's online (max, sum) pair and plain sum.
-        float m = -INFINITY, s = 0.f, sx = 0.f;
-        auto take = [&](const float* f, int n) {
-            float mv = f[0];
-            for (int i = 1; i < n; ++i) mv = fmaxf(mv, f[i]);
-            if (mv > m) {
-                s = m == -INFINITY ? 0.f : s * ex(m - mv);
-                m = mv;
-            }
-            if (m != -INFINITY)
-                for (int i = 0; i < n; ++i) s += ex(f[i] - m);
-            for (int i = 0; i < n; ++i) sx += f[i];
-        };
+        // Pass 1: this thread's online (max, sum) pair and plain sum, the sums as even/odd
+        // column pairs.
+        float m = -INFINITY;
+        f2 s2 = f2_splat(0.f), sx2 = f2_splat(0.f);
         if constexpr (VEC) {
             const int nvec = V / V8;
             const uint4* xv = reinterpret_cast<const uint4*>(X + base);
@@ -85,19 +84,44 @@ __global__ void __launch_bounds__(kXeThreads) xent_kernel(const XeParams p) {
                 }
 #pragma unroll
                 for (int k = 0; k < kXeUnroll; ++k) {
-                    if (v0 + k * kXeThreads < nvec) {
-                        float f[V8];
-                        IO::unpack(u[k], f);
-                        take(f, V8);
+                    if (v0 + k * kXeThreads >= nvec) continue;
+                    f2 x2[H];
+                    PR::unpack(u[k], x2);
+                    float mv = fmaxf(f2_lo(x2[0]), f2_hi(x2[0]));
+#pragma unroll
+                    for (int h = 1; h < H; ++h) mv = fmaxf(mv, fmaxf(f2_lo(x2[h]), f2_hi(x2[h])));
+                    if (mv > m) {  // a new running maximum: rescale the sum
+                        s2 = m == -INFINITY ? f2_splat(0.f)
+                                            : f2_mul(s2, f2_splat(ex2_fast((m - mv) * kLog2e)));
+                        m = mv;
                     }
+                    if (m != -INFINITY) {
+                        const f2 nm2 = f2_splat(-m * kLog2e);
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            const f2 z = f2_fma(x2[h], l2e2, nm2);
+                            s2 = f2_add(s2, f2_make(ex2_fast(f2_lo(z)), ex2_fast(f2_hi(z))));
+                        }
+                    }
+#pragma unroll
+                    for (int h = 0; h < H; ++h) sx2 = f2_add(sx2, x2[h]);
                 }
             }
         } else {
+            float s = 0.f, sx = 0.f;
             for (int j = tid; j < V; j += kXeThreads) {
                 const float f = IO::to_f(X[base + j]);
-                take(&f, 1);
+                if (f > m) {
+                    s = m == -INFINITY ? 0.f : s * ex2_fast((m - f) * kLog2e);
+                    m = f;
+                }
+                if (m != -INFINITY) s += ex_shift(f, -m * kLog2e);
+                sx += f;
             }
+            s2 = f2_make(s, 0.f);
+            sx2 = f2_make(sx, 0.f);
         }
+        float s = f2_lo(s2) + f2_hi(s2), sx = f2_lo(sx2) + f2_hi(sx2);
         // One block reduction of (max, sum) and the plain sum.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -121,28 +145,49 @@ __global__ void __launch_bounds__(kXeThreads) xent_kernel(const XeParams p) {
         }
         if (tid == 0 && p.losses)
             p.losses[row] = logf(s) + m - ((1.f - p.alpha) * xt_sh + p.alpha * inv_v * sx);
-        // Pass 2: dx = dloss * (exp(x - m) / s - alpha / V - (1 - alpha) [j == t]).
+        // Pass 2: dx = dloss * (exp(x - m) / s - alpha / V) and, at the target, minus
+        // dloss * (1 - alpha).
         if (DX) {
             const float c = p.dloss / s;
             const float base_p = p.dloss * p.alpha * inv_v;
             const float hit = p.dloss * (1.f - p.alpha);
+            const float nm = -m * kLog2e;
             if constexpr (VEC) {
                 const int nvec = V / V8;
+                const int tv = (t >= 0 && t < V) ? t / V8 : -1;  // the target's vector
                 const uint4* xv = reinterpret_cast<const uint4*>(X + base);
                 uint4* dv = reinterpret_cast<uint4*>(DX + base);
-                for (int v = tid; v < nvec; v += kXeThreads) {
-                    float f[V8];
-                    IO::unpack(__ldcs(xv + v), f);
+                const f2 nm2 = f2_splat(nm), c2 = f2_splat(c), nb2 = f2_splat(-base_p);
+                for (int v0 = tid; v0 < nvec; v0 += kXeUnroll * kXeThreads) {
+                    uint4 u[kXeUnroll];
 #pragma unroll
-                    for (int i = 0; i < V8; ++i) {
-                        f[i] = ex(f[i] - m) * c - base_p;
-                        if (v * V8 + i == t) f[i] -= hit;
+                    for (int k = 0; k < kXeUnroll; ++k) {
+                        const int v = v0 + k * kXeThreads;
+                        u[k] = v < nvec ? __ldcs(xv + v) : make_uint4(0, 0, 0, 0);
                     }
-                    __stcs(dv + v, IO::pack(f));
+#pragma unroll
+                    for (int k = 0; k < kXeUnroll; ++k) {
+                        const int v = v0 + k * kXeThreads;
+                        if (v >= nvec) continue;
+                        f2 x2[H], o[H];
+                        PR::unpack(u[k], x2);
+#pragma unroll
+                        for (int h = 0; h < H; ++h) {
+                            const f2 z = f2_fma(x2[h], l2e2, nm2);
+                            o[h] = f2_fma(f2_make(ex2_fast(f2_lo(z)), ex2_fast(f2_hi(z))), c2, nb2);
+                        }
+                        if (v == tv) {
+                            const int ti = t - v * V8;
+#pragma unroll
+                            for (int h = 0; h < H; ++h)
+                                o[h] = f2_sub(o[h], f2_make(2 * h == ti ? hit : 0.f, 2 * h + 1 == ti ? hit : 0.f));
+                        }
+                        __stcs(dv + v, PR::pack(o));
+                    }
                 }
             } else {
                 for (int j = tid; j < V; j += kXeThreads) {
-                    float g = ex(IO::to_f(X[base + j]) - m) * c - base_p;
+                    float g = fmaf(ex_shift(IO::to_f(X[base + j]), nm), c, -base_p);
                     if (j == t) g -= hit;
                     DX[base + j] = IO::from_f(g);
                 }
