@@ -81,7 +81,7 @@ def source_hash() -> str:
     csrc = os.path.join(ROOT, "layernorm_ln_fwd_gb300", "csrc")
     # The kernels and their launch planning; the API layer (argument checks, workspaces,
     # status handling) does not change what a kernel moves.
-    for name in ("ln_bwd.cu", "ln_bwd_kernels.cuh", "ln_device.cuh", "ln_fwd.cu",
+    for name in ("ln_bwd.cu", "ln_bwd_kernels.cuh", "ln_device.cuh", "ln_finish.cuh", "ln_fwd.cu",
                  "ln_fwd_kernels.cuh", "ln_internal.h", "rms_bwd.cu", "rms_fwd.cu"):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
             text = f.read()

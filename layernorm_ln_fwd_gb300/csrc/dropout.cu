@@ -6,38 +6,44 @@
 // mask.  Given ds, the gradient with respect to s (the LayerNorm backward's dx, which is also
 // the residual's gradient):
 //   dh = ds * keep / (1 - p),   dbias = sum over rows of dh.
-// dbias is reduced deterministically, without float atomics, in two launches.  The first is
-// a grid of (column tile) x (row segment) blocks of 32 x 8 threads, one wave of three blocks
-// per SM:
-// a thread owns one 16-byte vector of columns (or one column, for rows that are not
-// 16-byte multiples) and every 8th row of its segment, loads a batch of rows before it uses
-// any (many bytes in flight per SM), writes dh and keeps Kahan-compensated column sums; the
-// block folds its 8 row groups in order through shared memory and writes one (hi, lo)
-// partial row per segment.  The second launch adds, for each column, the segments' partials:
-// 16 threads per column each take every 16th segment with all their loads issued at once,
-// then the 16 sums are folded in order (TwoSum throughout); every partial read is zeroed,
-// leaving the workspace all zero for the next call.  The order of every addition depends
-// only on (rows, cols, device), so dbias is bitwise reproducible.
+// One cooperative launch.  A grid of (column tile) x (row segment) blocks of 256 threads
+// (32 column slots x 8 row groups), one wave of resident blocks: a thread owns one 16-byte
+// vector of columns (or one column, for rows that are not 16-byte multiples) and every 8th
+// row of its segment, loads a batch of rows before it uses any (many bytes in flight per
+// SM), writes dh and keeps Kahan-compensated column sums; the block folds its 8 row groups in
+// order through shared memory and stores one (hi, lo) partial row slice per segment, as
+// partials that announce themselves (ln_finish.cuh).  Then the first `segments` blocks each
+// finish a slice of the columns: they read every segment's partials of their slice as they
+// land and add them in segment order (TwoSum), zeroing what they read, so the workspace is
+// left all zero.  The order of every addition depends only on (rows, cols, device), so dbias
+// is bitwise reproducible; no float atomics, no second launch.
 #include <algorithm>
 
 #include "ln_device.cuh"
+#include "ln_finish.cuh"
 #include "ln_internal.h"
 
 namespace lnk {
 namespace {
 
-constexpr int kDbX = 32, kDbY = 8;  // the first launch's block: columns x row groups
+constexpr int kDbX = 32, kDbY = 8;  // a block: column slots x row groups
+constexpr int kDbThreads = kDbX * kDbY;
 constexpr int kDbBatch = 4;         // rows a thread loads before it uses any
-constexpr int kDbBlocksPerSm = 3;   // resident blocks of the first launch (its registers allow 3)
-constexpr int kFinY = 16;           // the finish's threads per column
-constexpr int kFinBatch = 8;        // partials a finish thread loads before it adds any
+constexpr int kDbBlocksPerSm = 3;   // resident blocks (the registers allow 3)
 
+// The finish (finish_units) reads its arguments by these names: one statistic, dbias as
+// "dgamma".
 struct DbParams {
     const void* ds;
     void* dh;
-    void* dbias;
-    float2* part;  // [segments][cols] (hi, lo)
-    int rows, cols, segs;
+    void* dgamma;  // dbias
+    void* dbeta;   // unused (one statistic)
+    float2* part;  // [segments][cols] (hi, lo), announcing themselves
+    int rows, cols, segs, ctiles;
+    int nstat;     // 1
+    int fin_rw;
+    unsigned* status;
+    uint64_t limit_ns;
     float scale;
     DropoutRng rng;
 };
@@ -47,13 +53,6 @@ __device__ __forceinline__ void kahan_step(float& s, float& c, float x) {
     const float t = __fadd_rn(s, y);
     c = __fsub_rn(__fsub_rn(t, s), y);
     s = t;
-}
-
-__device__ __forceinline__ void two_sum_add(float& S, float& C, float h, float l) {
-    float s, e;
-    two_sum_f(S, h, s, e);
-    S = s;
-    C = __fadd_rn(C, __fadd_rn(e, l));
 }
 
 // One 16-byte vector of ds (CV = Io<T>::kVec elements starting at element i0, i0 % CV == 0):
@@ -80,126 +79,103 @@ __device__ __forceinline__ uint4 drop_vec(const DbParams& p, const uint4& u, siz
 }
 
 // CV = Io<T>::kVec adjacent columns per thread with 16-byte accesses (cols % CV == 0 and
-// 16-byte aligned rows), or CV = 1 for any layout.
+// 16-byte aligned rows), or CV = 1 for any layout.  Column tiles are taken grid-stride, so
+// the widest rows still fit in one resident wave.
 template <typename T, int CV>
-__global__ void __launch_bounds__(kDbX * kDbY, kDbBlocksPerSm) dropout_bwd_kernel(const DbParams p) {
+__global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel(const DbParams p) {
     using IO = Io<T>;
     __shared__ float2 fold[kDbY][kDbX * CV];
+    __shared__ float scratch[kDbThreads * 4];  // the finish: 2 U floats per thread, U <= 2
     pdl_enter();
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int col0 = (blockIdx.x * kDbX + tx) * CV;
+    const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
     const int seg = blockIdx.y;
     const int r0 = (int)((long long)p.rows * seg / p.segs);
     const int r1 = (int)((long long)p.rows * (seg + 1) / p.segs);
     const T* ds = static_cast<const T*>(p.ds);
     T* dh = static_cast<T*>(p.dh);
-    float S[CV], C[CV];
+    for (int ct = blockIdx.x; ct < p.ctiles; ct += gridDim.x) {  // block-uniform
+        const int col0 = (ct * kDbX + tx) * CV;
+        float S[CV], C[CV];
 #pragma unroll
-    for (int k = 0; k < CV; ++k) S[k] = C[k] = 0.f;
-    if (col0 < p.cols) {
-        int r = r0 + ty;
-        if constexpr (CV > 1) {
-            for (; r + (kDbBatch - 1) * kDbY < r1; r += kDbBatch * kDbY) {
-                uint4 u[kDbBatch];
+        for (int k = 0; k < CV; ++k) S[k] = C[k] = 0.f;
+        if (col0 < p.cols) {
+            int r = r0 + ty;
+            if constexpr (CV > 1) {
+                for (; r + (kDbBatch - 1) * kDbY < r1; r += kDbBatch * kDbY) {
+                    uint4 u[kDbBatch];
 #pragma unroll
-                for (int b = 0; b < kDbBatch; ++b)
-                    u[b] = __ldcs(reinterpret_cast<const uint4*>(ds + (size_t)(r + b * kDbY) * p.cols + col0));
+                    for (int b = 0; b < kDbBatch; ++b)
+                        u[b] = __ldcs(reinterpret_cast<const uint4*>(ds + (size_t)(r + b * kDbY) * p.cols + col0));
 #pragma unroll
-                for (int b = 0; b < kDbBatch; ++b) {
-                    const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
-                    *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u[b], i0, S, C);
+                    for (int b = 0; b < kDbBatch; ++b) {
+                        const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
+                        *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u[b], i0, S, C);
+                    }
                 }
-            }
-            for (; r < r1; r += kDbY) {
-                const size_t i0 = (size_t)r * p.cols + col0;
-                const uint4 u = __ldcs(reinterpret_cast<const uint4*>(ds + i0));
-                *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u, i0, S, C);
-            }
-        } else {
-            for (; r + (kDbBatch - 1) * kDbY < r1; r += kDbBatch * kDbY) {
-                float v[kDbBatch];
+                for (; r < r1; r += kDbY) {
+                    const size_t i0 = (size_t)r * p.cols + col0;
+                    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(ds + i0));
+                    *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u, i0, S, C);
+                }
+            } else {
+                for (; r + (kDbBatch - 1) * kDbY < r1; r += kDbBatch * kDbY) {
+                    float v[kDbBatch];
 #pragma unroll
-                for (int b = 0; b < kDbBatch; ++b) v[b] = IO::to_f(ds[(size_t)(r + b * kDbY) * p.cols + col0]);
+                    for (int b = 0; b < kDbBatch; ++b) v[b] = IO::to_f(ds[(size_t)(r + b * kDbY) * p.cols + col0]);
 #pragma unroll
-                for (int b = 0; b < kDbBatch; ++b) {
-                    const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
-                    const float w = p.rng.keep(i0) ? __fmul_rn(v[b], p.scale) : 0.f;
+                    for (int b = 0; b < kDbBatch; ++b) {
+                        const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
+                        const float w = p.rng.keep(i0) ? __fmul_rn(v[b], p.scale) : 0.f;
+                        dh[i0] = IO::from_f(w);
+                        kahan_step(S[0], C[0], w);
+                    }
+                }
+                for (; r < r1; r += kDbY) {
+                    const size_t i0 = (size_t)r * p.cols + col0;
+                    const float w = p.rng.keep(i0) ? __fmul_rn(IO::to_f(ds[i0]), p.scale) : 0.f;
                     dh[i0] = IO::from_f(w);
                     kahan_step(S[0], C[0], w);
                 }
             }
-            for (; r < r1; r += kDbY) {
-                const size_t i0 = (size_t)r * p.cols + col0;
-                const float w = p.rng.keep(i0) ? __fmul_rn(IO::to_f(ds[i0]), p.scale) : 0.f;
-                dh[i0] = IO::from_f(w);
-                kahan_step(S[0], C[0], w);
-            }
         }
-    }
 #pragma unroll
-    for (int k = 0; k < CV; ++k) fold[ty][tx * CV + k] = make_float2(S[k], -C[k]);  // value S - C
-    __syncthreads();
-    // The 8 row groups' sums of each column, in row-group order: thread t of the block folds
-    // column slot t (and t + 256, ... for wider tiles), so the partial row is written by all
-    // threads with consecutive addresses.
-    for (int t = ty * kDbX + tx; t < kDbX * CV; t += kDbX * kDbY) {
-        const int c = blockIdx.x * kDbX * CV + t;
-        if (c >= p.cols) continue;
-        float hs = 0.f, ls = 0.f;
+        for (int k = 0; k < CV; ++k) fold[ty][tx * CV + k] = make_float2(S[k], -C[k]);  // value S - C
+        __syncthreads();
+        // The 8 row groups' sums of each column, in row-group order: thread t folds column
+        // slot t (and t + 256, ... for wider tiles), so the slice is stored with consecutive
+        // addresses.
+        for (int t = tid; t < kDbX * CV; t += kDbThreads) {
+            const int c = ct * kDbX * CV + t;
+            if (c >= p.cols) continue;
+            float hs = 0.f, ls = 0.f;
 #pragma unroll
-        for (int g = 0; g < kDbY; ++g) two_sum_add(hs, ls, fold[g][t].x, fold[g][t].y);
-        p.part[(size_t)seg * p.cols + c] = make_float2(hs, ls);
-    }
-}
-
-// Column c's dbias: thread (tx, ty) adds segments ty, ty + 16, ... (kFinBatch loads in
-// flight at a time), the 16 sums are folded in ty order; every partial read is zeroed.
-template <typename T>
-__global__ void __launch_bounds__(kDbX * kFinY) dropout_bias_finish(const DbParams p) {
-    using IO = Io<T>;
-    __shared__ float2 fold[kFinY][kDbX];
-    pdl_enter();
-    const int tx = threadIdx.x, ty = threadIdx.y;
-    const int c = blockIdx.x * kDbX + tx;
-    float hs = 0.f, ls = 0.f;
-    if (c < p.cols) {
-        for (int g0 = ty; g0 < p.segs; g0 += kFinY * kFinBatch) {
-            float2 v[kFinBatch];
-#pragma unroll
-            for (int b = 0; b < kFinBatch; ++b) {
-                const int g = g0 + b * kFinY;
-                v[b] = g < p.segs ? p.part[(size_t)g * p.cols + c] : make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int b = 0; b < kFinBatch; ++b) {
-                const int g = g0 + b * kFinY;
-                if (g < p.segs) p.part[(size_t)g * p.cols + c] = make_float2(0.f, 0.f);
-            }
-#pragma unroll
-            for (int b = 0; b < kFinBatch; ++b) two_sum_add(hs, ls, v[b].x, v[b].y);
+            for (int g = 0; g < kDbY; ++g) comp_add(hs, ls, fold[g][t].x, fold[g][t].y);
+            st_part2(p.part + (size_t)seg * p.cols + c, hs, ls);
         }
+        __syncthreads();  // fold is reused by the next column tile
     }
-    fold[ty][tx] = make_float2(hs, ls);
-    __syncthreads();
-    if (ty == 0 && c < p.cols) {
-        float H = 0.f, L = 0.f;
-#pragma unroll
-        for (int g = 0; g < kFinY; ++g) two_sum_add(H, L, fold[g][tx].x, fold[g][tx].y);
-        static_cast<T*>(p.dbias)[c] = IO::from_f(H + L);
+    // The finish: the first `segs` blocks each own a slice of the column groups.
+    const int f = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+    if (f < p.segs) {
+        if (p.cols % 2 == 0)
+            finish_units<T, 2, false>(p, p.segs, f, scratch);
+        else
+            finish_units<T, 1, false>(p, p.segs, f, scratch);
     }
 }
 
 template <typename T>
 cudaError_t launch_db_t(DbParams p, bool vec, cudaStream_t stream) {
     constexpr int kVec = Io<T>::kVec;
-    const int cv = vec ? kVec : 1;
-    const int ctiles = (p.cols + kDbX * cv - 1) / (kDbX * cv);
-    void* args[] = {&p};
     const void* k1 = vec ? (const void*)dropout_bwd_kernel<T, kVec> : (const void*)dropout_bwd_kernel<T, 1>;
-    cudaError_t e = launch_kernel(k1, dim3(ctiles, p.segs), dim3(kDbX, kDbY), 0, stream, args, false);
-    if (e != cudaSuccess) return e;
-    return launch_kernel((const void*)dropout_bias_finish<T>, dim3((p.cols + kDbX - 1) / kDbX),
-                         dim3(kDbX, kFinY), 0, stream, args, false);
+    const int occ = std::max(1, blocks_per_sm(k1, kDbThreads, 0));
+    const int slots = occ * device_info(-1).sms;  // blocks that can be resident at once
+    const int gx = std::max(1, std::min(p.ctiles, slots / p.segs));
+    if (gx * p.segs > slots) return cudaErrorCooperativeLaunchTooLarge;
+    p.fin_rw = fin_warps_per_group(kDbThreads / 32, p.segs, 2 * (p.cols % 2 == 0 ? 2 : 1));
+    void* args[] = {&p};
+    // Cooperative: every block resident, as the finish's polls need.
+    return launch_kernel(k1, dim3(gx, p.segs), dim3(kDbThreads), 0, stream, args, true);
 }
 
 }  // namespace
@@ -208,32 +184,40 @@ bool dropout_bwd_vector(Dtype dt, int cols, bool aligned) {
     return aligned && cols % (dt == Dtype::F32 ? 4 : 8) == 0;
 }
 
-// Segments of rows for the dbias partials: one wave of resident blocks over the column
-// tiles, at least one batch of rows per row group (32 rows), at most min(rows, 8 per SM)
-// segments (the workspace bound).
+// Segments of rows (partial rows of dbias): one wave of resident blocks over the column
+// tiles, at least one batch of rows per row group (32 rows), and at most min(rows,
+// kDbBlocksPerSm per SM) -- within the workspace bound of 8 per SM, and so that every
+// segment has a resident block for at least one column tile.
 int dropout_bwd_segments(int rows, int cols, int sms, int cv) {
     const int ctiles = (cols + kDbX * cv - 1) / (kDbX * cv);
     int segs = std::max(1, kDbBlocksPerSm * sms / ctiles);
     segs = std::min(segs, std::max(1, rows / (kDbY * kDbBatch)));
-    return std::max(1, std::min(segs, std::min(rows, 8 * sms)));
+    return std::max(1, std::min(segs, std::min(rows, kDbBlocksPerSm * sms)));
 }
 
 cudaError_t launch_dropout_bwd(Dtype dt, const DropoutBwdArgs& a, bool vec, cudaStream_t stream,
                                int* launches) {
     *launches = 0;
+    const int cv = vec ? (dt == Dtype::F32 ? 4 : 8) : 1;
     DbParams p;
     p.ds = a.ds;
     p.dh = a.dh;
-    p.dbias = a.dbias;
+    p.dgamma = a.dbias;
+    p.dbeta = nullptr;
     p.part = reinterpret_cast<float2*>(a.partials);
     p.rows = a.rows;
     p.cols = a.cols;
     p.segs = a.segs;
+    p.ctiles = (a.cols + kDbX * cv - 1) / (kDbX * cv);
+    p.nstat = 1;
+    p.fin_rw = 1;
+    p.status = a.status;
+    p.limit_ns = a.wait_limit_ns;
     p.scale = a.scale;
     p.rng = DropoutRng::make(a.seed, a.offset, a.thr);
     cudaError_t e = dt == Dtype::F32 ? launch_db_t<float>(p, vec, stream)
                                      : launch_db_t<__nv_bfloat16>(p, vec, stream);
-    if (e == cudaSuccess) *launches = 2;
+    if (e == cudaSuccess) *launches = 1;
     return e;
 }
 

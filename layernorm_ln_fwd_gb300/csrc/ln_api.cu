@@ -414,6 +414,8 @@ ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64
     a.thr = drop_threshold(p);
     a.seed = seed;
     a.offset = offset;
+    a.status = status_word();
+    a.wait_limit_ns = wait_limit_ns();
     int launches = 0;
     cudaError_t e = launch_dropout_bwd(dt, a, vec, stream, &launches);
     return finish_call(e, launches, stream);

@@ -173,7 +173,8 @@ cudaError_t launch_xent(Dtype dt, const XentArgs& a, bool aligned, cudaStream_t 
                         int* launches);
 
 // Backward of the bias + dropout + residual prologue: dh = ds * keep * scale and the
-// deterministic column sums dbias (partials: [segs][cols] (hi, lo) fp32 pairs, left zero).
+// deterministic column sums dbias (partials: [segs][cols] (hi, lo) fp32 pairs that announce
+// themselves, left zero), in one cooperative launch.
 struct DropoutBwdArgs {
     const void* ds;
     void* dh;
@@ -183,6 +184,8 @@ struct DropoutBwdArgs {
     float scale;
     uint32_t thr;
     unsigned long long seed, offset;
+    unsigned* status;          // the per-device status word (bounded waits)
+    uint64_t wait_limit_ns;
 };
 
 // Whether the kernels take 16-byte vectors (rows of whole vectors, aligned pointers).
