@@ -371,6 +371,8 @@ ln_status xent_impl(Dtype dt, const T* logits, const int32_t* targets, int64_t r
     a.dloss = dloss;
     a.losses = losses;
     a.dlogits = dlogits;
+    a.status = status_word();
+    a.wait_limit_ns = wait_limit_ns();
     int launches = 0;
     cudaError_t e = launch_xent(dt, a, vector_ok(dt, (int)V, ptrs, 2), stream, &launches);
     return finish_call(e, launches, stream);

@@ -167,6 +167,8 @@ struct XentArgs {
     float dloss;
     float* losses;
     void* dlogits;
+    unsigned* status;  // the per-device status word (bounded waits)
+    uint64_t wait_limit_ns;
 };
 
 cudaError_t launch_xent(Dtype dt, const XentArgs& a, bool aligned, cudaStream_t stream,
