@@ -3,12 +3,12 @@
 // Forward ("Accelerating Transformer on GPU (I)", section 4.1: scale, add the mask, row max,
 // exponentiate, row sum, divide, all in one kernel):
 //   z = scale * x + mask[r % mask_rows],  y = exp(z - max z) / sum exp(z - max z).
-// The row is read once into registers; each lane (thread) keeps the maximum m of its own
-// values and the sum s of exp(z - m), and the (m, s) pairs are merged in ONE reduction -- the
-// "online" merge m = max(ma, mb), s = sa exp(ma - m) + sb exp(mb - m) -- instead of the
-// page's two dependent reductions (max, then sum).  Each exponential is taken once:
-// y = exp(z - m_lane) * (exp(m_lane - M) / S).  The kernels work in base 2 -- z' = z log2(e)
-// = (scale log2 e) x + mask log2 e, and exp(z - m) = exp2(z' - m') -- so that every
+// The row is read once into registers.  A warp per row takes the page's two reductions (the
+// row maximum, then the sum of exp(z - max)): one shuffle and one max or add per butterfly
+// level.  A block per row merges its warps' (max, sum) pairs in ONE exchange through shared
+// memory with the "online" merge m = max(ma, mb), s = sa exp(ma - m) + sb exp(mb - m), which
+// saves a block barrier there.  The kernels work in base 2 -- z' = z log2(e) =
+// (scale log2 e) x + mask log2 e, and exp(z - m) = exp2(z' - m') -- so that every
 // exponential is one approximate base-2 exponent of the special-function unit (ex2_fast).
 // Backward ("Accelerating Transformer on GPU (II)", section 3.1: only y is needed, one row
 // reduction): dx = scale * y * (dy - sum dy y).
@@ -16,9 +16,9 @@
 // Kernel families, as for the LayerNorm: warp per row fed by a bulk-copy (TMA) tile ring for
 // rows of at most 256 vectors of 16 bytes (the page's lengths up to 2048 in bf16); a block
 // per row, registers loaded with 128-bit loads, for longer rows; a scalar kernel for rows
-// that are not 16-byte multiples or unaligned pointers.  The merge is symmetric in its two
-// operands (max, commutative sums of separately rounded products), so every lane ends with
-// the same bits.  A row whose entries are all -inf gives NaN, as the definition does.
+// that are not 16-byte multiples or unaligned pointers.  Reductions are symmetric in their
+// operands (max, commutative sums of separately rounded terms), so every lane ends with the
+// same bits.  A row whose entries are all -inf gives NaN, as the definition does.
 #include <algorithm>
 #include <math.h>
 
@@ -74,6 +74,65 @@ __device__ __forceinline__ float warp_sum1f(float a) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(kFullMask, a, o);
     return a;
+}
+
+__device__ __forceinline__ float warp_max1f(float a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFullMask, a, o));
+    return a;
+}
+
+// The forward of one row held by one warp, in the pages' two reductions ("Accelerating
+// Transformer on GPU (I)", section 4.1): the row maximum M (one butterfly), then
+// S = sum exp(z - M) (another), y = exp(z - M) / S.  Each butterfly level is one shuffle and
+// one max or add -- against two exponentials and a rescale per level for the online merge --
+// and the warp-per-row kernel runs enough warps per SM that instructions, not the second
+// butterfly's latency, set its time.  Every lane ends with the same M and S (each level
+// combines a pair commutatively).  A row whose entries are all -inf gives NaN (0 / 0).
+template <typename T, int VPL, typename XS, typename MS, typename VALID, typename STORE>
+__device__ __forceinline__ void warp_softmax_row(XS xs, MS ms, VALID valid, float scale,
+                                                 STORE store) {
+    using PR = Pairs<T>;
+    constexpr int H = PR::kPairs;
+    f2 z[VPL][H];
+    float m = -INFINITY;
+    const f2 a2 = f2_splat(scale * kLog2e), l2 = f2_splat(kLog2e);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        if (!valid(v)) continue;
+        f2 xv[H], mv[H];
+        PR::unpack(xs(v), xv);
+        PR::unpack(ms(v), mv);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            // z' = (scale log2 e) x + mask log2 e: the score in base 2.
+            z[v][h] = f2_fma(a2, xv[h], f2_mul(mv[h], l2));
+            m = fmaxf(m, fmaxf(f2_lo(z[v][h]), f2_hi(z[v][h])));
+        }
+    }
+    const float M = warp_max1f(m);
+    const f2 nM = f2_splat(M == -INFINITY ? 0.f : -M);
+    f2 acc = f2_splat(0.f);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        if (!valid(v)) continue;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+            const f2 t = f2_add(z[v][h], nM);
+            z[v][h] = f2_make(ex2_fast(f2_lo(t)), ex2_fast(f2_hi(t)));
+            acc = f2_add(acc, z[v][h]);
+        }
+    }
+    const float S = warp_sum1f(f2_lo(acc) + f2_hi(acc));
+    const f2 c2 = f2_splat(M == -INFINITY ? __int_as_float(0x7fc00000) : 1.0f / S);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+        if (!valid(v)) continue;
+        f2 o[H];
+#pragma unroll
+        for (int h = 0; h < H; ++h) o[h] = f2_mul(z[v][h], c2);
+        store(v, PR::pack(o));
+    }
 }
 
 // The forward of one row held as VPL vectors per lane (lane l: vectors l, l + stride, ...):
@@ -232,18 +291,12 @@ __global__ void __launch_bounds__(kSmTileThreads, VPL <= 4 ? 2 : 1) sm_tile_kern
                 }
             } else {
                 const T* mrow = M ? M + (size_t)(row % p.mask_rows) * cols : nullptr;
-                SmRow<T, VPL> r;
-                r.local([&](int v) { return vec(as, v); },
-                        [&](int v) { return mrow ? ld_keep(mrow + (size_t)(v * 32 + lane) * V)
-                                                 : make_uint4(0, 0, 0, 0); },
-                        valid, p.scale);
-                float mw = r.m, sw = r.s;
-                warp_online(mw, sw);  // the one reduction of the row
-                const float c = mw == -INFINITY ? __int_as_float(0x7fc00000)
-                                            : (r.m == -INFINITY ? 0.f : ex2_fast(r.m - mw) / sw);
-#pragma unroll
-                for (int v = 0; v < VPL; ++v)
-                    if (valid(v)) st_stream(out + base + (size_t)(v * 32 + lane) * V, r.y(v, c));
+                warp_softmax_row<T, VPL>(
+                    [&](int v) { return vec(as, v); },
+                    [&](int v) { return mrow ? ld_keep(mrow + (size_t)(v * 32 + lane) * V)
+                                             : make_uint4(0, 0, 0, 0); },
+                    valid, p.scale,
+                    [&](int v, const uint4& y) { st_stream(out + base + (size_t)(v * 32 + lane) * V, y); });
             }
         }
         __syncwarp();
