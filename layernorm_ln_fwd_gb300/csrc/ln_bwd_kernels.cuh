@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {
                         f2 d[H], xx[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
+                        PR::load_staged(dys[r] + (size_t)vi * V, d);
+                        PR::load_staged(xs[r] + (size_t)vi * V, xx);
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
                             const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {
                         f2 d[H], xx[H], o[H];
-                        PR::unpack(*reinterpret_cast<const uint4*>(dys[r] + (size_t)vi * V), d);
-                        PR::unpack(*reinterpret_cast<const uint4*>(xs[r] + (size_t)vi * V), xx);
+                        PR::load_staged(dys[r] + (size_t)vi * V, d);
+                        PR::load_staged(xs[r] + (size_t)vi * V, xx);
 #pragma unroll
                         for (int h = 0; h < H; ++h) {
                             const f2 xh = f2_mul(f2_sub(xx[h], mu2[r]), rs2[r]);
@@ -575,8 +575,8 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
                 f2 d[H], xx[H];
-                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                PR::load_staged(dys + (size_t)vi * V, d);
+                PR::load_staged(xs + (size_t)vi * V, xx);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);
@@ -613,8 +613,8 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
             const int vi = v * nthreads + tid;
             if (vi < nvec) {
                 f2 d[H], xx[H], o[H];
-                PR::unpack(*reinterpret_cast<const uint4*>(dys + (size_t)vi * V), d);
-                PR::unpack(*reinterpret_cast<const uint4*>(xs + (size_t)vi * V), xx);
+                PR::load_staged(dys + (size_t)vi * V, d);
+                PR::load_staged(xs + (size_t)vi * V, xx);
 #pragma unroll
                 for (int h = 0; h < H; ++h) {
                     const f2 xh = f2_mul(f2_sub(xx[h], mu2), rs2);

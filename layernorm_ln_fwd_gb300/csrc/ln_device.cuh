@@ -160,6 +160,16 @@ struct Pairs<float> {
         return make_uint4((uint32_t)p[0].v, (uint32_t)(p[0].v >> 32), (uint32_t)p[1].v,
                           (uint32_t)(p[1].v >> 32));
     }
+    // A vector staged in shared memory, as its two pairs, with ONE 128-bit load.  (Left to
+    // itself the compiler reads such a vector as two 64-bit loads, one per pair; at a lane
+    // stride of 16 bytes each of those is 2-way bank-conflicted.)  Ordered after the wait
+    // that made the data visible, like any other memory access.
+    static __device__ __forceinline__ void load_staged(const float* p, f2 (&o)[2]) {
+        asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];"
+                     : "=l"(o[0].v), "=l"(o[1].v)
+                     : "r"((unsigned)__cvta_generic_to_shared(p))
+                     : "memory");
+    }
 };
 
 template <>
@@ -183,6 +193,10 @@ struct Pairs<__nv_bfloat16> {
     }
     static __device__ __forceinline__ uint4 pack(const f2 (&p)[4]) {
         return make_uint4(bits(p[0]), bits(p[1]), bits(p[2]), bits(p[3]));
+    }
+    // A vector staged in shared memory (one 128-bit load: its four words feed four pairs).
+    static __device__ __forceinline__ void load_staged(const __nv_bfloat16* p, f2 (&o)[4]) {
+        unpack(*reinterpret_cast<const uint4*>(p), o);
     }
 };
 
