@@ -601,12 +601,7 @@ __global__ void __launch_bounds__(kBwdBlockMaxThreads, 1) bwd_block_kernel(const
         }
         __syncthreads();  // the one cross-warp exchange of the row
         if (abort_flag) break;
-        tg = 0.f;
-        tgx = 0.f;
-        for (int w = 0; w < nw; ++w) {  // same order in every thread
-            tg += red[0][w];
-            tgx += red[1][w];
-        }
+        sum_warp_values2(red[0], red[1], nw, tg, tgx);  // the same bits in every thread
         const f2 mg2 = f2_splat(RMS ? 0.f : rdiv.div(tg)), mgx2 = f2_splat(rdiv.div(tgx));
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {

@@ -236,6 +236,18 @@ __device__ __forceinline__ void warp_sum2(float& a, float& b) {
     b = f2_hi(v);
 }
 
+// The sums of n <= 32 per-warp values of two statistics exchanged through shared memory
+// (sa[0..n), sb[0..n)), the same bits in every thread of the block: each warp loads them into
+// its lanes (zeros past n) and adds them with the xor butterfly -- two loads and five
+// shuffle-adds instead of a serial loop over the warps.
+__device__ __forceinline__ void sum_warp_values2(const float* sa, const float* sb, int n,
+                                                 float& a, float& b) {
+    const int lane = threadIdx.x & 31;
+    a = lane < n ? sa[lane] : 0.f;
+    b = lane < n ? sb[lane] : 0.f;
+    warp_sum2(a, b);
+}
+
 // Division by the row length without a division per row: with inv = 1/n rounded once per
 // kernel, q0 = a * inv rounded, the residual r = a - q0 * n exact in one fma, and one
 // correction q = q0 + r * inv give the correctly rounded a / n (Markstein's correction; see

@@ -377,12 +377,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         }
         __syncthreads();
         if (abort_flag) return false;
-        a = 0.f;
-        b = 0.f;
-        for (int w = 0; w < nw; ++w) {
-            a += red[e][0][w];
-            b += red[e][1][w];
-        }
+        sum_warp_values2(red[e][0], red[e][1], nw, a, b);  // the same bits in every thread
         return true;
     };
 
