@@ -60,7 +60,7 @@ constexpr int kTileThreads = (kTileRows + 1) * 32;
 constexpr int kBwdBlockMaxThreads = 512;
 constexpr int kBwdScalarThreads = 256;
 constexpr int kMaxStages = 8;
-constexpr int kBlockStages = 4;
+constexpr int kBlockStages = 3;
 // The warp kernel is used for bf16 rows of up to 5 vectors per lane (1280 columns) and at
 // most this many rows, which keeps its plain per-lane chains short.
 constexpr int kWarpPathMaxRows = 65536;
@@ -878,8 +878,10 @@ cudaError_t plan_bwd_t(Dtype dt, int rows, int cols, bool aligned, int path_over
             const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
             const size_t share = std::min<size_t>(
                 (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
-            // Rows in flight: up to 4, within the block's share of shared memory (measured on
-            // GB300, deeper prefetch only delays every block's first row).
+            // Rows in flight: up to 3, within the block's share of shared memory.  Measured on
+            // GB300 at bf16 4096 x 8192: 2 / 3 / 4 rows 45.0 / 41.7 / 42.5 us; refilling a slot
+            // a pass earlier than after the row's last use (more lead) took 60.7 us -- deeper
+            // prefetch delays every block's first rows in the DRAM queue.
             const int stages = (int)std::min<size_t>(kBlockStages, share / slot);
             p.stages = std::max(1, stages);
             p.smem = std::max<size_t>((size_t)p.stages * slot, (size_t)p.threads * 32);
