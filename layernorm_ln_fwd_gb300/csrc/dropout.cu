@@ -158,9 +158,9 @@ __global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel
     const int f = (int)(blockIdx.y * gridDim.x + blockIdx.x);
     if (f < p.segs) {
         if (p.cols % 2 == 0)
-            finish_units<T, 2, false>(p, p.segs, f, scratch);
+            finish_units<T, 2, false>(p, p.segs, p.segs, f, scratch);
         else
-            finish_units<T, 1, false>(p, p.segs, f, scratch);
+            finish_units<T, 1, false>(p, p.segs, p.segs, f, scratch);
     }
 }
 

@@ -81,6 +81,8 @@ struct KParams {
     int compact;   // partials without the lo half (kernels whose column sums are plain)
     int fin_rw;    // warps per unit group in the finish (divides the block's warp count)
     int nstat;     // column statistics: 2 (dgamma, dbeta) or 1 (the RMSNorm's dgamma)
+    int P;         // partial rows (the row kernel's grid)
+    int split_finish;  // 1: a separate dependent launch finishes; 0: the row kernel does
     unsigned* ctr;  // a zero word nothing writes (the bounded-wait test polls it)
     unsigned* status;
     uint64_t limit_ns;
@@ -113,15 +115,40 @@ __device__ __forceinline__ void kahan_add(float& s, float& c, float x) {
     s = t;
 }
 
-// Called by every thread of every block once the block's partial row is stored.  Blocks that
-// own no unit group of the finish are done and leave, freeing their SM; the others finish
-// their groups, picking up each block's partials as they land.
+// The finish of block f of F over P partial rows, for the partial layout the plan chose.
+template <typename T>
+__device__ void finish_dispatch(const KParams& a, int P, int F, int f, float* scratch) {
+    if (a.compact) {
+        if (a.cols % 4 == 0)
+            finish_units<T, 4, true>(a, P, F, f, scratch);
+        else if (a.cols % 2 == 0)
+            finish_units<T, 2, true>(a, P, F, f, scratch);
+        else
+            finish_units<T, 1, true>(a, P, F, f, scratch);
+    } else {
+        if (a.cols % 2 == 0)
+            finish_units<T, 2, false>(a, P, F, f, scratch);
+        else
+            finish_units<T, 1, false>(a, P, F, f, scratch);
+    }
+}
+
+// Unit groups of the finish (as finish_units splits them).
+__device__ __forceinline__ int finish_groups(const KParams& a) {
+    const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
+                            : (a.cols % 2 == 0 ? 2 : 1);  // as finish_dispatch instantiates
+    return (a.nstat * (a.cols / U) + kFinUnits - 1) / kFinUnits;
+}
+
+// Called by every thread of every block once the block's partial row is stored, when the
+// finish runs inside the row kernel.  Blocks that own no unit group of the finish are done
+// and leave, freeing their SM; the others finish their groups, picking up each block's
+// partials as they land.
 template <typename T>
 __device__ void finish_if_owner(const KParams& a, float* scratch) {
+    if (a.split_finish) return;  // a separate launch finishes
     const int P = (int)gridDim.x, f = (int)blockIdx.x;
-    const int U = a.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
-                            : (a.cols % 2 == 0 ? 2 : 1);  // as finish_units is instantiated
-    const int ng = (a.nstat * (a.cols / U) + kFinUnits - 1) / kFinUnits;
+    const int ng = finish_groups(a);
     const bool finisher = (f + 1) * ng / P > f * ng / P;  // as finish_units splits the groups
     if (!finisher) return;  // the same for every thread of the block
     __syncthreads();        // shared memory becomes the finish's scratch
@@ -129,19 +156,21 @@ __device__ void finish_if_owner(const KParams& a, float* scratch) {
         // Test hook: also wait for a word that nothing writes, so the limit runs out.
         if (!wait_counter_geq(a.ctr, 1u, a.limit_ns)) raise_status(a.status, kStatusTimeout);
     }
-    if (a.compact) {
-        if (a.cols % 4 == 0)
-            finish_units<T, 4, true>(a, P, f, scratch);
-        else if (a.cols % 2 == 0)
-            finish_units<T, 2, true>(a, P, f, scratch);
-        else
-            finish_units<T, 1, true>(a, P, f, scratch);
-    } else {
-        if (a.cols % 2 == 0)
-            finish_units<T, 2, false>(a, P, f, scratch);
-        else
-            finish_units<T, 1, false>(a, P, f, scratch);
+    finish_dispatch<T>(a, P, P, f, scratch);
+}
+
+// The finish as its own launch, programmatically dependent on the row kernel: its blocks are
+// scheduled while the row kernel runs and wait (griddepcontrol.wait) until it has completed,
+// so every partial row is already written when they read them -- no polling.
+constexpr int kFinThreads = 256;
+template <typename T>
+__global__ void __launch_bounds__(kFinThreads) bwd_finish_kernel(const KParams a) {
+    __shared__ float scratch[kFinThreads * 8];  // 2 U floats per thread, U <= 4
+    pdl_enter();
+    if (a.wait_extra && threadIdx.x == 0) {
+        if (!wait_counter_geq(a.ctr, 1u, a.limit_ns)) raise_status(a.status, kStatusTimeout);
     }
+    finish_dispatch<T>(a, a.P, (int)gridDim.x, (int)blockIdx.x, scratch);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -930,10 +959,18 @@ cudaError_t launch_bwd_t(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStrea
     k.acc = bwd_plan_acc_region(p) ? k.part + 2ull * (size_t)p.grid * (size_t)a.cols : nullptr;
     k.compact = (p.path == kPathScalar || p.kahan) ? 0 : 1;
     k.nstat = RMS ? 1 : 2;
+    k.P = p.grid;
+    // The block-per-row kernel hands the finish to a separate dependent launch: there every
+    // block would finish (one block per SM, wide rows) and the early ones poll rows not yet
+    // written.  Measured on GB300: bf16 4096 x 8192 backward 41.8 -> 40.9 us split; the warp
+    // kernel's in-kernel finish is faster (bf16 8192 x 768 12.0 us against 13.3 split).
+    const bool split = p.path == kPathBlock;
+    k.split_finish = split ? 1 : 0;
     {
         const int U = k.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
                                 : (a.cols % 2 == 0 ? 2 : 1);
-        k.fin_rw = fin_warps_per_group(p.threads / 32, p.grid, (k.compact ? 1 : 2) * U);
+        const int nw = (split ? kFinThreads : p.threads) / 32;
+        k.fin_rw = fin_warps_per_group(nw, p.grid, (k.compact ? 1 : 2) * U);
     }
     k.ctr = a.counters;
     k.status = a.status;
@@ -941,6 +978,18 @@ cudaError_t launch_bwd_t(Dtype dt, const BwdArgs& a, const BwdPlan& p, cudaStrea
     k.wait_extra = a.wait_extra;
     k.stages = p.stages;
     void* args[] = {&k};
+    if (split) {
+        cudaError_t e = launch_kernel(kern, dim3(p.grid), dim3(p.threads), p.smem, stream, args, false);
+        if (e != cudaSuccess) return e;
+        const int U = k.compact ? (a.cols % 4 == 0 ? 4 : a.cols % 2 == 0 ? 2 : 1)
+                                : (a.cols % 2 == 0 ? 2 : 1);
+        const int ng = (k.nstat * (a.cols / U) + kFinUnits - 1) / kFinUnits;
+        const void* fk = dt == Dtype::F32 ? (const void*)bwd_finish_kernel<float>
+                                          : (const void*)bwd_finish_kernel<__nv_bfloat16>;
+        e = launch_kernel(fk, dim3(std::max(1, ng)), dim3(kFinThreads), 0, stream, args, false);
+        if (e == cudaSuccess) *launches = 2;
+        return e;
+    }
     // A cooperative launch: all blocks co-resident, as the finish's polls need.
     cudaError_t e = launch_kernel(kern, dim3(p.grid), dim3(p.threads), p.smem, stream, args, true);
     if (e == cudaSuccess) *launches = 1;

@@ -25,7 +25,7 @@ __device__ __forceinline__ void comp_add(float& S, float& C, float h, float l) {
 // (hi, lo) pair per column, or one plain fp32 sum when COMPACT, and U is chosen so that one
 // unit of one partial row is a single 16-byte load where the row length allows.  Units are
 // taken in groups of kFinUnits adjacent ones (128 contiguous bytes of a partial row); block f
-// of P owns groups [f * g / P, (f + 1) * g / P).  The block's warps work on GW groups at a
+// of the F finishing blocks owns groups [f * g / F, (f + 1) * g / F).  The block's warps work on GW groups at a
 // time, RW warps per group (RW * GW = the warp count, RW chosen by the host so that a lane's
 // rows fit in one batch).  Warp r of a group's RW takes the contiguous range of partial rows
 // [r * P / RW, (r + 1) * P / RW); lane (s, k), s < kFinSub, k < kFinUnits, adds unit k of
@@ -68,7 +68,7 @@ __device__ __forceinline__ bool has_zero(const uint32_t (&w)[N]) {
 }
 
 template <typename T, int U, bool COMPACT, typename A>
-__device__ void finish_units(const A& a, int P, int f, float* scratch) {
+__device__ void finish_units(const A& a, int P, int F, int f, float* scratch) {
     using IO = Io<T>;
     constexpr int E = COMPACT ? 1 : 2;  // floats per column of a partial
     constexpr int W = E * U;            // words per unit of a partial row: 1, 2 or 4
@@ -77,7 +77,7 @@ __device__ void finish_units(const A& a, int P, int f, float* scratch) {
     const int ngroups = cols / U;       // units per statistic
     const int nunits = a.nstat * ngroups;
     const int ng = (nunits + kFinUnits - 1) / kFinUnits;
-    const int g0 = f * ng / P, g1 = (f + 1) * ng / P;  // f * ng < 2^24: 32-bit is exact
+    const int g0 = f * ng / F, g1 = (f + 1) * ng / F;  // f * ng < 2^24: 32-bit is exact
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int RW = a.fin_rw, GW = nw / RW;
     const int gw = warp / RW, rw = warp - gw * RW;

@@ -50,7 +50,9 @@ def test_noalloc_backward_matches_regular_backward_twice(rows, cols):
         dx_ref, dg_ref, db_ref = ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd)
         st, dx, dg, db = _noalloc(d, res_out, mean, rstd, stream)
         assert st == 0, ln.STATUS.get(st, st)
-        assert ln.last_launch_count() == 1
+        # The block-per-row kernel (aligned rows wider than 1280 bf16 columns) hands its
+        # column sums' finish to a second, dependent launch.
+        assert ln.last_launch_count() == (2 if cols > 1280 and cols % 8 == 0 else 1)
         torch.cuda.synchronize()
         for name, got, ref in (("dx", dx, dx_ref), ("dgamma", dg, dg_ref),
                                ("dbeta", db, db_ref)):
