@@ -2,7 +2,8 @@
 oracle ("Accelerating Transformer on GPU (I)", section 5.2): losses (fp32, 2e-5 relative
 above 1 as for the other fp32 statistics) and the gradient dloss * (q - p) (fp32 2e-5,
 bf16 2 ulps), with and without label smoothing, in place over the logits, for vocabulary
-widths that are and are not 16-byte multiples (GPT-2's 50257, llm.c's padded 50304), and at
+widths that are and are not 16-byte multiples (GPT-2's 50257, llm.c's padded 50304), on
+both forms of the kernel (rows staged in shared memory, rows streamed through L2), and at
 the GPT-2-small classifier size (8 x 1024 rows) on every element."""
 import numpy as np
 import pytest
@@ -42,6 +43,17 @@ def test_widths_against_oracle(dtype, V, alpha):
     rows = 64 if V < 10000 else 24
     x, t = case(rows, V, dtype, seed=V)
     check(x, t, alpha, 1.0 / rows, dtype)
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 56320), ("bf16", 65536), ("f32", 24576),
+                                     ("f32", 50304)])
+def test_staged_and_streaming_forms(dtype, V):
+    """Rows of 16-byte vectors that fit twice in shared memory are staged whole (bf16 56320:
+    2 x 110 KB; fp32 24576: 2 x 96 KB); wider ones stream through L2 (bf16 65536, fp32
+    50304).  Both forms against the oracle, in place and not."""
+    x, t = case(12, V, dtype, seed=V + 1)
+    check(x, t, 0.1, 1.0 / 12, dtype)
+    check(x, t, 0.0, 1.0, dtype, in_place=True)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
