@@ -38,9 +38,10 @@
  *    forward; for the backward it writes dgamma = dbeta = 0.  With rows == 0 the pointers
  *    to [rows, cols] and [rows] arrays may be NULL (empty tensors often have no storage).
  *    eps must be finite and >= 0.
- *  - Kernels are launched with programmatic dependent launch allowed (and the backward
- *    cooperatively).  Each kernel still waits for the work before it in the stream to finish
- *    before it touches memory, so stream order is the usual one, in CUDA graphs too.
+ *  - Kernels are launched with programmatic dependent launch allowed (backward kernels that
+ *    finish their column sums in-kernel, and the dropout backward, cooperatively).  Each
+ *    kernel still waits for the work before it in the stream to finish before it touches
+ *    memory, so stream order is the usual one, in CUDA graphs too.
  *  - Thread safety: entry points may be called from several host threads.  Two backward
  *    calls that share a workspace (the same stream, or the same caller-owned workspace) must
  *    not overlap on the GPU; stream order takes care of that for one stream.
@@ -435,7 +436,9 @@ int ln_version(void);
 int ln_debug_force_path(int path);
 void ln_debug_wait_test(unsigned limit_us);
 
-/* Number of kernels the most recent ln_fwd_* / ln_bwd_* call on this host thread launched. */
+/* Number of kernels the most recent call of this library on this host thread launched (1 for
+ * most calls; 2 for a backward on the block-per-row path, whose column sums are finished by
+ * a second, dependent launch). */
 int ln_last_launch_count(void);
 
 #ifdef __cplusplus

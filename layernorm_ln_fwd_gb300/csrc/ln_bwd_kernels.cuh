@@ -26,10 +26,12 @@
 //     has read for the next call.
 //  This is the last-block-finishes idea of llm.c's layernorm_backward_kernel10 ("llm.c: the
 //  llmc/ CUDA kernel layer", section 3.3), widened from one finishing block to many so that
-//  the finish is spread over SMs instead of serialising one SM on all partials.  The grid
-//  is launched cooperatively, so every block is resident and the polls always end.  Which
-//  block adds which rows, and in what order, depends only on (rows, cols, device), so
-//  dgamma and dbeta are bitwise reproducible run to run.
+//  the finish is spread over SMs instead of serialising one SM on all partials.  The warp
+//  and scalar kernels finish in the same launch, which is cooperative, so every block is
+//  resident and the polls always end; the block-per-row kernel hands the finish to a second
+//  launch that waits for it to complete (programmatic dependent launch), so nothing polls
+//  there.  Which block adds which rows, and in what order, depends only on (rows, cols,
+//  device), so dgamma and dbeta are bitwise reproducible run to run.
 //
 // Accuracy of the column sums.  A plain fp32 sum of n terms of size sigma carries an error
 // of about 2^-24 * sigma * sqrt(n * L) for chains of L additions, whatever the order: for
