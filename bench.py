@@ -469,10 +469,11 @@ class OpBench(Workbench):
         elif op["kind"] == "xent":  # one fused kernel: read the logits, write the gradient
             self.set_bytes = 2 * R * C * s
             self.fwd_b, self.bwd_b = 2 * R * C * s + 8 * R, 0
-        else:  # bdr: the prologue-fused LayerNorm forward; the prologue's backward
-            self.set_bytes = 7 * R * C * s
-            self.fwd_b = fwd_bytes(R, C, s) + C * s
-            self.bwd_b = 2 * R * C * s + C * s
+        else:  # bdr, bdr_keep: the prologue-fused LayerNorm forward; the prologue's backward
+            kb = R * ((C + 7) // 8) if op["kind"] == "bdr_keep" else 0  # the stored keep bits
+            self.set_bytes = 7 * R * C * s + kb
+            self.fwd_b = fwd_bytes(R, C, s) + C * s + kb
+            self.bwd_b = 2 * R * C * s + C * s + kb
         nsets = max(2, -(-3 * l2 // self.set_bytes) + 1)
         self.nsets = nsets + nsets % 2
         self.sets = []
@@ -486,7 +487,9 @@ class OpBench(Workbench):
                                                      dtype=torch.int32),
                      "loss": torch.empty(R, dtype=torch.float32, device="cuda"),
                      "dx": torch.empty_like(d["x"])}
-            elif op["kind"] == "bdr":
+            elif op["kind"] in ("bdr", "bdr_keep"):
+                if op["kind"] == "bdr_keep":
+                    d.update(keep=torch.empty(R * ((C + 7) // 8), dtype=torch.uint8, device="cuda"))
                 d.update(bias=(0.1 * d["beta"].float()).to(td), out=torch.empty_like(d["x"]),
                          res_out=torch.empty_like(d["x"]), dx=torch.empty_like(d["x"]),
                          mean=torch.empty(R, dtype=torch.float32, device="cuda"),
@@ -521,7 +524,8 @@ class OpBench(Workbench):
         else:
             self.ln.fwd_bias_dropout(S["x"], S["bias"], S["res"], S["gamma"], S["beta"], 1e-5,
                                      self.op["p"], 17, i, out=S["out"], res_out=S["res_out"],
-                                     mean=S["mean"], rstd=S["rstd"], stream=self.stream)
+                                     mean=S["mean"], rstd=S["rstd"], keep=S.get("keep"),
+                                     stream=self.stream)
 
     def bwd(self, i):
         S = self.sets[i % self.nsets]
@@ -531,9 +535,9 @@ class OpBench(Workbench):
                             dgamma=S["dgamma"], workspace=self.ws, stream=self.stream)
         elif kind == "softmax":
             self.ln.softmax_bwd(S["dy"], S["y"], self.op["scale"], dx=S["dx"], stream=self.stream)
-        elif kind == "bdr":
+        elif kind in ("bdr", "bdr_keep"):
             self.ln.dropout_bwd(S["dy"], self.op["p"], 17, i, dh=S["dx"], dbias=S["dbias"],
-                                workspace=self.ws, stream=self.stream)
+                                workspace=self.ws, keep=S.get("keep"), stream=self.stream)
 
 
 def run_ours(args):

@@ -311,7 +311,8 @@ ln_status ln_xent_bf16(const ln_bf16* logits, const int32_t* targets, int64_t ro
  * counter-based generator Philox-4x32-10 (Salmon, Moraes, Dror and Shaw, SC 2011) at counter
  * (i / 4 as two 32-bit words, offset as two 32-bit words) under key (seed as two 32-bit
  * words) is at least floor(p * 2^32).  The mask is a pure function of (seed, offset, i), so
- * the backward regenerates it; nothing is stored.  Use a new offset (or seed) per call.
+ * the backward regenerates it and nothing need be stored (the _keep variants below also
+ * store it, as bits, for a backward that reads them).  Use a new offset (or seed) per call.
  *
  *   h        [rows, cols]  the linear layer's output
  *   bias     [cols]        its bias
@@ -361,6 +362,52 @@ ln_status ln_dropout_bwd_f32_ws(const float* ds, float p, uint64_t seed, uint64_
 ln_status ln_dropout_bwd_bf16_ws(const ln_bf16* ds, float p, uint64_t seed, uint64_t offset,
                                  int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
                                  void* workspace, size_t workspace_bytes, ln_stream_t stream);
+
+/*
+ * The prologue with its keep decisions stored for the backward ("Accelerating Transformer on
+ * GPU (II): Training with LightSeq2", section 3.2: the dropout backward needs the forward's
+ * mask; LightSeq keeps one byte per element, this keeps one bit).  The forward decides each
+ * element anyway; the _keep forward also writes the decisions as bits:
+ *
+ *   bit (col % 8) of keep[row * ceil(cols / 8) + col / 8] = 1  when (row, col) is kept
+ *
+ * (rows padded to whole bytes; the pad bits of a row's last byte are 0), and the _keep
+ * backward reads them instead of running the generator again -- its result is bit for bit
+ * that of ln_dropout_bwd_* with the forward's (p, seed, offset).  keep: caller-owned device
+ * memory of ln_dropout_keep_bytes(rows, cols) bytes.  Arguments, workspace rules and errors as
+ * for ln_fwd_bias_dropout_* / ln_dropout_bwd_*, plus LN_EINVAL for a NULL keep with
+ * rows > 0.  ln_dropout_keep_bytes returns 0 for invalid sizes.
+ */
+size_t ln_dropout_keep_bytes(int64_t rows, int64_t cols);
+
+ln_status ln_fwd_bias_dropout_keep_f32(const float* h, const float* bias, const float* res,
+                                       const float* gamma, const float* beta, float eps, float p,
+                                       uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                       float* out, float* res_out, float* mean, float* rstd,
+                                       uint8_t* keep, ln_stream_t stream);
+
+ln_status ln_fwd_bias_dropout_keep_bf16(const ln_bf16* h, const ln_bf16* bias,
+                                        const ln_bf16* res, const ln_bf16* gamma,
+                                        const ln_bf16* beta, float eps, float p, uint64_t seed,
+                                        uint64_t offset, int64_t rows, int64_t cols,
+                                        ln_bf16* out, ln_bf16* res_out, float* mean, float* rstd,
+                                        uint8_t* keep, ln_stream_t stream);
+
+ln_status ln_dropout_bwd_keep_f32(const float* ds, float p, const uint8_t* keep, int64_t rows,
+                                  int64_t cols, float* dh, float* dbias, ln_stream_t stream);
+
+ln_status ln_dropout_bwd_keep_bf16(const ln_bf16* ds, float p, const uint8_t* keep,
+                                   int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                   ln_stream_t stream);
+
+ln_status ln_dropout_bwd_keep_f32_ws(const float* ds, float p, const uint8_t* keep,
+                                     int64_t rows, int64_t cols, float* dh, float* dbias,
+                                     void* workspace, size_t workspace_bytes, ln_stream_t stream);
+
+ln_status ln_dropout_bwd_keep_bf16_ws(const ln_bf16* ds, float p, const uint8_t* keep,
+                                      int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                      void* workspace, size_t workspace_bytes,
+                                      ln_stream_t stream);
 
 /*
  * Backward (bf16) that allocates nothing.  The pages have no counterpart to this entry

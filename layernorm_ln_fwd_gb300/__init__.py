@@ -72,6 +72,15 @@ SIGNATURES = {
     "ln_dropout_bwd_bf16": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P]),
     "ln_dropout_bwd_f32_ws": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "ln_dropout_bwd_bf16_ws": (_INT, [_P, _F, _U64, _U64, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "ln_dropout_keep_bytes": (_SZ, [_I64, _I64]),
+    "ln_fwd_bias_dropout_keep_f32": (_INT, [_P, _P, _P, _P, _P, _F, _F, _U64, _U64, _I64, _I64,
+                                            _P, _P, _P, _P, _P, _P]),
+    "ln_fwd_bias_dropout_keep_bf16": (_INT, [_P, _P, _P, _P, _P, _F, _F, _U64, _U64, _I64, _I64,
+                                             _P, _P, _P, _P, _P, _P]),
+    "ln_dropout_bwd_keep_f32": (_INT, [_P, _F, _P, _I64, _I64, _P, _P, _P]),
+    "ln_dropout_bwd_keep_bf16": (_INT, [_P, _F, _P, _I64, _I64, _P, _P, _P]),
+    "ln_dropout_bwd_keep_f32_ws": (_INT, [_P, _F, _P, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "ln_dropout_bwd_keep_bf16_ws": (_INT, [_P, _F, _P, _I64, _I64, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -367,11 +376,19 @@ def xent(logits, targets, alpha: float = 0.0, dloss: float = 1.0, losses=None, d
     return losses, dlogits
 
 
+def dropout_keep_bytes(rows: int, cols: int) -> int:
+    """Bytes of the stored keep bits of a [rows, cols] prologue: rows * ceil(cols / 8)."""
+    return int(lib().ln_dropout_keep_bytes(rows, cols))
+
+
 def fwd_bias_dropout(h, bias, res, gamma, beta, eps: float = 1e-5, p: float = 0.1, seed: int = 0,
-                     offset: int = 0, out=None, res_out=None, mean=None, rstd=None, stream=None):
+                     offset: int = 0, out=None, res_out=None, mean=None, rstd=None, keep=None,
+                     stream=None):
     """LayerNorm forward with the bias + dropout + residual prologue: s = res + keep * (h +
     bias) / (1 - p) (stored as res_out), then LN(s).  The dropout mask is a function of
-    (seed, offset, element index).  Returns (out, res_out, mean, rstd)."""
+    (seed, offset, element index); given ``keep`` (a uint8 tensor of
+    :func:`dropout_keep_bytes` bytes), the decisions are also stored there as bits, for
+    :func:`dropout_bwd`.  Returns (out, res_out, mean, rstd)."""
     import torch
     if h.dim() != 2:
         raise ValueError("h must be 2-D [rows, cols]")
@@ -388,18 +405,28 @@ def fwd_bias_dropout(h, bias, res, gamma, beta, eps: float = 1e-5, p: float = 0.
             else _need(mean, "mean", (rows,), torch.float32, dev))
     rstd = (torch.empty(rows, dtype=torch.float32, device=dev) if rstd is None
             else _need(rstd, "rstd", (rows,), torch.float32, dev))
-    name = f"ln_fwd_bias_dropout_{sfx}"
-    _check(name, getattr(lib(), name)(_ptr(h), _ptr(bias), _ptr(res), _ptr(gamma), _ptr(beta),
-                                      float(eps), float(p), int(seed), int(offset), rows, cols,
-                                      _ptr(out), _ptr(res_out), _ptr(mean), _ptr(rstd),
-                                      _stream(stream)))
+    args = [_ptr(h), _ptr(bias), _ptr(res), _ptr(gamma), _ptr(beta), float(eps), float(p),
+            int(seed), int(offset), rows, cols, _ptr(out), _ptr(res_out), _ptr(mean), _ptr(rstd)]
+    if keep is None:
+        name = f"ln_fwd_bias_dropout_{sfx}"
+    else:
+        name = f"ln_fwd_bias_dropout_keep_{sfx}"
+        args.append(_ptr(_keep_bytes(keep, rows, cols, dev)))
+    _check(name, getattr(lib(), name)(*args, _stream(stream)))
     return out, res_out, mean, rstd
 
 
-def dropout_bwd(ds, p: float, seed: int, offset: int, dh=None, dbias=None, workspace=None,
-                stream=None):
+def _keep_bytes(keep, rows, cols, dev):
+    import torch
+    return _need(keep, "keep", (dropout_keep_bytes(rows, cols),), torch.uint8, dev)
+
+
+def dropout_bwd(ds, p: float, seed: int = 0, offset: int = 0, dh=None, dbias=None,
+                workspace=None, keep=None, stream=None):
     """Backward of the prologue: dh = ds * keep / (1 - p), dbias = sum over rows of dh (ds:
-    the gradient with respect to s, i.e. :func:`bwd`'s dx).  Returns (dh, dbias)."""
+    the gradient with respect to s, i.e. :func:`bwd`'s dx); keep regenerated from (seed,
+    offset), or read from the bits a :func:`fwd_bias_dropout` call with ``keep`` stored.
+    Returns (dh, dbias)."""
     import torch
     if ds.dim() != 2:
         raise ValueError("ds must be 2-D [rows, cols]")
@@ -410,12 +437,16 @@ def dropout_bwd(ds, p: float, seed: int, offset: int, dh=None, dbias=None, works
     dh = torch.empty_like(ds) if dh is None else _need(dh, "dh", (rows, cols), dt, dev)
     dbias = (torch.empty(cols, dtype=dt, device=dev) if dbias is None
              else _need(dbias, "dbias", (cols,), dt, dev))
-    args = [_ptr(ds), float(p), int(seed), int(offset), rows, cols, _ptr(dh), _ptr(dbias)]
+    if keep is None:
+        kind, src = "", [int(seed), int(offset)]
+    else:
+        kind, src = "keep_", [_ptr(_keep_bytes(keep, rows, cols, dev))]
+    args = [_ptr(ds), float(p), *src, rows, cols, _ptr(dh), _ptr(dbias)]
     if workspace is None:
-        name = f"ln_dropout_bwd_{sfx}"
+        name = f"ln_dropout_bwd_{kind}{sfx}"
         _check(name, getattr(lib(), name)(*args, _stream(stream)))
     else:
         nbytes = workspace.numel() * workspace.element_size()
-        name = f"ln_dropout_bwd_{sfx}_ws"
+        name = f"ln_dropout_bwd_{kind}{sfx}_ws"
         _check(name, getattr(lib(), name)(*args, _ptr(workspace), nbytes, _stream(stream)))
     return dh, dbias

@@ -2,8 +2,10 @@
 //
 // The forward ("Accelerating Transformer on GPU (I)", section 2.3, fused into the LayerNorm
 // forward kernels) computes s = res + keep * (h + bias) / (1 - p) with keep regenerated from
-// a counter-based generator (Philox-4x32-10, see DropoutRng), so the backward needs no stored
-// mask.  Given ds, the gradient with respect to s (the LayerNorm backward's dx, which is also
+// a counter-based generator (Philox-4x32-10, see DropoutRng), so the backward can regenerate
+// it, or read the bits the forward stored while it decided (1 bit per element, rows padded
+// to whole bytes; "... (II)", section 3.2: the dropout backward needs the mask -- LightSeq
+// keeps one byte per element).  Given ds, the gradient with respect to s (the LayerNorm backward's dx, which is also
 // the residual's gradient):
 //   dh = ds * keep / (1 - p),   dbias = sum over rows of dh.
 // One cooperative launch.  A grid of (column tile) x (row segment) blocks of 256 threads
@@ -46,6 +48,8 @@ struct DbParams {
     uint64_t limit_ns;
     float scale;
     DropoutRng rng;
+    const uint8_t* keep;  // the forward's stored keep bits (rows padded to bytes), or null
+    int keep_stride;      // bytes per row of keep: ceil(cols / 8)
 };
 
 __device__ __forceinline__ void kahan_step(float& s, float& c, float x) {
@@ -57,23 +61,49 @@ __device__ __forceinline__ void kahan_step(float& s, float& c, float x) {
 
 // One 16-byte vector of ds (CV = Io<T>::kVec elements starting at element i0, i0 % CV == 0):
 // dh = keep ? ds * scale : 0, stored, and added to the thread's column sums.
-template <typename T, int CV>
-__device__ __forceinline__ uint4 drop_vec(const DbParams& p, const uint4& u, size_t i0,
-                                          float (&S)[CV], float (&C)[CV]) {
+// The stored keep bits of the CV (4 or 8) columns from col0 of `row` (col0 % CV == 0): a
+// byte, or half of one.
+template <int CV, bool BITS>
+__device__ __forceinline__ unsigned keep_bits_of(const DbParams& p, int row, int col0, size_t) {
+    static_assert(BITS, "the generator's decisions are compared in drop_vec");
+    const unsigned b = __ldg(p.keep + (size_t)row * p.keep_stride + (col0 >> 3));
+    return CV == 8 ? b : (b >> (col0 & 4)) & 0xFu;
+}
+
+template <bool BITS>
+__device__ __forceinline__ bool keep_one(const DbParams& p, int row, int col, size_t i) {
+    if constexpr (BITS)
+        return (__ldg(p.keep + (size_t)row * p.keep_stride + (col >> 3)) >> (col & 7)) & 1u;
+    else
+        return p.rng.keep(i);
+}
+
+template <typename T, int CV, bool BITS>
+__device__ __forceinline__ uint4 drop_vec(const DbParams& p, const uint4& u, int row, int col0,
+                                          size_t i0, float (&S)[CV], float (&C)[CV]) {
     using IO = Io<T>;
     float v[CV];
     IO::unpack(u, v);
-    uint32_t w[CV];
-    const uint4 wa = p.rng.words(i0 >> 2);
-    w[0] = wa.x; w[1] = wa.y; w[2] = wa.z; w[3] = wa.w;
-    if constexpr (CV == 8) {
-        const uint4 wb = p.rng.words((i0 >> 2) + 1);
-        w[4] = wb.x; w[5] = wb.y; w[6] = wb.z; w[7] = wb.w;
-    }
+    if constexpr (BITS) {
+        const unsigned kb = keep_bits_of<CV, true>(p, row, col0, i0);
 #pragma unroll
-    for (int k = 0; k < CV; ++k) {
-        v[k] = w[k] >= p.rng.thr ? __fmul_rn(v[k], p.scale) : 0.f;
-        kahan_step(S[k], C[k], v[k]);
+        for (int k = 0; k < CV; ++k) {
+            v[k] = (kb >> k) & 1u ? __fmul_rn(v[k], p.scale) : 0.f;
+            kahan_step(S[k], C[k], v[k]);
+        }
+    } else {  // the generator's words compared directly
+        uint32_t w[CV];
+        const uint4 wa = p.rng.words(i0 >> 2);
+        w[0] = wa.x; w[1] = wa.y; w[2] = wa.z; w[3] = wa.w;
+        if constexpr (CV == 8) {
+            const uint4 wb = p.rng.words((i0 >> 2) + 1);
+            w[4] = wb.x; w[5] = wb.y; w[6] = wb.z; w[7] = wb.w;
+        }
+#pragma unroll
+        for (int k = 0; k < CV; ++k) {
+            v[k] = w[k] >= p.rng.thr ? __fmul_rn(v[k], p.scale) : 0.f;
+            kahan_step(S[k], C[k], v[k]);
+        }
     }
     return IO::pack(v);
 }
@@ -81,7 +111,7 @@ __device__ __forceinline__ uint4 drop_vec(const DbParams& p, const uint4& u, siz
 // CV = Io<T>::kVec adjacent columns per thread with 16-byte accesses (cols % CV == 0 and
 // 16-byte aligned rows), or CV = 1 for any layout.  Column tiles are taken grid-stride, so
 // the widest rows still fit in one resident wave.
-template <typename T, int CV>
+template <typename T, int CV, bool BITS>
 __global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel(const DbParams p) {
     using IO = Io<T>;
     __shared__ float2 fold[kDbY][kDbX * CV];
@@ -109,13 +139,13 @@ __global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel
 #pragma unroll
                     for (int b = 0; b < kDbBatch; ++b) {
                         const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
-                        *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u[b], i0, S, C);
+                        *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV, BITS>(p, u[b], r + b * kDbY, col0, i0, S, C);
                     }
                 }
                 for (; r < r1; r += kDbY) {
                     const size_t i0 = (size_t)r * p.cols + col0;
                     const uint4 u = __ldcs(reinterpret_cast<const uint4*>(ds + i0));
-                    *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV>(p, u, i0, S, C);
+                    *reinterpret_cast<uint4*>(dh + i0) = drop_vec<T, CV, BITS>(p, u, r, col0, i0, S, C);
                 }
             } else {
                 for (; r + (kDbBatch - 1) * kDbY < r1; r += kDbBatch * kDbY) {
@@ -125,14 +155,14 @@ __global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel
 #pragma unroll
                     for (int b = 0; b < kDbBatch; ++b) {
                         const size_t i0 = (size_t)(r + b * kDbY) * p.cols + col0;
-                        const float w = p.rng.keep(i0) ? __fmul_rn(v[b], p.scale) : 0.f;
+                        const float w = keep_one<BITS>(p, r + b * kDbY, col0, i0) ? __fmul_rn(v[b], p.scale) : 0.f;
                         dh[i0] = IO::from_f(w);
                         kahan_step(S[0], C[0], w);
                     }
                 }
                 for (; r < r1; r += kDbY) {
                     const size_t i0 = (size_t)r * p.cols + col0;
-                    const float w = p.rng.keep(i0) ? __fmul_rn(IO::to_f(ds[i0]), p.scale) : 0.f;
+                    const float w = keep_one<BITS>(p, r, col0, i0) ? __fmul_rn(IO::to_f(ds[i0]), p.scale) : 0.f;
                     dh[i0] = IO::from_f(w);
                     kahan_step(S[0], C[0], w);
                 }
@@ -167,7 +197,10 @@ __global__ void __launch_bounds__(kDbThreads, kDbBlocksPerSm) dropout_bwd_kernel
 template <typename T>
 cudaError_t launch_db_t(DbParams p, bool vec, cudaStream_t stream) {
     constexpr int kVec = Io<T>::kVec;
-    const void* k1 = vec ? (const void*)dropout_bwd_kernel<T, kVec> : (const void*)dropout_bwd_kernel<T, 1>;
+    const void* k1 = p.keep ? (vec ? (const void*)dropout_bwd_kernel<T, kVec, true>
+                                   : (const void*)dropout_bwd_kernel<T, 1, true>)
+                            : (vec ? (const void*)dropout_bwd_kernel<T, kVec, false>
+                                   : (const void*)dropout_bwd_kernel<T, 1, false>);
     const int occ = std::max(1, blocks_per_sm(k1, kDbThreads, 0));
     const int slots = occ * device_info(-1).sms;  // blocks that can be resident at once
     const int gx = std::max(1, std::min(p.ctiles, slots / p.segs));
@@ -215,6 +248,8 @@ cudaError_t launch_dropout_bwd(Dtype dt, const DropoutBwdArgs& a, bool vec, cuda
     p.limit_ns = a.wait_limit_ns;
     p.scale = a.scale;
     p.rng = DropoutRng::make(a.seed, a.offset, a.thr);
+    p.keep = a.keep;
+    p.keep_stride = (a.cols + 7) / 8;
     cudaError_t e = dt == Dtype::F32 ? launch_db_t<float>(p, vec, stream)
                                      : launch_db_t<__nv_bfloat16>(p, vec, stream);
     if (e == cudaSuccess) *launches = 1;

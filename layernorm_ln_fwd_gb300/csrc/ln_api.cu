@@ -210,7 +210,7 @@ template <typename T>
 ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma, const T* beta,
                    float eps, int64_t rows, int64_t cols, T* out, T* res_out, float* mean,
                    float* rstd, ln_stream_t stream_, const T* bias = nullptr, float p = 0.f,
-                   uint64_t seed = 0, uint64_t offset = 0) {
+                   uint64_t seed = 0, uint64_t offset = 0, uint8_t* keep_out = nullptr) {
     t_last_launches = 0;
     if (!std::isfinite(eps) || eps < 0.f) return LN_EINVAL;
     ln_status st = check_sizes(rows, cols);
@@ -227,6 +227,8 @@ ln_status fwd_impl(Dtype dt, bool rms, const T* x, const T* res, const T* gamma,
         a.pro.bias = bias;
         a.pro.scale = 1.0f / (1.0f - p);
         a.pro.rng = DropoutRng::make(seed, offset, drop_threshold(p));
+        a.pro.keep_out = keep_out;
+        a.pro.keep_stride = (int)((cols + 7) / 8);
     }
     a.x = x;
     a.res = res;
@@ -385,7 +387,7 @@ namespace {
 template <typename T>
 ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64_t offset,
                            int64_t rows, int64_t cols, T* dh, T* dbias, void* ws, size_t ws_bytes,
-                           bool own_ws, ln_stream_t stream_) {
+                           bool own_ws, ln_stream_t stream_, const uint8_t* keep = nullptr) {
     t_last_launches = 0;
     if (!std::isfinite(p) || p < 0.f || p >= 1.f) return LN_EINVAL;
     ln_status st = check_sizes(rows, cols);
@@ -418,6 +420,7 @@ ln_status dropout_bwd_impl(Dtype dt, const T* ds, float p, uint64_t seed, uint64
     a.offset = offset;
     a.status = status_word();
     a.wait_limit_ns = wait_limit_ns();
+    a.keep = keep;
     int launches = 0;
     cudaError_t e = launch_dropout_bwd(dt, a, vec, stream, &launches);
     return finish_call(e, launches, stream);
@@ -652,6 +655,74 @@ ln_status ln_dropout_bwd_bf16_ws(const ln_bf16* ds, float p, uint64_t seed, uint
                                     rows, cols, reinterpret_cast<B*>(dh),
                                     reinterpret_cast<B*>(dbias), workspace, workspace_bytes, false,
                                     stream);
+}
+
+size_t ln_dropout_keep_bytes(int64_t rows, int64_t cols) {
+    if (lnk::check_sizes(rows, cols) != LN_OK) return 0;
+    return (size_t)rows * (size_t)((cols + 7) / 8);
+}
+
+ln_status ln_fwd_bias_dropout_keep_f32(const float* h, const float* bias, const float* res,
+                                       const float* gamma, const float* beta, float eps, float p,
+                                       uint64_t seed, uint64_t offset, int64_t rows, int64_t cols,
+                                       float* out, float* res_out, float* mean, float* rstd,
+                                       uint8_t* keep, ln_stream_t stream) {
+    if (!bias || (rows > 0 && (!res || !keep)) || !std::isfinite(p) || p < 0.f || p >= 1.f)
+        return LN_EINVAL;
+    return lnk::fwd_impl<float>(Dtype::F32, false, h, res, gamma, beta, eps, rows, cols, out,
+                                res_out, mean, rstd, stream, bias, p, seed, offset, keep);
+}
+
+ln_status ln_fwd_bias_dropout_keep_bf16(const ln_bf16* h, const ln_bf16* bias,
+                                        const ln_bf16* res, const ln_bf16* gamma,
+                                        const ln_bf16* beta, float eps, float p, uint64_t seed,
+                                        uint64_t offset, int64_t rows, int64_t cols,
+                                        ln_bf16* out, ln_bf16* res_out, float* mean, float* rstd,
+                                        uint8_t* keep, ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    if (!bias || (rows > 0 && (!res || !keep)) || !std::isfinite(p) || p < 0.f || p >= 1.f)
+        return LN_EINVAL;
+    return lnk::fwd_impl<B>(Dtype::BF16, false, reinterpret_cast<const B*>(h),
+                            reinterpret_cast<const B*>(res), reinterpret_cast<const B*>(gamma),
+                            reinterpret_cast<const B*>(beta), eps, rows, cols,
+                            reinterpret_cast<B*>(out), reinterpret_cast<B*>(res_out), mean, rstd,
+                            stream, reinterpret_cast<const B*>(bias), p, seed, offset, keep);
+}
+
+ln_status ln_dropout_bwd_keep_f32(const float* ds, float p, const uint8_t* keep, int64_t rows,
+                                  int64_t cols, float* dh, float* dbias, ln_stream_t stream) {
+    if (rows > 0 && !keep) return LN_EINVAL;
+    return lnk::dropout_bwd_impl<float>(Dtype::F32, ds, p, 0, 0, rows, cols, dh, dbias, nullptr,
+                                        0, true, stream, keep);
+}
+
+ln_status ln_dropout_bwd_keep_bf16(const ln_bf16* ds, float p, const uint8_t* keep,
+                                   int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                   ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    if (rows > 0 && !keep) return LN_EINVAL;
+    return lnk::dropout_bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(ds), p, 0, 0, rows,
+                                    cols, reinterpret_cast<B*>(dh), reinterpret_cast<B*>(dbias),
+                                    nullptr, 0, true, stream, keep);
+}
+
+ln_status ln_dropout_bwd_keep_f32_ws(const float* ds, float p, const uint8_t* keep,
+                                     int64_t rows, int64_t cols, float* dh, float* dbias,
+                                     void* workspace, size_t workspace_bytes, ln_stream_t stream) {
+    if (rows > 0 && !keep) return LN_EINVAL;
+    return lnk::dropout_bwd_impl<float>(Dtype::F32, ds, p, 0, 0, rows, cols, dh, dbias, workspace,
+                                        workspace_bytes, false, stream, keep);
+}
+
+ln_status ln_dropout_bwd_keep_bf16_ws(const ln_bf16* ds, float p, const uint8_t* keep,
+                                      int64_t rows, int64_t cols, ln_bf16* dh, ln_bf16* dbias,
+                                      void* workspace, size_t workspace_bytes,
+                                      ln_stream_t stream) {
+    using B = __nv_bfloat16;
+    if (rows > 0 && !keep) return LN_EINVAL;
+    return lnk::dropout_bwd_impl<B>(Dtype::BF16, reinterpret_cast<const B*>(ds), p, 0, 0, rows,
+                                    cols, reinterpret_cast<B*>(dh), reinterpret_cast<B*>(dbias),
+                                    workspace, workspace_bytes, false, stream, keep);
 }
 
 ln_status ln_device_check(ln_stream_t stream_) {

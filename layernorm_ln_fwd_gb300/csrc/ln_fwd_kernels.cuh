@@ -64,11 +64,11 @@ __device__ __forceinline__ float warp_sum1(float a) {
 
 // The prologue of one 16-byte vector: s = res + keep * (x + bias) * scale for the V elements
 // starting at element index i0 (a multiple of 4), rounded to the I/O type.  Dropped elements
-// take res itself.
+// take res itself.  kb returns the V keep decisions as bits (bit k: element i0 + k).
 template <typename T>
 __device__ __forceinline__ uint4 prologue_vec(const uint4& xv, const uint4& rv, const uint4& bv,
                                               const DropoutRng& rng, float scale,
-                                              unsigned long long i0) {
+                                              unsigned long long i0, unsigned& kb) {
     using PR = Pairs<T>;
     constexpr int H = PR::kPairs;
     f2 hv[H], r2[H], bias[H], o[H];
@@ -84,14 +84,33 @@ __device__ __forceinline__ uint4 prologue_vec(const uint4& xv, const uint4& rv, 
         w[4] = wb.x; w[5] = wb.y; w[6] = wb.z; w[7] = wb.w;
     }
     const f2 sc = f2_splat(scale);
+    kb = 0;
 #pragma unroll
     for (int h = 0; h < H; ++h) {
+        const bool k0 = w[2 * h] >= rng.thr, k1 = w[2 * h + 1] >= rng.thr;
+        kb |= (k0 ? 1u : 0u) << (2 * h) | (k1 ? 1u : 0u) << (2 * h + 1);
         const f2 t = f2_mul(f2_add(hv[h], bias[h]), sc);
-        const f2 kt = f2_make(w[2 * h] >= rng.thr ? f2_lo(t) : 0.f,
-                              w[2 * h + 1] >= rng.thr ? f2_hi(t) : 0.f);
+        const f2 kt = f2_make(k0 ? f2_lo(t) : 0.f, k1 ? f2_hi(t) : 0.f);
         o[h] = f2_add(r2[h], kt);
     }
     return PR::pack(o);
+}
+
+// Stores vector vi's keep bits kb (0 for a lane past the row's end) in the prologue's bit
+// mask: one byte per 8 columns, rows padded to whole bytes.  An fp32 vector holds 4 columns,
+// half a byte: the even lane of each pair of lanes (vectors vi and vi + 1, which adjacent
+// lanes hold) writes both halves.  Every lane of the warp calls it (the exchange is a
+// shuffle).
+template <typename T>
+__device__ __forceinline__ void store_keep_bits(const Prologue& pro, int row, int vi, bool valid,
+                                                unsigned kb) {
+    uint8_t* dst = pro.keep_out + (size_t)row * pro.keep_stride;
+    if constexpr (Io<T>::kVec == 8) {
+        if (valid) dst[vi] = (uint8_t)kb;
+    } else {
+        const unsigned hi = __shfl_xor_sync(kFullMask, kb, 1);
+        if (valid && (vi & 1) == 0) dst[vi >> 1] = (uint8_t)(kb | (hi << 4));
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -106,7 +125,7 @@ __device__ __forceinline__ uint4 prologue_vec(const uint4& xv, const uint4& rv, 
 // completes when its copies land; the empty barrier when all consumer warps are done.
 // The bytes in flight per SM are set by the ring, not by the registers of resident warps.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPL, bool HAS_RES, bool RMS, bool PRO = false>
+template <typename T, int VPL, bool HAS_RES, bool RMS, int PRO = 0>
 __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
     fwd_tile_kernel(const T* __restrict__ x, const T* __restrict__ res,
                     const T* __restrict__ gamma, const T* __restrict__ beta, float eps, int rows,
@@ -193,27 +212,38 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
             const T* rsm = xs + (size_t)kTileRows * cols;
             // s = x + res, rounded to the stored type (one packed add per pair for bf16), or
             // the prologue's res + keep * (x + bias) * scale; it is what gets normalised.
-            auto s_vec = [&](int v) {
+            auto s_vec_kb = [&](int v, unsigned& kb) {
                 const int vi = v * 32 + lane;
                 const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
                 if constexpr (PRO)
                     return prologue_vec<T>(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V),
                                            ld_keep(bptr + (size_t)vi * V), rng, pro.scale,
-                                           base + (size_t)vi * V);
+                                           base + (size_t)vi * V, kb);
                 else
                     return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
                                    : xv;
             };
+            auto s_vec = [&](int v) {
+                unsigned kb;
+                return s_vec_kb(v, kb);
+            };
             uint4 sp[VPL];
+            unsigned kbv[VPL];
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
                 const int vi = v * 32 + lane;
+                kbv[v] = 0;
                 if (vi < nvec) {
-                    sp[v] = s_vec(v);
+                    sp[v] = s_vec_kb(v, kbv[v]);
                     if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
                 } else {
                     sp[v] = make_uint4(0, 0, 0, 0);
                 }
+            }
+            if constexpr (PRO == 2) {
+#pragma unroll
+                for (int v = 0; v < VPL; ++v)
+                    store_keep_bits<T>(pro, row, v * 32 + lane, v * 32 + lane < nvec, kbv[v]);
             }
             if constexpr (RMS) {
                 // Sum of squares (the low halves of the pairs take the even columns, the high
@@ -309,7 +339,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
 // (end-of-row barrier) it refills that slot with the row `stages` iterations ahead.
 // Thread t of the block owns vectors t, t + blockDim.x, ... of every row.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPT, bool HAS_RES, bool RMS, bool PRO = false>
+template <typename T, int VPT, bool HAS_RES, bool RMS, int PRO = 0>
 __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
     fwd_block_kernel(const T* __restrict__ x, const T* __restrict__ res,
                      const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
@@ -390,28 +420,39 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
         const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes);
         const T* rsm = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes + row_bytes);
         const size_t base = (size_t)row * cols;
-        auto s_vec = [&](int v) {
+        auto s_vec_kb = [&](int v, unsigned& kb) {
             const int vi = v * nthreads + tid;
             const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
             if constexpr (PRO)
                 return prologue_vec<T>(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V),
                                        ld_keep(bptr + (size_t)vi * V), rng, pro.scale,
-                                       base + (size_t)vi * V);
+                                       base + (size_t)vi * V, kb);
             else
                 return HAS_RES ? IO::add_round(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V))
                                : xv;
         };
+        auto s_vec = [&](int v) {
+            unsigned kb;
+            return s_vec_kb(v, kb);
+        };
 
         uint4 sp[VPT];
+        unsigned kbv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int vi = v * nthreads + tid;
+            kbv[v] = 0;
             if (vi < nvec) {
-                sp[v] = s_vec(v);
+                sp[v] = s_vec_kb(v, kbv[v]);
                 if (write_res) st_stream(res_out + base + (size_t)vi * V, sp[v]);
             } else {
                 sp[v] = make_uint4(0, 0, 0, 0);
             }
+        }
+        if constexpr (PRO == 2) {  // nthreads is a multiple of 32: adjacent lanes, adjacent vectors
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                store_keep_bits<T>(pro, row, v * nthreads + tid, v * nthreads + tid < nvec, kbv[v]);
         }
         if constexpr (RMS) {
             f2 sv[VPT][H];
@@ -444,9 +485,10 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
             // shared memory).  The low halves of the pairs sum the even columns, the high
             // halves the odd ones.
             // (With the prologue every thread recomputes s of the first vector.)
+            unsigned kb0;
             const uint4 first = PRO ? prologue_vec<T>(*reinterpret_cast<const uint4*>(xs),
                                                       *reinterpret_cast<const uint4*>(rsm),
-                                                      ld_keep(bptr), rng, pro.scale, base)
+                                                      ld_keep(bptr), rng, pro.scale, base, kb0)
                                 : HAS_RES ? IO::add_round(*reinterpret_cast<const uint4*>(xs),
                                                           *reinterpret_cast<const uint4*>(rsm))
                                           : *reinterpret_cast<const uint4*>(xs);
@@ -527,7 +569,7 @@ __global__ void __launch_bounds__(kFwdBlockMaxThreads, 1)
 // pairwise (Welford/Chan), with the plain sum of s alongside for the stored mean.  RMSNorm:
 // per-thread sums of squares.
 // ---------------------------------------------------------------------------------------
-template <typename T, bool HAS_RES, bool RMS, bool PRO = false>
+template <typename T, bool HAS_RES, bool RMS, int PRO = 0>
 __global__ void __launch_bounds__(kFwdScalarThreads)
     fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ res,
                       const T* __restrict__ gamma, const T* __restrict__ beta, float eps,
@@ -551,14 +593,20 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
     for (int row = blockIdx.x; row < rows; row += gridDim.x) {
         const size_t base = (size_t)row * cols;
         const DropoutRng& rng = pro.rng;
-        auto load_s = [&](int j) -> float {
+        auto load_s_k = [&](int j, bool& kept) -> float {
             float v = IO::to_f(x[base + j]);
+            kept = true;
             if constexpr (PRO) {
                 const float t = (v + IO::to_f(static_cast<const T*>(pro.bias)[j])) * pro.scale;
-                return IO::round(IO::to_f(res[base + j]) + (rng.keep(base + j) ? t : 0.f));
+                kept = rng.keep(base + j);
+                return IO::round(IO::to_f(res[base + j]) + (kept ? t : 0.f));
             }
             if (HAS_RES) v = IO::round(v + IO::to_f(res[base + j]));
             return v;
+        };
+        auto load_s = [&](int j) -> float {
+            bool kept;
+            return load_s_k(j, kept);
         };
         if constexpr (RMS) {
             float ss = 0.f;
@@ -586,8 +634,19 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
             // mean and M2 of d = s - K.
             float S = 0.f, md = 0.f, M2 = 0.f, n = 0.f;
             for (int j = tid; j < cols; j += kFwdScalarThreads) {
-                const float sv = load_s(j);
+                bool kept;
+                const float sv = load_s_k(j, kept);
                 if (write_res) res_out[base + j] = IO::from_f(sv);
+                if constexpr (PRO == 2) {  // the warp's 32 columns j0 .. j0 + 31, by ballot
+                    const int j0 = j - lane;
+                    const unsigned m = cols - j0 >= 32 ? kFullMask : (1u << (cols - j0)) - 1u;
+                    const unsigned bits = __ballot_sync(m, kept);
+                    if (lane == 0) {
+                        uint8_t* dst = pro.keep_out + (size_t)row * pro.keep_stride + j0 / 8;
+                        const int nb = min(4, (cols - j0 + 7) / 8);
+                        for (int q = 0; q < nb; ++q) dst[q] = (uint8_t)(bits >> (8 * q));
+                    }
+                }
                 S = __fadd_rn(S, sv);
                 const float d = __fsub_rn(sv, K);
                 n = __fadd_rn(n, 1.f);
@@ -636,24 +695,24 @@ __global__ void __launch_bounds__(kFwdScalarThreads)
 // ---------------------------------------------------------------------------------------
 // The kernel of a family for a residual (or not); the prologue always has a residual, and
 // its instantiations exist only in that form.
-template <typename T, int N, bool RMS, bool PRO>
+template <typename T, int N, bool RMS, int PRO>
 const void* tile_ptr(bool has_res) {
     if constexpr (PRO)
-        return (const void*)fwd_tile_kernel<T, N, true, RMS, true>;
+        return (const void*)fwd_tile_kernel<T, N, true, RMS, PRO>;
     else
-        return has_res ? (const void*)fwd_tile_kernel<T, N, true, RMS, false>
-                       : (const void*)fwd_tile_kernel<T, N, false, RMS, false>;
+        return has_res ? (const void*)fwd_tile_kernel<T, N, true, RMS, 0>
+                       : (const void*)fwd_tile_kernel<T, N, false, RMS, 0>;
 }
-template <typename T, int N, bool RMS, bool PRO>
+template <typename T, int N, bool RMS, int PRO>
 const void* block_ptr(bool has_res) {
     if constexpr (PRO)
-        return (const void*)fwd_block_kernel<T, N, true, RMS, true>;
+        return (const void*)fwd_block_kernel<T, N, true, RMS, PRO>;
     else
-        return has_res ? (const void*)fwd_block_kernel<T, N, true, RMS, false>
-                       : (const void*)fwd_block_kernel<T, N, false, RMS, false>;
+        return has_res ? (const void*)fwd_block_kernel<T, N, true, RMS, 0>
+                       : (const void*)fwd_block_kernel<T, N, false, RMS, 0>;
 }
 
-template <bool RMS, bool PRO, typename T>
+template <bool RMS, int PRO, typename T>
 cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     const void* kern = nullptr;
     const bool has_res = a.res != nullptr;
@@ -705,7 +764,7 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     return launch_kernel(kern, dim3(grid), dim3(kTileThreads), smem, stream, args, false);
 }
 
-template <bool RMS, bool PRO, typename T>
+template <bool RMS, int PRO, typename T>
 cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
     const int nvec = a.cols / V;
@@ -782,15 +841,15 @@ cudaError_t launch_block(const FwdArgs& a, cudaStream_t stream) {
     return launch_kernel(kern, dim3(grid), dim3(threads), smem, stream, args, false);
 }
 
-template <bool RMS, bool PRO, typename T>
+template <bool RMS, int PRO, typename T>
 cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     const bool has_res = a.res != nullptr;
     const void* kern;
     if constexpr (PRO)
-        kern = (const void*)fwd_scalar_kernel<T, true, RMS, true>;
+        kern = (const void*)fwd_scalar_kernel<T, true, RMS, PRO>;
     else
-        kern = has_res ? (const void*)fwd_scalar_kernel<T, true, RMS, false>
-                       : (const void*)fwd_scalar_kernel<T, false, RMS, false>;
+        kern = has_res ? (const void*)fwd_scalar_kernel<T, true, RMS, 0>
+                       : (const void*)fwd_scalar_kernel<T, false, RMS, 0>;
     const DeviceInfo& di = device_info(-1);
     const int occ = std::max(1, blocks_per_sm(kern, kFwdScalarThreads, 0));
     const int grid = std::max(1, std::min(a.rows, di.sms * occ));
@@ -809,7 +868,7 @@ cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     return launch_kernel(kern, dim3(grid), dim3(kFwdScalarThreads), 0, stream, args, false);
 }
 
-template <bool RMS, bool PRO, typename T>
+template <bool RMS, int PRO, typename T>
 cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
     if (!aligned || path == kPathScalar) return launch_scalar<RMS, PRO, T>(a, stream);
@@ -821,7 +880,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t 
 }
 
 // The forward of a LayerNorm (RMS = false) or an RMSNorm (RMS = true): one kernel launch.
-template <bool RMS, bool PRO = false>
+template <bool RMS, int PRO = 0>
 cudaError_t launch_norm_fwd(Dtype dt, const FwdArgs& a, bool aligned, int path_override,
                             cudaStream_t stream, int* launches) {
     *launches = 0;

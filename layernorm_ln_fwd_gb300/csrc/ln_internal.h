@@ -36,6 +36,10 @@ struct Prologue {
     const void* bias = nullptr;
     float scale = 1.f;
     DropoutRng rng{};
+    // Optional: the keep decisions also stored as bits, rows padded to whole bytes: bit
+    // (c % 8) of keep_out[row * keep_stride + c / 8] for column c, keep_stride = ceil(cols / 8).
+    uint8_t* keep_out = nullptr;
+    int keep_stride = 0;
 };
 
 struct FwdArgs {
@@ -174,8 +178,8 @@ struct XentArgs {
 cudaError_t launch_xent(Dtype dt, const XentArgs& a, bool aligned, cudaStream_t stream,
                         int* launches);
 
-// Backward of the bias + dropout + residual prologue: dh = ds * keep * scale and the
-// deterministic column sums dbias (partials: [segs][cols] (hi, lo) fp32 pairs that announce
+// Backward of the bias + dropout + residual prologue: dh = ds * keep * scale (keep from the
+// generator, or from the bits the forward stored) and the deterministic column sums dbias (partials: [segs][cols] (hi, lo) fp32 pairs that announce
 // themselves, left zero), in one cooperative launch.
 struct DropoutBwdArgs {
     const void* ds;
@@ -188,6 +192,7 @@ struct DropoutBwdArgs {
     unsigned long long seed, offset;
     unsigned* status;          // the per-device status word (bounded waits)
     uint64_t wait_limit_ns;
+    const uint8_t* keep = nullptr;  // stored keep bits (Prologue::keep_out's layout), or null
 };
 
 // Whether the kernels take 16-byte vectors (rows of whole vectors, aligned pointers).

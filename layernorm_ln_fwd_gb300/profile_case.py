@@ -6,7 +6,7 @@
 
 Workloads are the LayerNorm ones of ``synth.WORKLOADS`` and the other fused row operations
 of ``synth.OP_WORKLOADS`` (RMSNorm, softmax, cross-entropy, the bias + dropout + residual
-prologue), with the seeded synthetic inputs of ``synth`` (``--rows`` keeps the workload's
+prologue, its mask regenerated or stored as bits), with the seeded synthetic inputs of ``synth`` (``--rows`` keeps the workload's
 width, dtype and distributions and takes fewer or more rows, for captures that must stay
 small or spill out of L2); backwards use a caller-owned workspace, as the benchmark does.
 Nothing is checked.
@@ -44,8 +44,10 @@ def op_case(name: str, rows: int, iters: int) -> None:
     if kind == "xent":
         t = torch.randint(0, C, (R,), generator=torch.Generator(device="cuda").manual_seed(0),
                           device="cuda", dtype=torch.int32)
-    if kind == "bdr":
+    if kind in ("bdr", "bdr_keep"):
         bias = (0.1 * d["beta"].float()).to(d["beta"].dtype)
+        keep = (torch.empty(ln.dropout_keep_bytes(R, C), dtype=torch.uint8, device="cuda")
+                if kind == "bdr_keep" else None)
     for i in range(iters):
         if kind == "rms":
             out, res_out, rrms = ln.rms_fwd(d["x"], d["res"], d["gamma"], 1e-5)
@@ -57,8 +59,9 @@ def op_case(name: str, rows: int, iters: int) -> None:
             ln.xent(d["x"], t, op["alpha"], 1.0 / R)
         else:
             out, res_out, mean, rstd = ln.fwd_bias_dropout(d["x"], bias, d["res"], d["gamma"],
-                                                           d["beta"], 1e-5, op["p"], 17, i)
-            ln.dropout_bwd(d["dy"], op["p"], 17, i, workspace=ws)
+                                                           d["beta"], 1e-5, op["p"], 17, i,
+                                                           keep=keep)
+            ln.dropout_bwd(d["dy"], op["p"], 17, i, workspace=ws, keep=keep)
 
 
 def main() -> int:

@@ -125,6 +125,8 @@ OP_WORKLOADS = {
     # bias + dropout + residual prologue of the LayerNorm forward at the GPT-2 small shape,
     # p = 0.1 ("Accelerating Transformer on GPU (I)", section 2.3).
     "bdr_bf16_8192x768": dict(kind="bdr", dtype="bf16", rows=8192, cols=768, p=0.1),
+    # the same with the keep decisions stored as bits by the forward, read by the backward
+    "bdr_keep_bf16_8192x768": dict(kind="bdr_keep", dtype="bf16", rows=8192, cols=768, p=0.1),
 }
 
 

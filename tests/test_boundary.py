@@ -103,6 +103,23 @@ def test_invalid_arguments_are_rejected_on_the_host(lib):
     assert lib.ln_rms_fwd_f32(NULL, NULL, NULL, 1e-5, 0, 4, NULL, NULL, NULL, NULL) == 0
 
 
+def test_stored_keep_bits_calls_are_checked_on_the_host(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.ln_dropout_keep_bytes(4, 9) == 8  # rows padded to whole bytes
+    assert lib.ln_dropout_keep_bytes(3, 16) == 6
+    assert lib.ln_dropout_keep_bytes(4, 0) == 0
+    assert lib.ln_dropout_keep_bytes(-1, 8) == 0
+    # A missing keep buffer, or a bad p, is refused before anything is launched.
+    assert lib.ln_fwd_bias_dropout_keep_f32(p, p, p, p, p, 1e-5, 0.1, 1, 2, 4, 8, p, p, p, p,
+                                            NULL, NULL) == 1
+    assert lib.ln_fwd_bias_dropout_keep_bf16(p, p, p, p, p, 1e-5, 1.0, 1, 2, 4, 8, p, p, p, p,
+                                             p, NULL) == 1
+    assert lib.ln_dropout_bwd_keep_f32(p, 0.1, NULL, 4, 8, p, p, NULL) == 1
+    assert lib.ln_dropout_bwd_keep_bf16_ws(p, 0.1, p, 4, 8, p, p, ctypes.c_void_p(272), 1 << 20,
+                                           NULL) == 2
+    assert lib.ln_last_launch_count() == 0
+
+
 def test_force_path_hook_round_trips(lib):
     prev = lib.ln_debug_force_path(ln.PATH_SCALAR)
     assert lib.ln_debug_force_path(ln.PATH_AUTO) == ln.PATH_SCALAR

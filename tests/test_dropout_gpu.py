@@ -134,3 +134,85 @@ def test_invalid_arguments():
         ln.fwd_bias_dropout(x, b, x, b, b, EPS, 1.0, 0, 0)
     with pytest.raises(ln.LnError):
         ln.dropout_bwd(x, -0.1, 0, 0)
+
+
+# ---------------------------------------------------------------------------------------
+# The keep decisions stored as bits by the forward and read by the backward.
+
+def oracle_keep_bytes(seed, offset, p, rows, cols):
+    """The oracle's mask packed as the library stores it: bit (c % 8) of byte
+    [row, c // 8], rows padded to whole bytes with zero bits."""
+    m = oracle.dropout_mask(seed, offset, p, rows, cols).astype(np.uint8)
+    return np.packbits(m, axis=1, bitorder="little")
+
+
+@pytest.mark.parametrize("dtype,rows,cols,path", [
+    ("bf16", 300, 768, ln.PATH_AUTO),      # warp per row
+    ("bf16", 37, 4104, ln.PATH_AUTO),      # block per row
+    ("bf16", 300, 1001, ln.PATH_AUTO),     # scalar (not 16-byte rows)
+    ("bf16", 5, 8, ln.PATH_AUTO),          # one vector per row
+    ("f32", 64, 1000, ln.PATH_AUTO),       # fp32: two lanes share a byte
+    ("f32", 7, 1004, ln.PATH_AUTO),        # an odd number of vectors per row
+    ("f32", 9, 4104, ln.PATH_AUTO),        # fp32 block per row
+    ("f32", 37, 768, ln.PATH_BLOCK),
+    ("bf16", 37, 768, ln.PATH_SCALAR),
+])
+def test_forward_stores_the_oracle_decisions(dtype, rows, cols, path):
+    p, seed, offset = 0.25, 2 ** 36 + 9, 1000 + rows
+    inp = synth.make_inputs(rows, cols, dtype, seed=cols)
+    bias = synth.make_inputs(1, cols, dtype, seed=3, x=("normal", 0.0, 0.1))["x"][0].cuda()
+    d = P.to_device(inp)
+    keep = torch.full((ln.dropout_keep_bytes(rows, cols),), 0xAA, dtype=torch.uint8, device="cuda")
+    ln.force_path(path)
+    a = ln.fwd_bias_dropout(d["x"], bias, d["res"], d["gamma"], d["beta"], EPS, p, seed, offset)
+    b = ln.fwd_bias_dropout(d["x"], bias, d["res"], d["gamma"], d["beta"], EPS, p, seed, offset,
+                            keep=keep)
+    torch.cuda.synchronize()
+    got = keep.cpu().numpy().reshape(rows, (cols + 7) // 8)
+    np.testing.assert_array_equal(got, oracle_keep_bytes(seed, offset, p, rows, cols))
+    for k in range(4):  # storing the bits changes nothing else
+        assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(300, 768), (300, 1001), (8192, 768), (7, 1004)])
+def test_backward_from_stored_bits_is_the_generator_backward(dtype, rows, cols):
+    if dtype == "bf16" and cols == 1004:
+        cols = 1000
+    p, seed, offset = 0.1, 5, 17
+    inp = synth.make_inputs(rows, cols, dtype, seed=7)
+    d = P.to_device(inp)
+    bias = torch.zeros(cols, dtype=d["x"].dtype, device="cuda")
+    keep = torch.empty(ln.dropout_keep_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    ln.fwd_bias_dropout(d["x"], bias, d["res"], d["gamma"], d["beta"], EPS, p, seed, offset,
+                        keep=keep)
+    a = ln.dropout_bwd(d["dy"], p, seed, offset)
+    b = ln.dropout_bwd(d["dy"], p, keep=keep)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    ref = oracle.dropout_bwd(P.to64(d["dy"]), p, seed, offset, io=dtype)
+    P.compare("dx", P.to64(b[0]), ref["dh"], dtype)
+
+
+def test_stored_bits_path_full_size_gpt2_small():
+    """8192 x 768 bf16, p = 0.1: forward storing the bits, backward reading them, against the
+    oracle; the workspace is left zero."""
+    rows, cols, p, seed, offset = 8192, 768, 0.1, 1234, 0
+    inp = synth.make_inputs(rows, cols, "bf16", seed=rows + cols)
+    bias = synth.make_inputs(1, cols, "bf16", seed=3, x=("normal", 0.0, 0.1))["x"][0]
+    d = P.to_device(inp)
+    keep = torch.empty(ln.dropout_keep_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ln.workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+    out, res_out, mean, rstd = ln.fwd_bias_dropout(d["x"], bias.cuda(), d["res"], d["gamma"],
+                                                   d["beta"], EPS, p, seed, offset, keep=keep)
+    dh, dbias = ln.dropout_bwd(d["dy"], p, keep=keep, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(torch.count_nonzero(ws)) == 0
+    keepm = oracle.dropout_mask(seed, offset, p, rows, cols).astype(bool)
+    np.testing.assert_array_equal(P.to64(res_out)[~keepm], P.to64(inp["res"])[~keepm])
+    b = oracle.dropout_bwd(P.to64(d["dy"]), p, seed, offset, io="bf16")
+    assert P.compare("dx", P.to64(dh), b["dh"], "bf16")["n_over_stated"] == 0
+    terms = keepm * P.to64(d["dy"]) / (1 - p)
+    allow = 36.0 * 2.0 ** -24 * np.sqrt((terms ** 2).sum(axis=0))
+    P.compare("dbeta", P.to64(dbias), b["dbias"], "bf16", extra=allow)
+
