@@ -59,6 +59,22 @@ namespace {
 // allocated to warps in groups of four (a 9-warp block would pay for 12).
 constexpr int kTileRows = 7;
 constexpr int kTileThreads = (kTileRows + 1) * 32;
+
+// Rows per tile of the tile kernel with W warps per row (rows wider than one warp's share
+// of registers).  One block per SM; its consumer warps + the producer are as many as the
+// registers allow: a thread keeps gamma and the column sums of VPL vectors (H fp32 pairs
+// each; the sums compensated when KAHAN) plus ~56 registers of working state, and warps
+// are paid for in fours.
+__host__ __device__ constexpr int tile_rows_for(int H, int vpl, bool kahan, int W) {
+    if (W == 1) return kTileRows;
+    const int regs = 2 * (kahan ? 5 : 3) * vpl * H + 56;
+    const int warps = (65536 / (32 * ((regs + 7) / 8 * 8))) / 4 * 4;
+    return (warps - 1) / W > 1 ? (warps - 1) / W : 1;
+}
+template <typename T, int VPL, bool KAHAN, int W>
+constexpr int tile_threads() {
+    return (tile_rows_for(Pairs<T>::kPairs, VPL, KAHAN, W) * W + 1) * 32;
+}
 constexpr int kBwdBlockMaxThreads = 512;
 constexpr int kBwdScalarThreads = 256;
 constexpr int kMaxStages = 8;
@@ -177,13 +193,19 @@ __global__ void __launch_bounds__(kFinThreads) bwd_finish_kernel(const KParams a
 
 // ---------------------------------------------------------------------------------------
 // Warp per row, fed by a bulk-copy (TMA) pipeline (the forward's tile kernel, for dy and x).
-// The block owns a fixed set of tiles (7 consecutive rows each, every G-th); the producer
+// The block owns a fixed set of tiles (RT consecutive rows each, every G-th); the producer
 // warp's lane 0 fetches each tile of dy and of x with one cp.async.bulk apiece, `stages`
 // tiles ahead; consumer warp w handles row w of every tile.  Lane l owns the columns of
 // vectors l, l+32, ... in every row, so its column sums stay in registers (Kahan-compensated
-// when KAHAN, for fp32 I/O and for long chains of rows); at the end the 7 consumer warps'
+// when KAHAN, for fp32 I/O and for long chains of rows); at the end the consumer warps'
 // sums are added in warp order with TwoSum through shared memory (the drained ring) into
 // the block's (hi, lo) partial row.
+// Rows too wide for one warp's registers (W = 2 or 4): W warps share each row of the tile,
+// lane l of warp p taking vectors (v * W + p) * 32 + l, and add their two row sums in warp
+// order after exchanging them through shared memory (each warp announces its pair on an
+// mbarrier; bounded waits).  The block then keeps RT rows in flight at once instead of one
+// (the block-per-row kernel): bf16 8192 x 2560 backward 44.0 -> 31.7 us, 8192 x 2048
+// 28.0 -> 23.4 us, fp32 8192 x 1280 41.3 -> 28.9 us, measured on GB300.
 // ---------------------------------------------------------------------------------------
 // Two blocks per SM when the per-lane state (gamma, column sums and their compensations,
 // in fp32 pairs) leaves room: at most 128 registers per thread.
@@ -192,18 +214,30 @@ constexpr int tile_min_blocks() {
     return (KAHAN ? 5 : 3) * VPL * Pairs<T>::kPairs <= 36 ? 2 : 1;
 }
 
-template <typename T, int VPL, bool KAHAN, bool RMS>
-__global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>())
+template <typename T, int VPL, bool KAHAN, bool RMS, int W = 1>
+__global__ void __launch_bounds__(tile_threads<T, VPL, KAHAN, W>(),
+                                  W == 1 ? tile_min_blocks<T, VPL, KAHAN>() : 1)
     bwd_tile_kernel(const KParams a) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
+    // RT rows per tile, W warps per row: consumer warp c takes row c / W of every tile and,
+    // in it, the vectors (v * W + c % W) * 32 + lane.
+    constexpr int RT = tile_rows_for(Pairs<T>::kPairs, VPL, KAHAN, W);
+    constexpr int NCW = RT * W;  // consumer warps; warp NCW is the producer
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+    // W > 1: the W warps of a row exchange their two row sums through xval, announced on
+    // xbar (one barrier per row of the tile, double-buffered by step parity).
+    __shared__ uint64_t xbar[W > 1 ? 2 * RT : 1];
+    __shared__ float2 xval[W > 1 ? 2 * RT * W : 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wrow = warp / W, wpos = warp - wrow * W;  // row of the tile, place in the row
+    const int lane_vec = wpos * 32 + lane;              // this lane's first vector of a row
+    constexpr int VSTRIDE = 32 * W;                     // between a lane's vectors
     const int cols = a.cols, nvec = cols / V, stages = a.stages, rows = a.rows;
     const RowDivisor rdiv(cols);
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
-    const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
+    const unsigned tile_bytes = (unsigned)RT * row_bytes;
     const unsigned slot_bytes = 2u * tile_bytes;
     const T* __restrict__ dy = static_cast<const T*>(a.dy);
     const T* __restrict__ xr = static_cast<const T*>(a.xr);
@@ -213,16 +247,18 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     // contiguous range, so the first tiles every block requests are the first tiles of the
     // tensor and the DRAM queue serves all blocks evenly (measured on GB300: bf16 8192x1280
     // backward 18.4 -> 17.8 us).  The assignment depends only on (rows, cols, device).
-    const int ntiles = (rows + kTileRows - 1) / kTileRows;
+    const int ntiles = (rows + RT - 1) / RT;
     const int G = (int)gridDim.x, b = (int)blockIdx.x;
     const int my_tiles = b < ntiles ? (ntiles - 1 - b) / G + 1 : 0;
-    auto tile_row0 = [&](int k) { return (b + k * G) * kTileRows; };  // first row of step k
+    auto tile_row0 = [&](int k) { return (b + k * G) * RT; };  // first row of step k
 
     if (tid == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kTileRows);
+            mbar_init(&empty_bar[i], NCW);
         }
+        if constexpr (W > 1)
+            for (int i = 0; i < 2 * RT; ++i) mbar_init(&xbar[i], W);
         fence_barrier_init();
     }
     __syncthreads();
@@ -243,7 +279,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
         for (int h = 0; h < H; ++h) cmpg[v][h] = cmpb[v][h] = f2_splat(0.f);
 
-    if (warp == kTileRows) {  // producer
+    if (warp == NCW) {  // producer
         if (lane == 0) {
             int k = 0;
             RingPos pos;
@@ -262,7 +298,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                     break;
                 }
                 const int r0 = tile_row0(k);
-                const unsigned bytes = (unsigned)min(kTileRows, rows - r0) * row_bytes;
+                const unsigned bytes = (unsigned)min(RT, rows - r0) * row_bytes;
                 unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
                 mbar_arrive_expect_tx(&full_bar[slot], 2u * bytes);
                 bulk_g2s(dst, dy + (size_t)r0 * cols, bytes, &full_bar[slot]);
@@ -275,9 +311,11 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
         f2 gm[VPL][H];  // gamma of this lane's columns as fp32 pairs, loaded once
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
+            const int vi = v * VSTRIDE + lane_vec;
             PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gm[v]);
         }
+        int xstep = 0;    // W > 1: rows this warp has exchanged sums for (buffer and phase)
+        bool xok = true;  // W > 1: the row's other warps announced their sums in time
         // One or two rows through both passes.  With two (the warp's row of tile k and of
         // tile k + 1), their first passes run together, their four row sums share one
         // butterfly and their second passes run together; per lane the column sums still add
@@ -291,8 +329,8 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 dys[r] = reinterpret_cast<const T*>(smem_raw + (size_t)slot_[r] * slot_bytes +
-                                                    (size_t)warp * row_bytes);
-                xs[r] = dys[r] + (size_t)kTileRows * cols;
+                                                    (size_t)wrow * row_bytes);
+                xs[r] = dys[r] + (size_t)RT * cols;
                 mu2[r] = f2_splat(mu_[r]);
                 rs2[r] = f2_splat(rs_[r]);
                 // Row sums; the low halves take the even columns, the high halves the odd.
@@ -300,7 +338,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             }
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
+                const int vi = v * VSTRIDE + lane_vec;
                 if (vi < nvec) {
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {
@@ -341,6 +379,24 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
 #pragma unroll
                 for (int r = 0; r < NR; ++r) warp_sum2(t[2 * r], t[2 * r + 1]);
             }
+            if constexpr (W > 1) {  // one row (NR = 1): add the W warps' sums in warp order
+                const int xi = (xstep & 1) * RT + wrow;
+                if (lane == 0) {
+                    xval[xi * W + wpos] = make_float2(t[0], t[1]);
+                    mbar_arrive(&xbar[xi]);
+                }
+                xok = __all_sync(kFullMask, mbar_wait(&xbar[xi], (unsigned)(xstep >> 1) & 1u, a.limit_ns));
+                ++xstep;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < W; ++j) {
+                    const float2 q = xval[xi * W + j];
+                    s0 += q.x;
+                    s1 += q.y;
+                }
+                t[0] = s0;
+                t[1] = s1;
+            }
             // dx = rs * (g - (mg + xhat * mgx)) with the same rounded g as in the sums, so
             // g - mg cancels exactly where it should (a one-column row gives dx = 0); mg = 0
             // for the RMSNorm.
@@ -352,7 +408,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
             }
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
+                const int vi = v * VSTRIDE + lane_vec;
                 if (vi < nvec) {  // second pass re-reads the rows from shared memory
 #pragma unroll
                     for (int r = 0; r < NR; ++r) {
@@ -376,14 +432,14 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
         // GB300 (bf16 8192x1280: 21.8 -> 19.9 us; fp32 262144x1000: 544 -> 507 us, there
         // even at ring depths that keep it to one row at a time); bf16 rows of 3 or fewer
         // vectors per lane measured slower with it.
-        constexpr bool kPairRows = (Io<T>::kVec == 8 && VPL >= 4) || Io<T>::kVec == 4;
+        constexpr bool kPairRows = W == 1 && ((Io<T>::kVec == 8 && VPL >= 4) || Io<T>::kVec == 4);
         const int pair_max = (kPairRows && stages >= 4) ? 2 : 1;
         // mean and rstd of the next step's rows are loaded a step ahead, so their latency is
         // not on the rows' critical path.
         auto load_stats = [&](int kk, int nr, float (&mu)[2], float (&rs)[2]) {
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int rr = tile_row0(kk + r) + warp;
+                const int rr = tile_row0(kk + r) + wrow;
                 const bool valid = r < nr && kk + r < my_tiles && rr < rows;
                 mu[r] = valid && !RMS ? a.mean[rr] : 0.f;  // the RMSNorm subtracts no mean
                 rs[r] = valid ? a.rstd[rr] : 0.f;
@@ -410,7 +466,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                 if (lane == 0) raise_status(a.status, kStatusTimeout);
                 break;
             }
-            const int rws[2] = {tile_row0(k) + warp, tile_row0(k + 1) + warp};
+            const int rws[2] = {tile_row0(k) + wrow, tile_row0(k + 1) + wrow};
             if constexpr (kPairRows) {
                 if (nr == 2 && rws[1] < rows)
                     body(std::integral_constant<int, 2>{}, rws, slots, mu, rs);
@@ -418,6 +474,10 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
                     body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
             } else if (rws[0] < rows) {
                 body(std::integral_constant<int, 1>{}, rws, slots, mu, rs);
+            }
+            if (!xok) {  // (W > 1) a warp of this row stopped: stop too, bounded
+                if (lane == 0) raise_status(a.status, kStatusTimeout);
+                break;
             }
             __syncwarp();
             if (lane == 0) {
@@ -430,21 +490,22 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     __syncthreads();  // the ring is drained and no warp reads it any more
 
     // Block partial row.  The consumer warps put their sums in shared memory as
-    // [stat][warp][cols] floats (the drained ring), followed by the negated compensations in
-    // the same layout when KAHAN; then each thread adds the 7 warps' values of a group of 4
-    // columns in warp order (with TwoSum when KAHAN) and stores the block's partials of them.
+    // [stat][row of the tile][cols] floats (the drained ring; the W warps of a row own
+    // disjoint columns), followed by the negated compensations in the same layout when
+    // KAHAN; then each thread adds the RT rows' values of a group of 4 columns in order (with
+    // TwoSum when KAHAN) and stores the block's partials of them.
     float* smem_f = reinterpret_cast<float*>(smem_raw);
-    const size_t lo_off = (size_t)2 * kTileRows * cols;
+    const size_t lo_off = (size_t)2 * RT * cols;
     auto put = [&](float* dst, f2 a0, f2 a1) {
         *reinterpret_cast<float4*>(dst) = make_float4(f2_lo(a0), f2_hi(a0), f2_lo(a1), f2_hi(a1));
     };
-    if (warp < kTileRows) {
+    if (warp < NCW) {
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-            const int vi = v * 32 + lane;
+            const int vi = v * VSTRIDE + lane_vec;
             if (vi < nvec) {
-                float* dg = smem_f + (size_t)warp * cols + (size_t)vi * V;
-                float* db = dg + (size_t)kTileRows * cols;
+                float* dg = smem_f + (size_t)wrow * cols + (size_t)vi * V;
+                float* db = dg + (size_t)RT * cols;
                 const f2 z = f2_splat(0.f);
                 if constexpr (H == 4) {
                     // A lane's 8 columns are two 16-byte halves at a 32-byte lane stride.
@@ -487,11 +548,11 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
     for (int u = tid; u < (RMS ? 1 : 2) * quarter; u += blockDim.x) {
         const int stat = u >= quarter ? 1 : 0;
         const int c = 4 * (u - stat * quarter);
-        const float* src = smem_f + (size_t)stat * kTileRows * cols + c;
+        const float* src = smem_f + (size_t)stat * RT * cols + c;
         if constexpr (KAHAN) {
             float S[4] = {0.f, 0.f, 0.f, 0.f}, C[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int w = 0; w < kTileRows; ++w) {
+            for (int w = 0; w < RT; ++w) {
                 const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
                 const float4 l = *reinterpret_cast<const float4*>(src + lo_off + (size_t)w * cols);
                 comp_add(S[0], C[0], t.x, l.x);
@@ -505,7 +566,7 @@ __global__ void __launch_bounds__(kTileThreads, tile_min_blocks<T, VPL, KAHAN>()
         } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
             f2 S01 = f2_splat(0.f), S23 = f2_splat(0.f);
 #pragma unroll
-            for (int w = 0; w < kTileRows; ++w) {
+            for (int w = 0; w < RT; ++w) {
                 const float4 t = *reinterpret_cast<const float4*>(src + (size_t)w * cols);
                 S01 = f2_add(S01, f2_make(t.x, t.y));
                 S23 = f2_add(S23, f2_make(t.z, t.w));
@@ -805,12 +866,49 @@ const void* warp_kernel_k(int vpl) {
     return nullptr;
 }
 
+// Rows wider than one warp's registers: W = 2 or 4 warps per row, 3 or 4 vectors per lane
+// (bf16 up to 4096 columns, fp32 up to 2048).
+template <typename T, bool K, bool RMS>
+const void* group_kernel_k(int vpl, int W) {
+    if constexpr (Io<T>::kVec == 8) {
+        if (W == 2) return vpl == 3 ? (const void*)bwd_tile_kernel<T, 3, K, RMS, 2>
+                         : vpl == 4 ? (const void*)bwd_tile_kernel<T, 4, K, RMS, 2> : nullptr;
+    }
+    if (W == 4) return vpl == 3 ? (const void*)bwd_tile_kernel<T, 3, K, RMS, 4>
+                     : vpl == 4 ? (const void*)bwd_tile_kernel<T, 4, K, RMS, 4> : nullptr;
+    return nullptr;
+}
+
 template <typename T, bool RMS>
-const void* warp_kernel(int vpl, bool kahan) {
+const void* warp_kernel(int vpl, bool kahan, int W) {
+    if (W > 1) {
+        if constexpr (Io<T>::kVec == 4)  // fp32 sums are always compensated
+            return kahan ? group_kernel_k<T, true, RMS>(vpl, W) : nullptr;
+        else
+            return kahan ? group_kernel_k<T, true, RMS>(vpl, W) : group_kernel_k<T, false, RMS>(vpl, W);
+    }
     return kahan ? warp_kernel_k<T, true, RMS>(vpl) : warp_kernel_k<T, false, RMS>(vpl);
 }
 
 int warp_max_vpl(Dtype dt, bool kahan) { return dt == Dtype::F32 ? 8 : (kahan ? 4 : 5); }
+
+// Warps per row of the tile kernel and vectors per lane: one warp while a lane's share of
+// the row fits its registers, else the fewest of 2 or 4 warps that bring it to at most 4
+// vectors (W = 0: the row is too wide for the tile kernel).
+void tile_shape(Dtype dt, int nvec, bool kahan, int* W, int* vpl) {
+    *W = 1;
+    *vpl = (nvec + 31) / 32;
+    if (*vpl <= warp_max_vpl(dt, kahan)) return;
+    for (int w = dt == Dtype::F32 ? 4 : 2; w <= 4; w *= 2) {
+        const int v = (nvec + 32 * w - 1) / (32 * w);
+        if (v <= 4) {
+            *W = w;
+            *vpl = v;
+            return;
+        }
+    }
+    *W = 0;
+}
 
 // Block path: cols <= 16384 and 512 threads give at most 4 vectors per thread for bf16 and
 // 8 for fp32.  Compensated (Kahan) column sums where the plan asks for them: the registers
@@ -844,8 +942,8 @@ template <bool RMS>
 const void* kernel_for(Dtype dt, const BwdPlan& p) {
     const bool f = dt == Dtype::F32;
     if (p.path == kPathWarp)
-        return f ? warp_kernel<float, RMS>(p.per_thread, p.kahan)
-                 : warp_kernel<__nv_bfloat16, RMS>(p.per_thread, p.kahan);
+        return f ? warp_kernel<float, RMS>(p.per_thread, p.kahan, p.wpr)
+                 : warp_kernel<__nv_bfloat16, RMS>(p.per_thread, p.kahan, p.wpr);
     if (p.path == kPathBlock)
         return f ? block_kernel<float, RMS>(p.per_thread, p.kahan)
                  : block_kernel<__nv_bfloat16, RMS>(p.per_thread, p.kahan);
@@ -864,18 +962,21 @@ cudaError_t plan_bwd_t(Dtype dt, int rows, int cols, bool aligned, int path_over
     p.rms = RMS;
     if (aligned && path_override != kPathScalar) {
         const int nvec = cols / V;
-        const int vpl = (nvec + 31) / 32;
         // The warp path keeps each lane's column sums over all the rows its warp handles:
         // compensated for fp32 I/O, and for bf16 once those chains can get long.
         const bool wk = dt == Dtype::F32 || rows > kWarpPathMaxRows;
-        const bool warp_fits = vpl <= warp_max_vpl(dt, wk);
+        int W, vpl;
+        tile_shape(dt, nvec, wk, &W, &vpl);
+        const bool warp_fits = W > 0;
         if (warp_fits && (path_override == kPathWarp || path_override == kPathAuto)) {
             p.path = kPathWarp;
             p.per_thread = vpl;
-            p.threads = kTileThreads;
+            p.wpr = W;
+            p.tile_rows = tile_rows_for(dt == Dtype::F32 ? 2 : 4, vpl, wk, W);
+            p.threads = (p.tile_rows * W + 1) * 32;
             p.kahan = wk;
-            const size_t slot = 2ull * kTileRows * cols * esize;  // a tile of dy and of x
-            const size_t combine = (wk ? 4ull : 2ull) * kTileRows * cols * 4;
+            const size_t slot = 2ull * p.tile_rows * cols * esize;  // a tile of dy and of x
+            const size_t combine = (wk ? 4ull : 2ull) * p.tile_rows * cols * 4;
             // About four tiles in flight per SM, split over the blocks the registers allow
             // on an SM, within each block's share of its shared memory.  Measured on GB300:
             // deeper rings request a block's whole share of rows at once, the DRAM queue then
@@ -891,7 +992,7 @@ cudaError_t plan_bwd_t(Dtype dt, int rows, int cols, bool aligned, int path_over
             stages = std::max(2, stages);
             p.stages = stages;
             // The ring, reused afterwards for the warps' sums.
-            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)kTileThreads * 32});
+            p.smem = std::max<size_t>({(size_t)stages * slot, combine, (size_t)p.threads * 32});
         } else {
             p.path = kPathBlock;
             p.per_thread = (nvec + kBwdBlockMaxThreads - 1) / kBwdBlockMaxThreads;
@@ -934,7 +1035,7 @@ cudaError_t plan_bwd_t(Dtype dt, int rows, int cols, bool aligned, int path_over
     if (e != cudaSuccess) return e;
     const int occ = blocks_per_sm(kern, p.threads, p.smem);
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int need = p.path == kPathWarp ? (rows + kTileRows - 1) / kTileRows : rows;
+    const int need = p.path == kPathWarp ? (rows + p.tile_rows - 1) / p.tile_rows : rows;
     p.grid = std::max(1, std::min(need, di.sms * occ));
     *plan = p;
     return cudaSuccess;

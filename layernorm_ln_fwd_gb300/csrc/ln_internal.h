@@ -82,6 +82,8 @@ struct BwdPlan {
     bool rms = false;     // the RMSNorm backward (one row sum, one column sum: dgamma)
     int path = kPathAuto;
     int per_thread = 0;   // vectors per lane (warp path) or per thread (block path)
+    int wpr = 1;          // warp path: warps per row
+    int tile_rows = 0;    // warp path: rows per tile
     int threads = 0;
     int grid = 0;
     bool kahan = false;   // compensated per-thread column sums (block path)

@@ -107,7 +107,9 @@ def test_constant_zero_and_outlier_rows(dtype, path):
 
 
 @pytest.mark.parametrize("dtype,rows,cols", [("bf16", 8192, 768), ("bf16", 8192, 1280),
-                                             ("f32", 4096, 1000), ("bf16", 4096, 8192)])
+                                             ("f32", 4096, 1000), ("bf16", 4096, 8192),
+                                             ("bf16", 2503, 1600), ("bf16", 2503, 2560),
+                                             ("bf16", 2503, 4096), ("f32", 2503, 1600)])
 def test_full_size_every_row_and_bitwise_repeatable(dtype, rows, cols):
     inp = synth.make_inputs(rows, cols, dtype, seed=0)
     gpu = run_gpu(inp)
