@@ -866,16 +866,23 @@ const void* warp_kernel_k(int vpl) {
     return nullptr;
 }
 
-// Rows wider than one warp's registers: W = 2 or 4 warps per row, 3 or 4 vectors per lane
-// (bf16 up to 4096 columns, fp32 up to 2048).
+// Rows wider than one warp's registers: W = 4 warps per row with 3 or 4 vectors per lane,
+// or W = 2 with 3 or 4 (bf16) or 5 (compensated sums) -- the shapes tile_shape picks from.
 template <typename T, bool K, bool RMS>
 const void* group_kernel_k(int vpl, int W) {
-    if constexpr (Io<T>::kVec == 8) {
-        if (W == 2) return vpl == 3 ? (const void*)bwd_tile_kernel<T, 3, K, RMS, 2>
-                         : vpl == 4 ? (const void*)bwd_tile_kernel<T, 4, K, RMS, 2> : nullptr;
+    if (W == 2) {
+        if constexpr (K) {
+            if (vpl == 5) return (const void*)bwd_tile_kernel<T, 5, K, RMS, 2>;
+        }
+        if constexpr (Io<T>::kVec == 8) {
+            if (vpl == 3) return (const void*)bwd_tile_kernel<T, 3, K, RMS, 2>;
+            if (vpl == 4) return (const void*)bwd_tile_kernel<T, 4, K, RMS, 2>;
+        }
     }
-    if (W == 4) return vpl == 3 ? (const void*)bwd_tile_kernel<T, 3, K, RMS, 4>
-                     : vpl == 4 ? (const void*)bwd_tile_kernel<T, 4, K, RMS, 4> : nullptr;
+    if constexpr (!K || Io<T>::kVec == 4) {  // (bf16 compensated: one row per tile; not used)
+        if (W == 4) return vpl == 3 ? (const void*)bwd_tile_kernel<T, 3, K, RMS, 4>
+                         : vpl == 4 ? (const void*)bwd_tile_kernel<T, 4, K, RMS, 4> : nullptr;
+    }
     return nullptr;
 }
 
@@ -893,21 +900,32 @@ const void* warp_kernel(int vpl, bool kahan, int W) {
 int warp_max_vpl(Dtype dt, bool kahan) { return dt == Dtype::F32 ? 8 : (kahan ? 4 : 5); }
 
 // Warps per row of the tile kernel and vectors per lane: one warp while a lane's share of
-// the row fits its registers, else the fewest of 2 or 4 warps that bring it to at most 4
-// vectors (W = 0: the row is too wide for the tile kernel).
+// the row fits its registers; else, of 2 warps (3 to 5 vectors per lane) and 4 warps (3 or
+// 4), the one that keeps the most rows of a tile in flight, then the one with more warps
+// (W = 0: the row is too wide, or only one row per tile would fit: the block-per-row kernel
+// is used).  Measured on GB300: bf16 8192 x 2560 2 x 5 / 4 x 3 (3 rows per tile each):
+// 34.3 / 31.7 us; fp32 8192 x 1280 2 x 5 (5 rows) / 4 x 3 (3 rows): 26.1 / 28.6 us; bf16
+// 65600 x 2560, compensated sums: 2 x 5 (3 rows) / 4 x 3 (1 row): 281 / 438 us.
 void tile_shape(Dtype dt, int nvec, bool kahan, int* W, int* vpl) {
     *W = 1;
     *vpl = (nvec + 31) / 32;
     if (*vpl <= warp_max_vpl(dt, kahan)) return;
-    for (int w = dt == Dtype::F32 ? 4 : 2; w <= 4; w *= 2) {
+    const int H = dt == Dtype::F32 ? 2 : 4;
+    int best_w = 0, best_v = 0, best_rt = 1;
+    for (int w = 2; w <= 4; w *= 2) {
         const int v = (nvec + 32 * w - 1) / (32 * w);
-        if (v <= 4) {
-            *W = w;
-            *vpl = v;
-            return;
+        const bool built = w == 4 ? (v == 3 || v == 4) && !(kahan && dt != Dtype::F32)
+                                  : (v == 5 ? kahan : (v == 3 || v == 4) && dt != Dtype::F32);
+        if (!built) continue;
+        const int rt = tile_rows_for(H, v, kahan, w);
+        if (rt >= best_rt && rt > 1) {  // ties go to the larger W
+            best_w = w;
+            best_v = v;
+            best_rt = rt;
         }
     }
-    *W = 0;
+    *W = best_w;
+    *vpl = best_v;
 }
 
 // Block path: cols <= 16384 and 512 threads give at most 4 vectors per thread for bf16 and
@@ -983,12 +1001,14 @@ cudaError_t plan_bwd_t(Dtype dt, int rows, int cols, bool aligned, int path_over
             // serves blocks roughly in launch order and the late ones set the kernel's end
             // (bf16 8192x768, two blocks per SM: 5 stages 14.2 us, 2 stages 13.5 us; bf16
             // 8192x1280, one block per SM: 6 stages 18.8 us, 4 stages 18.5 us, 2 stages 19.4 us).
+            // With W > 1 warps per row, 3 tiles (bf16 8192x3072: 2 / 3 / 4 / 6 stages
+            // 34.0 / 32.6 / 33.1 / 34.8 us).
             const void* kern = kernel_for<RMS>(dt, p);
             if (!kern) return cudaErrorInvalidValue;
             const int occ_regs = std::max(1, blocks_per_sm(kern, p.threads, 0));
             const size_t share = std::min<size_t>(
                 (size_t)di.smem_optin, (size_t)di.smem_per_sm / occ_regs - 1024);
-            int stages = (int)std::min<size_t>(std::min(kMaxStages, 4 / occ_regs), share / slot);
+            int stages = (int)std::min<size_t>(std::min(kMaxStages, W > 1 ? 3 : 4 / occ_regs), share / slot);
             stages = std::max(2, stages);
             p.stages = stages;
             // The ring, reused afterwards for the warps' sums.

@@ -3,12 +3,14 @@
     python -m layernorm_ln_fwd_gb300.profile_case --workload bf16_8192x768 --iters 3
     python -m layernorm_ln_fwd_gb300.profile_case --workload f32_262144x1000 --rows 32768
     python -m layernorm_ln_fwd_gb300.profile_case --workload bdr_bf16_8192x768 --rows 65536
+    python -m layernorm_ln_fwd_gb300.profile_case --workload bf16_8192x1280 --cols 2560
 
 Workloads are the LayerNorm ones of ``synth.WORKLOADS`` and the other fused row operations
 of ``synth.OP_WORKLOADS`` (RMSNorm, softmax, cross-entropy, the bias + dropout + residual
 prologue, its mask regenerated or stored as bits), with the seeded synthetic inputs of ``synth`` (``--rows`` keeps the workload's
 width, dtype and distributions and takes fewer or more rows, for captures that must stay
-small or spill out of L2); backwards use a caller-owned workspace, as the benchmark does.
+small or spill out of L2; ``--cols`` likewise takes another width for a LayerNorm workload);
+backwards use a caller-owned workspace, as the benchmark does.
 Nothing is checked.
 """
 from __future__ import annotations
@@ -21,13 +23,13 @@ import layernorm_ln_fwd_gb300 as ln
 from layernorm_ln_fwd_gb300 import synth
 
 
-def layernorm_case(name: str, rows: int, iters: int) -> None:
+def layernorm_case(name: str, rows: int, iters: int, cols: int = 0) -> None:
     w = synth.WORKLOADS[name]
-    rows = rows or w.rows
-    inp = synth.make_inputs(rows, w.cols, w.dtype, seed=0, x=w.x, res=w.res, dy=w.dy,
+    rows, cols = rows or w.rows, cols or w.cols
+    inp = synth.make_inputs(rows, cols, w.dtype, seed=0, x=w.x, res=w.res, dy=w.dy,
                             gamma=w.gamma, beta=w.beta)
     d = {k: v.cuda() for k, v in inp.items()}
-    ws = torch.zeros(ln.workspace_bytes(rows, w.cols), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ln.workspace_bytes(rows, cols), dtype=torch.uint8, device="cuda")
     for _ in range(iters):
         out, res_out, mean, rstd = ln.fwd(d["x"], d["res"], d["gamma"], d["beta"], w.eps)
         ln.bwd(d["dy"], res_out, d["gamma"], mean, rstd, workspace=ws)
@@ -70,10 +72,14 @@ def main() -> int:
                     choices=list(synth.WORKLOADS) + list(synth.OP_WORKLOADS))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--rows", type=int, default=0, help="rows to use (default: the workload's)")
+    ap.add_argument("--cols", type=int, default=0,
+                    help="width of a LayerNorm workload (default: the workload's)")
     args = ap.parse_args()
     if args.workload in synth.WORKLOADS:
-        layernorm_case(args.workload, args.rows, args.iters)
+        layernorm_case(args.workload, args.rows, args.iters, args.cols)
     else:
+        if args.cols:
+            ap.error("--cols applies to the LayerNorm workloads")
         op_case(args.workload, args.rows, args.iters)
     torch.cuda.synchronize()
     print(f"ran {args.iters} iterations of {args.workload} ({args.rows or 'all'} rows)")

@@ -79,10 +79,10 @@ def test_every_kernel_family(dtype, path, rows, cols):
 
 # Rows wider than one warp's share of registers go to the tile kernel with 2 or 4 warps per
 # row (bf16 1288-4096 columns, fp32 1028-2048); 2503 rows give every block several tiles and
-# a ragged last tile at every rows-per-tile the plan picks (7, 5, 3, 2, 1).
+# a ragged last tile at every rows-per-tile the plan picks (7, 5, 3, 2).
 WIDE_TILE = [("bf16", 1288), ("bf16", 1536), ("bf16", 1600), ("bf16", 2048), ("bf16", 2056),
              ("bf16", 2560), ("bf16", 3072), ("bf16", 4096), ("f32", 1028), ("f32", 1280),
-             ("f32", 1600), ("f32", 2048)]
+             ("f32", 1284), ("f32", 1600), ("f32", 2048)]
 
 
 @pytest.mark.parametrize("dtype,cols", WIDE_TILE)
@@ -105,10 +105,11 @@ def test_rows_shared_by_several_warps(dtype, cols):
         assert torch.equal(db2, gpu["dbeta"])
 
 
-@pytest.mark.parametrize("cols", [2048, 3072])
+@pytest.mark.parametrize("cols", [1536, 2560, 3072])
 def test_rows_shared_by_several_warps_long_chains(cols):
-    """bf16 with more than 65536 rows: the per-lane column sums are compensated (2 and 4
-    warps per row); rows compared on a sample, dgamma/dbeta over all rows."""
+    """bf16 with more than 65536 rows: the per-lane column sums are compensated (2 warps per
+    row with 3 and 5 vectors per lane; at 3072 columns the block-per-row kernel); rows
+    compared on a sample, dgamma/dbeta over all rows."""
     rows = 65600
     inp = synth.make_inputs(rows, cols, "bf16", seed=cols)
     gpu = P.run_gpu(inp, EPS)
