@@ -48,6 +48,18 @@ namespace {
 // allocated to warps in groups of four (a 9-warp block would pay for 12).
 constexpr int kTileRows = 7;
 constexpr int kTileThreads = (kTileRows + 1) * 32;
+// Rows per tile with W > 1 warps per row (bf16, VPL vectors per lane): one block per SM of
+// as many warps as the registers allow -- a thread keeps gamma, beta, the row's values and
+// their shifted pairs (~28 registers per vector) plus ~32 -- paid for in fours.
+__host__ __device__ constexpr int fwd_tile_rows(int vpl, int W) {
+    if (W == 1) return kTileRows;
+    const int regs = 28 * vpl + 32;
+    const int warps = (65536 / (32 * ((regs + 7) / 8 * 8))) / 4 * 4;
+    return (warps - 1) / W;
+}
+__host__ __device__ constexpr int fwd_tile_threads(int vpl, int W) {
+    return (fwd_tile_rows(vpl, W) * W + 1) * 32;
+}
 constexpr int kFwdBlockMaxThreads = 512;
 constexpr int kFwdScalarThreads = 256;
 constexpr int kMaxStages = 4;
@@ -125,8 +137,8 @@ __device__ __forceinline__ void store_keep_bits(const Prologue& pro, int row, in
 // completes when its copies land; the empty barrier when all consumer warps are done.
 // The bytes in flight per SM are set by the ring, not by the registers of resident warps.
 // ---------------------------------------------------------------------------------------
-template <typename T, int VPL, bool HAS_RES, bool RMS, int PRO = 0>
-__global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
+template <typename T, int VPL, bool HAS_RES, bool RMS, int PRO = 0, int W = 1>
+__global__ void __launch_bounds__(fwd_tile_threads(VPL, W), W == 1 && VPL <= (PRO ? 3 : 4) ? 2 : 1)
     fwd_tile_kernel(const T* __restrict__ x, const T* __restrict__ res,
                     const T* __restrict__ gamma, const T* __restrict__ beta, float eps, int rows,
                     int cols, T* __restrict__ out, T* __restrict__ res_out,
@@ -134,29 +146,43 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     unsigned* status, uint64_t wait_limit_ns, Prologue pro) {
     using IO = Io<T>;
     constexpr int V = IO::kVec;
+    // RT rows per tile, W warps per row: consumer warp c normalises row c / W of every tile,
+    // its lanes taking the vectors (v * W + c % W) * 32 + lane.  With W > 1 the W warps of a
+    // row exchange their sums through xval, announced on xbar (one mbarrier per row of the
+    // tile, double-buffered by exchange parity), and add them in warp order.
+    constexpr int RT = fwd_tile_rows(VPL, W);
+    constexpr int NCW = RT * W;  // consumer warps; warp NCW is the producer
+    constexpr int VSTRIDE = 32 * W;
+    static_assert(W == 1 || PRO == 0, "the prologue runs with one warp per row");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+    __shared__ uint64_t xbar[W > 1 ? 2 * RT : 1];
+    __shared__ float2 xval[W > 1 ? 2 * RT * W : 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wrow = warp / W, wpos = warp - wrow * W;
+    const int lane_vec = wpos * 32 + lane;
     const int nvec = cols / V;
     const RowDivisor rdiv(cols);
     const unsigned row_bytes = (unsigned)cols * (unsigned)sizeof(T);
-    const unsigned tile_bytes = (unsigned)kTileRows * row_bytes;
+    const unsigned tile_bytes = (unsigned)RT * row_bytes;
     const unsigned slot_bytes = (HAS_RES ? 2u : 1u) * tile_bytes;
-    const int ntiles = (rows + kTileRows - 1) / kTileRows;
+    const int ntiles = (rows + RT - 1) / RT;
     const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(&full_bar[i], 1);
-            mbar_init(&empty_bar[i], kTileRows);
+            mbar_init(&empty_bar[i], NCW);
         }
+        if constexpr (W > 1)
+            for (int i = 0; i < 2 * RT; ++i) mbar_init(&xbar[i], W);
         fence_barrier_init();
     }
     __syncthreads();
     // Set-up done; nothing above touches global memory, so it overlaps the previous grid.
     pdl_enter();
 
-    if (warp == kTileRows) {  // producer
+    if (warp == NCW) {  // producer
         if (lane == 0) {
             int k = 0;
             RingPos pos;
@@ -167,8 +193,8 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     raise_status(status, kStatusTimeout);
                     break;
                 }
-                const int r0 = ((int)blockIdx.x + k * (int)gridDim.x) * kTileRows;
-                const unsigned bytes = (unsigned)min(kTileRows, rows - r0) * row_bytes;
+                const int r0 = ((int)blockIdx.x + k * (int)gridDim.x) * RT;
+                const unsigned bytes = (unsigned)min(RT, rows - r0) * row_bytes;
                 unsigned char* dst = smem_raw + (size_t)slot * slot_bytes;
                 mbar_arrive_expect_tx(&full_bar[slot], (HAS_RES ? 2u : 1u) * bytes);
                 bulk_g2s(dst, x + (size_t)r0 * cols, bytes, &full_bar[slot]);
@@ -187,7 +213,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
     f2 gp[VPL][H], bp[VPL][H];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
-        const int vi = v * 32 + lane;
+        const int vi = v * VSTRIDE + lane_vec;
         PR::unpack(vi < nvec ? ld_keep(gamma + (size_t)vi * V) : make_uint4(0, 0, 0, 0), gp[v]);
         if constexpr (!RMS)
             PR::unpack(vi < nvec ? ld_keep(beta + (size_t)vi * V) : make_uint4(0, 0, 0, 0), bp[v]);
@@ -196,6 +222,30 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
     const T* bptr = static_cast<const T*>(pro.bias);
     const DropoutRng& rng = pro.rng;
     const bool write_res = res_out != nullptr;
+    // W > 1: the row's W warps add their sums (a, b) in warp order; every warp gets the same
+    // bits.  `xok` turns false when a partner's sums did not arrive within the time limit.
+    int xstep = 0;
+    bool xok = true;
+    auto row_total = [&](float& a, float& b) {
+        if constexpr (W > 1) {
+            const int xi = (xstep & 1) * RT + wrow;
+            if (lane == 0) {
+                xval[xi * W + wpos] = make_float2(a, b);
+                mbar_arrive(&xbar[xi]);
+            }
+            xok = __all_sync(kFullMask, mbar_wait(&xbar[xi], (unsigned)(xstep >> 1) & 1u, wait_limit_ns)) && xok;
+            ++xstep;
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < W; ++j) {
+                const float2 q = xval[xi * W + j];
+                s0 += q.x;
+                s1 += q.y;
+            }
+            a = s0;
+            b = s1;
+        }
+    };
     RingPos pos;
     for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
         const int slot = pos.slot;
@@ -204,16 +254,16 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
             if (lane == 0) raise_status(status, kStatusTimeout);
             break;
         }
-        const int row = ((int)blockIdx.x + k * (int)gridDim.x) * kTileRows + warp;
+        const int row = ((int)blockIdx.x + k * (int)gridDim.x) * RT + wrow;
         if (row < rows) {
             const size_t base = (size_t)row * cols;
             const T* xs = reinterpret_cast<const T*>(smem_raw + (size_t)slot * slot_bytes +
-                                                     (size_t)warp * row_bytes);
-            const T* rsm = xs + (size_t)kTileRows * cols;
+                                                     (size_t)wrow * row_bytes);
+            const T* rsm = xs + (size_t)RT * cols;
             // s = x + res, rounded to the stored type (one packed add per pair for bf16), or
             // the prologue's res + keep * (x + bias) * scale; it is what gets normalised.
             auto s_vec_kb = [&](int v, unsigned& kb) {
-                const int vi = v * 32 + lane;
+                const int vi = v * VSTRIDE + lane_vec;
                 const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)vi * V);
                 if constexpr (PRO)
                     return prologue_vec<T>(xv, *reinterpret_cast<const uint4*>(rsm + (size_t)vi * V),
@@ -231,7 +281,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
             unsigned kbv[VPL];
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {
-                const int vi = v * 32 + lane;
+                const int vi = v * VSTRIDE + lane_vec;
                 kbv[v] = 0;
                 if (vi < nvec) {
                     sp[v] = s_vec_kb(v, kbv[v]);
@@ -253,19 +303,21 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
                     PR::unpack(sp[v], sv[v]);
-                    if (v * 32 + lane < nvec) {
+                    if (v * VSTRIDE + lane_vec < nvec) {
 #pragma unroll
                         for (int h = 0; h < H; ++h) q[h & 1] = f2_fma(sv[v][h], sv[v][h], q[h & 1]);
                     }
                 }
                 const f2 q2 = f2_add(q[0], q[1]);
-                const float ss = warp_sum1(f2_lo(q2) + f2_hi(q2));  // the one reduction
+                float ss = warp_sum1(f2_lo(q2) + f2_hi(q2));  // the one reduction
+                float unused = 0.f;
+                row_total(ss, unused);
                 const float r = rsqrtf(rdiv.div(ss) + eps);
-                if (lane == 0) rstd[row] = r;
+                if (lane == 0 && wpos == 0) rstd[row] = r;
                 const f2 r2 = f2_splat(r);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
-                    const int vi = v * 32 + lane;
+                    const int vi = v * VSTRIDE + lane_vec;
                     if (vi < nvec) {
                         f2 o[H];
 #pragma unroll
@@ -274,9 +326,16 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     }
                 }
             } else {
-                // Shifted sums: K = the row's first stored value (lane 0's).  The low halves
-                // of the pairs sum the even columns, the high halves the odd ones.
-                float K = __shfl_sync(kFullMask, first_value<T>(sp[0]), 0);
+                // Shifted sums: K = the row's first stored value (lane 0's; with W > 1 each
+                // warp forms it from the row in shared memory).  The low halves of the pairs
+                // sum the even columns, the high halves the odd ones.
+                float K;
+                if constexpr (W == 1) {
+                    K = __shfl_sync(kFullMask, first_value<T>(sp[0]), 0);
+                } else {
+                    const uint4 x0 = *reinterpret_cast<const uint4*>(xs);
+                    K = first_value<T>(HAS_RES ? IO::add_round(x0, *reinterpret_cast<const uint4*>(rsm)) : x0);
+                }
                 f2 d[VPL][H];
                 float md, var;
                 auto shifted_sums = [&](auto s_of, float sd_shift) {
@@ -284,7 +343,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     f2 a = f2_splat(0.f), q = f2_splat(0.f);
 #pragma unroll
                     for (int v = 0; v < VPL; ++v) {
-                        if (v * 32 + lane < nvec) {
+                        if (v * VSTRIDE + lane_vec < nvec) {
                             PR::unpack(s_of(v), d[v]);
 #pragma unroll
                             for (int h = 0; h < H; ++h) {
@@ -296,6 +355,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     }
                     float sd = f2_lo(a) + f2_hi(a), sd2 = f2_lo(q) + f2_hi(q);
                     warp_sum2(sd, sd2);
+                    row_total(sd, sd2);
                     md = rdiv.div(sd);
                     var = rdiv.div(sd2) - md * md;
                 };
@@ -307,7 +367,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     shifted_sums(s_vec, K);
                 }
                 const float rs = rsqrtf(fmaxf(var, 0.f) + eps);
-                if (lane == 0) {
+                if (lane == 0 && wpos == 0) {
                     mean[row] = K + md;
                     rstd[row] = rs;
                 }
@@ -315,7 +375,7 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                 const f2 rs2 = f2_splat(rs), nmr2 = f2_splat(-md * rs);
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) {
-                    const int vi = v * 32 + lane;
+                    const int vi = v * VSTRIDE + lane_vec;
                     if (vi < nvec) {
                         f2 o[H];
 #pragma unroll
@@ -325,6 +385,10 @@ __global__ void __launch_bounds__(kTileThreads, VPL <= (PRO ? 3 : 4) ? 2 : 1)
                     }
                 }
             }
+        }
+        if (!xok) {  // (W > 1) a warp of this row stopped: stop too, bounded
+            if (lane == 0) raise_status(status, kStatusTimeout);
+            break;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);  // this warp is done with the slot
@@ -712,15 +776,33 @@ const void* block_ptr(bool has_res) {
                        : (const void*)fwd_block_kernel<T, N, false, RMS, 0>;
 }
 
+// The forward tile kernels with W > 1 warps per row (bf16, no prologue).
+template <typename T, int VPL, int W, bool RMS>
+const void* wide_ptr(bool has_res) {
+    return has_res ? (const void*)fwd_tile_kernel<T, VPL, true, RMS, 0, W>
+                   : (const void*)fwd_tile_kernel<T, VPL, false, RMS, 0, W>;
+}
+template <typename T, bool RMS>
+const void* wide_kernel(bool has_res, int W, int vpl) {
+    if (W == 4 && vpl == 3) return wide_ptr<T, 3, 4, RMS>(has_res);
+    return nullptr;
+}
+
 template <bool RMS, int PRO, typename T>
-cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
+cudaError_t launch_warp(const FwdArgs& a, int vpl, int W, cudaStream_t stream) {
     const void* kern = nullptr;
     const bool has_res = a.res != nullptr;
+    const int rt = fwd_tile_rows(vpl, W);
+    const int threads = (rt * W + 1) * 32;
 #define LNK_FWD_TILE_CASE(N)                                                               \
     case N:                                                                                \
         kern = tile_ptr<T, N, RMS, PRO>(has_res);                                          \
         break;
-    switch (vpl) {
+    if (W > 1) {
+        if constexpr (Io<T>::kVec == 8 && PRO == 0)
+            kern = wide_kernel<T, RMS>(has_res, W, vpl);
+        if (!kern) return cudaErrorInvalidValue;
+    } else switch (vpl) {
         LNK_FWD_TILE_CASE(1)
         LNK_FWD_TILE_CASE(2)
         LNK_FWD_TILE_CASE(3)
@@ -734,7 +816,7 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     }
 #undef LNK_FWD_TILE_CASE
     const DeviceInfo& di = device_info(-1);
-    const size_t slot_bytes = (size_t)(has_res ? 2 : 1) * kTileRows * a.cols * sizeof(T);
+    const size_t slot_bytes = (size_t)(has_res ? 2 : 1) * rt * a.cols * sizeof(T);
     // Two to four tiles in flight per block, two blocks per SM when they fit.
     int stages = (int)std::min<size_t>(kMaxStages, ((size_t)di.smem_optin / 2) / slot_bytes);
     stages = std::max(2, stages);
@@ -743,8 +825,8 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    const int ntiles = (a.rows + kTileRows - 1) / kTileRows;
-    const int occ = std::max(1, blocks_per_sm(kern, kTileThreads, smem));
+    const int ntiles = (a.rows + rt - 1) / rt;
+    const int occ = std::max(1, blocks_per_sm(kern, threads, smem));
     const int grid = std::max(1, std::min(ntiles, di.sms * occ));
     const T* x = static_cast<const T*>(a.x);
     const T* res = static_cast<const T*>(a.res);
@@ -761,7 +843,7 @@ cudaError_t launch_warp(const FwdArgs& a, int vpl, cudaStream_t stream) {
     Prologue pro = a.pro;
     void* args[] = {&x,   &res,     &gamma, &beta, &eps,    &rows,   &cols,
                     &out, &res_out, &mean,  &rstd, &stages, &status, &limit, &pro};
-    return launch_kernel(kern, dim3(grid), dim3(kTileThreads), smem, stream, args, false);
+    return launch_kernel(kern, dim3(grid), dim3(threads), smem, stream, args, false);
 }
 
 template <bool RMS, int PRO, typename T>
@@ -868,6 +950,21 @@ cudaError_t launch_scalar(const FwdArgs& a, cudaStream_t stream) {
     return launch_kernel(kern, dim3(grid), dim3(kFwdScalarThreads), 0, stream, args, false);
 }
 
+// bf16 rows (no prologue) that take W > 1 warps per row: W and the vectors per lane, or W = 0.
+// bf16 rows of 2056-3072 columns: 4 warps per row keep 3 rows of a tile in flight per block,
+// where the block-per-row kernel has one per block (8192 x 2560: 32.0 -> 27.4 us, 8192 x 3072
+// 39.7 -> 32.8 us on GB300).  Narrower rows stay with one warp per row: at 8192 x 1280 one
+// warp 14.7 us, 2 warps x 3 vectors 15.0, 4 x 2 16.3; at 1600 and 2048 columns the shapes
+// with 2 or 4 warps per row were within 3 % of one warp.
+inline void fwd_wide_shape(int nvec, int* W, int* vpl) {
+    *W = 0;
+    *vpl = 0;
+    if (nvec > 256 && nvec <= 384) {
+        *W = 4;
+        *vpl = 3;
+    }
+}
+
 template <bool RMS, int PRO, typename T>
 cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t stream) {
     constexpr int V = Io<T>::kVec;
@@ -875,7 +972,10 @@ cudaError_t launch_fwd_t(const FwdArgs& a, bool aligned, int path, cudaStream_t 
     const int nvec = a.cols / V;
     const int vpl = (nvec + 31) / 32;
     if (path == kPathBlock) return launch_block<RMS, PRO, T>(a, stream);
-    if (vpl <= 8) return launch_warp<RMS, PRO, T>(a, vpl, stream);
+    int W = 0, wv = 0;
+    if (V == 8 && PRO == 0) fwd_wide_shape(nvec, &W, &wv);
+    if (W > 1) return launch_warp<RMS, PRO, T>(a, wv, W, stream);
+    if (vpl <= 8) return launch_warp<RMS, PRO, T>(a, vpl, 1, stream);
     return launch_block<RMS, PRO, T>(a, stream);
 }
 

@@ -77,9 +77,10 @@ def test_every_kernel_family(dtype, path, rows, cols):
     P.compare_all(P.run_gpu(inp, EPS), P.run_oracle(inp, EPS), dtype, conditioned=True)
 
 
-# Rows wider than one warp's share of registers go to the tile kernel with 2 or 4 warps per
-# row (bf16 1288-4096 columns, fp32 1028-2048); 2503 rows give every block several tiles and
-# a ragged last tile at every rows-per-tile the plan picks (7, 5, 3, 2).
+# Rows wider than one warp's share of registers go to the backward tile kernel with 2 or 4
+# warps per row (bf16 1288-4096 columns, fp32 1028-2048) and, at bf16 2056-3072 columns, to
+# the forward tile kernel with 4 warps per row; 2503 rows give every block several tiles and
+# a ragged last tile at every rows-per-tile the plans pick (7, 5, 3, 2).
 WIDE_TILE = [("bf16", 1288), ("bf16", 1536), ("bf16", 1600), ("bf16", 2048), ("bf16", 2056),
              ("bf16", 2560), ("bf16", 3072), ("bf16", 4096), ("f32", 1028), ("f32", 1280),
              ("f32", 1284), ("f32", 1600), ("f32", 2048)]
@@ -126,7 +127,7 @@ def test_rows_shared_by_several_warps_long_chains(cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("cols", [768, 1000, 8192])
+@pytest.mark.parametrize("cols", [768, 1000, 2560, 8192])
 def test_plain_layernorm_without_residual(dtype, cols):
     inp = synth.make_inputs(33, cols, dtype, seed=3)
     gpu = P.run_gpu(inp, EPS, has_res=False)

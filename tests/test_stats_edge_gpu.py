@@ -79,7 +79,7 @@ def _backward_on_stored(inp, has_res=True, rounding_allowance=False):
 # 32-lane vector stride (1000 fp32, 1032 bf16) and rows that need a scalar kernel (1001).
 CASES = [
     (ln.PATH_WARP, "f32", 768), (ln.PATH_WARP, "bf16", 768), (ln.PATH_WARP, "f32", 1000),
-    (ln.PATH_WARP, "bf16", 1280), (ln.PATH_WARP, "bf16", 1032),
+    (ln.PATH_WARP, "bf16", 1280), (ln.PATH_WARP, "bf16", 1032), (ln.PATH_AUTO, "bf16", 2560),
     (ln.PATH_BLOCK, "f32", 4104), (ln.PATH_BLOCK, "bf16", 8192), (ln.PATH_BLOCK, "bf16", 768),
     (ln.PATH_BLOCK, "f32", 1000),
     (ln.PATH_SCALAR, "f32", 1001), (ln.PATH_SCALAR, "bf16", 768), (ln.PATH_SCALAR, "f32", 2048),
