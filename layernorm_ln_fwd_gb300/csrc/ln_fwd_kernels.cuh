@@ -29,7 +29,9 @@
 // Three kernel families compute the same function:
 //  * warp per row (rows of at most 256 vectors of 16 bytes): tiles of 7 rows are staged in
 //    shared memory by bulk copies several tiles ahead; each warp normalises one row with
-//    128-bit reads and stores and one xor butterfly, no block barrier;
+//    128-bit reads and stores and one xor butterfly, no block barrier; bf16 rows of 257-384
+//    vectors take 4 warps per row (tiles of 3 rows), which add their sums through shared
+//    memory announced on an mbarrier;
 //  * block per row (wider rows): a persistent block streams rows into shared memory with
 //    bulk copies (cp.async.bulk, completed on an mbarrier) several rows ahead, so each row
 //    is read from HBM once; one warp butterfly plus one cross-warp exchange per row;
@@ -128,8 +130,9 @@ __device__ __forceinline__ void store_keep_bits(const Prologue& pro, int row, in
 // ---------------------------------------------------------------------------------------
 // Warp per row, fed by a bulk-copy (TMA) pipeline.
 //
-// A block has kTileRows (7) consumer warps and one producer warp.  A tile is kTileRows
-// consecutive rows -- one contiguous stretch of memory per tensor -- so the producer's lane 0
+// A block has kTileRows (7) consumer warps and one producer warp (with W > 1 warps per row:
+// RT rows of W warps each).  A tile is kTileRows (RT) consecutive rows -- one contiguous
+// stretch of memory per tensor -- so the producer's lane 0
 // fetches a whole tile of x (and of res) with one cp.async.bulk each, `stages` tiles ahead,
 // into a ring of shared-memory slots.  Each consumer warp normalises one row of the tile
 // from shared memory (128-bit reads, lane l holds vectors l, l+32, ...), writes res_out and
