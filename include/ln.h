@@ -470,9 +470,10 @@ int ln_version(void);
  * computes the same function.
  *
  * ln_debug_force_path selects the kernel family for later calls on all threads:
- * 0 = automatic (default), 1 = warp per row (128-bit vectors; falls back to automatic when
- * the row does not fit), 2 = block per row with bulk-copy (TMA) staging, 3 = scalar
- * kernels.  Returns the previous setting.
+ * 0 = automatic (default), 1 = tile kernels, one warp per row or, for rows wider than one
+ * warp's registers, 2 or 4 warps per row (128-bit vectors; falls back to automatic when the
+ * row does not fit), 2 = block per row with bulk-copy (TMA) staging, 3 = scalar kernels.
+ * Returns the previous setting.
  *
  * ln_debug_wait_test makes the finishing blocks of the next backward launches also wait for
  * a workspace word that nothing writes, with a wait limit of ``limit_us`` microseconds, so
