@@ -6,8 +6,10 @@ statistics, normalisation) and the backward (dx, dgamma, dbeta).  The headline l
 the largest workload, fp32 262144 x 1000 (the metric names no configuration); the same line
 carries every workload's forward, backward and step times under ``workloads`` (fp32 64x768,
 the GPT-2-shaped bf16 8192x768 and 8192x1280, the wide bf16 4096x8192 with mean 100, and
-the headline), and those of the other fused row operations (the fused add + RMSNorm at the
-GPT-2 shapes, the fused softmax of causal attention scores), all on seeded synthetic inputs.
+the headline), three other widths whose rows are wider than one warp's registers (bf16
+8192x1600 and 8192x2560, fp32 8192x1280; not benchmark configurations), and those of the
+other fused row operations (the fused add + RMSNorm at the GPT-2 shapes, the fused softmax
+of causal attention scores), all on seeded synthetic inputs.
 
 Metric: achieved HBM GB/s of the algorithmic bytes (and rows/s), next to the 8 TB/s HBM
 roofline and the measured copy bandwidth.  Algorithmic bytes per step:
@@ -328,7 +330,7 @@ class Workbench:
         import layernorm_ln_fwd_gb300 as ln
         from layernorm_ln_fwd_gb300 import synth
         self.ln = ln
-        self.w = w = synth.WORKLOADS[name]
+        self.w = w = synth.workload(name)
         self.name = name
         self.R, self.C, td = w.rows, w.cols, synth.torch_dtype(w.dtype)
         self.s = 4 if w.dtype == "f32" else 2
@@ -657,6 +659,10 @@ def run_ours(args):
         if name == args.workload:
             workloads[name] = head
             continue
+        other = Workbench(name, rank, stream)
+        workloads[name] = other.kernels(200, peak)
+        other.free()
+    for name in synth.EXTRA_WORKLOADS:  # other widths (rows wider than one warp)
         other = Workbench(name, rank, stream)
         workloads[name] = other.kernels(200, peak)
         other.free()

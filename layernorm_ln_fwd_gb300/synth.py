@@ -60,6 +60,26 @@ WORKLOADS = {
 # timed, in the same line).
 BENCH_WORKLOAD = "f32_262144x1000"
 
+# Other Transformer widths, timed in the benchmark's line beside the workloads above (not
+# benchmark configurations): rows wider than one warp's registers, which take the tile
+# kernels with 2 or 4 warps per row.
+EXTRA_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("bf16_8192x1600", "bf16", 8192, 1600,
+                 note="GPT-2 XL hidden size 1600: 2 warps per row in the backward"),
+        Workload("bf16_8192x2560", "bf16", 8192, 2560,
+                 note="4 warps per row in the forward and the backward"),
+        Workload("f32_8192x1280", "f32", 8192, 1280,
+                 note="fp32 rows of 1280 columns: 2 warps per row in the backward"),
+    ]
+}
+
+
+def workload(name: str) -> Workload:
+    """A workload of either table."""
+    return WORKLOADS[name] if name in WORKLOADS else EXTRA_WORKLOADS[name]
+
 
 def torch_dtype(dtype: str):
     return {"f32": torch.float32, "bf16": torch.bfloat16}[dtype]
@@ -99,7 +119,7 @@ def make_inputs(rows: int, cols: int, dtype: str, seed: int = 0, x=("normal", 0.
 
 
 def workload_inputs(name: str, seed: int = 0, device="cpu") -> dict:
-    w = WORKLOADS[name]
+    w = workload(name)
     return make_inputs(w.rows, w.cols, w.dtype, seed=seed, x=w.x, res=w.res, dy=w.dy,
                        gamma=w.gamma, beta=w.beta, device=device)
 
