@@ -277,15 +277,17 @@ def test_integer_dy_gives_exact_dbeta(dtype, rows, cols):
 SAMPLED_WORKLOADS = {"f32_262144x1000"}
 
 
-@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+@pytest.mark.parametrize("name", list(synth.WORKLOADS) + list(synth.EXTRA_WORKLOADS))
 def test_workload_full_size(name):
-    """The five workloads at full size, in the benchmark's launch configuration: every
-    output element by element (all rows; a 256-row sample of the largest), dgamma/dbeta over
-    all rows, and bitwise-repeatable results.  Every output meets the bare stated tolerance
-    (no element needs the column-sum allowance), except dgamma/dbeta of the 262144-row
-    fp32 workload, whose sums over 262144 rows the allowance covers for at most
-    MAX_COLUMNS_OVER_STATED columns."""
-    w = synth.WORKLOADS[name]
+    """The five workloads (and the benchmark's three other widths) at full size, in the
+    benchmark's launch configuration: every output element by element (all rows; a 256-row
+    sample of the largest), dgamma/dbeta over all rows, and bitwise-repeatable results.
+    Every output of the five workloads meets the bare stated tolerance (no element needs the
+    column-sum allowance), except dgamma/dbeta of the 262144-row fp32 workload, whose sums
+    over 262144 rows the allowance covers for at most MAX_COLUMNS_OVER_STATED columns; the
+    other widths are held to the rule of the multi-warp tests (a few dgamma/dbeta columns
+    that cancel to almost zero may use the allowance)."""
+    w = synth.workload(name)
     inp = synth.workload_inputs(name, seed=0)
     gpu = P.run_gpu(inp, w.eps)
     rows_idx = None
@@ -303,7 +305,8 @@ def test_workload_full_size(name):
     for k in ("dgamma", "dbeta"):
         infos.append(P.compare(k, P.to64(gpu[k]), ref_p[k], w.dtype, extra=ref_p["_colsum"][k]))
     over = {i["name"]: i["n_over_stated"] for i in infos if i["n_over_stated"]}
-    allowed = {"dgamma", "dbeta"} if name in SAMPLED_WORKLOADS else set()
+    allowed = ({"dgamma", "dbeta"} if name in SAMPLED_WORKLOADS or name in synth.EXTRA_WORKLOADS
+               else set())
     assert set(over) <= allowed, over
     # Where the allowance is used at all, only a few columns lean on it (2 of the 1000 dgamma
     # columns at 262144 rows when this was written): more means the sums got worse.
