@@ -247,9 +247,31 @@ __global__ void __launch_bounds__(kSmTileThreads, VPL <= 4 ? 2 : 1) sm_tile_kern
 
     const RowDivisor rdiv(cols);
     (void)rdiv;
+    // Forward: the mask vectors of this warp's row of step k + 1 are loaded during step k
+    // (the mask is read through the cache, and its load latency would otherwise stall every
+    // row after its tile has landed).
+    uint4 mk[BWD ? 1 : VPL];
+    auto load_mask = [&](int kk) {
+        if constexpr (!BWD) {
+            const int r = ((int)blockIdx.x + kk * (int)gridDim.x) * kSmTileRows + warp;
+            const T* mrow = M && kk < my_tiles && r < rows ? M + (size_t)(r % p.mask_rows) * cols
+                                                          : nullptr;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                mk[v] = mrow && v * 32 + lane < nvec ? ld_keep(mrow + (size_t)(v * 32 + lane) * V)
+                                                     : make_uint4(0, 0, 0, 0);
+        }
+    };
+    load_mask(0);
     RingPos pos;
     for (int k = 0; k < my_tiles; ++k, pos.next(stages)) {
         const int slot = pos.slot;
+        uint4 mcur[BWD ? 1 : VPL];
+        if constexpr (!BWD) {
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) mcur[v] = mk[v];
+            load_mask(k + 1);
+        }
         const bool ok = mbar_wait(&full_bar[slot], pos.phase, p.limit_ns);
         if (!__all_sync(kFullMask, ok)) {
             if (lane == 0) raise_status(p.status, kStatusTimeout);
@@ -290,11 +312,8 @@ __global__ void __launch_bounds__(kSmTileThreads, VPL <= 4 ? 2 : 1) sm_tile_kern
                     st_stream(out + base + (size_t)(v * 32 + lane) * V, Pairs<T>::pack(o));
                 }
             } else {
-                const T* mrow = M ? M + (size_t)(row % p.mask_rows) * cols : nullptr;
                 warp_softmax_row<T, VPL>(
-                    [&](int v) { return vec(as, v); },
-                    [&](int v) { return mrow ? ld_keep(mrow + (size_t)(v * 32 + lane) * V)
-                                             : make_uint4(0, 0, 0, 0); },
+                    [&](int v) { return vec(as, v); }, [&](int v) { return mcur[v]; },
                     valid, p.scale,
                     [&](int v, const uint4& y) { st_stream(out + base + (size_t)(v * 32 + lane) * V, y); });
             }
