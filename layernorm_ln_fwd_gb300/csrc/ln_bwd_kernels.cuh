@@ -14,7 +14,7 @@
 // near-constant values) any difference between them would be amplified into dx.
 //
 // Column sums, deterministic and without float atomics, in two stages:
-//  1. Each block owns a FIXED set of rows (every G-th row or 7-row tile; a contiguous range
+//  1. Each block owns a FIXED set of rows (every G-th row or tile of rows; a contiguous range
 //     in the scalar kernel).  While it computes dx it
 //     accumulates dy * xhat and dy for the columns its threads own and, at the end, writes
 //     one row of partial sums per statistic to the workspace: part[stat][block][col].
@@ -563,7 +563,7 @@ __global__ void __launch_bounds__(tile_threads<T, VPL, KAHAN, W>(),
             float4* dst = reinterpret_cast<float4*>(a.part + ((size_t)stat * P + blockIdx.x) * cols + c);
             st_part4(dst, S[0], C[0], S[1], C[1]);
             st_part4(dst + 1, S[2], C[2], S[3], C[3]);
-        } else {  // plain fp32 sums feeding a bf16 result: seven more additions are noise
+        } else {  // plain fp32 sums feeding a bf16 result: a few more additions are noise
             f2 S01 = f2_splat(0.f), S23 = f2_splat(0.f);
 #pragma unroll
             for (int w = 0; w < RT; ++w) {
