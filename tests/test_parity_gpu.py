@@ -1,8 +1,10 @@
 """Parity of the CUDA path (called through the C ABI) with the float64 oracle.
 
-Small shapes run the oracle on every element; the five full-size workloads compare every
-row (a sample of the 262144-row one) element by element and dgamma/dbeta over all rows, in
-the launch configuration the benchmark uses.  Tolerances are stated in ``lnparity``.
+Small shapes run the oracle on every element; the five full-size workloads (and the
+benchmark's three other widths) compare every row (a sample of the 262144-row one) element
+by element and dgamma/dbeta over all rows, in the launch configuration the benchmark uses;
+rows wider than one warp's registers (2 or 4 warps per row) are swept over thirteen widths.
+Tolerances are stated in ``lnparity``.
 """
 import os
 
